@@ -1,0 +1,772 @@
+// attn_fwd_sm103.cu -- fused attention forward for GB300 (sm_103a).
+//
+// One persistent CTA per SM walks a list of work items; an item is a pair of
+// 128-row query tiles of one (batch, head).  Warp roles:
+//
+//   warps 0-3  softmax warpgroup for query tile 0 (one thread per row)
+//   warps 4-7  softmax warpgroup for query tile 1
+//   warp  8    TMA producer: Q tiles and a ring of K / V tiles
+//   warp  9    Tensor Memory owner and MMA issuer (one elected thread)
+//
+// Per key tile j the tensor core computes S_t = Q_t K_j^T into Tensor Memory
+// (fp32), the softmax warpgroup of tile t turns S_t into P_t (bf16, written
+// back over S_t in Tensor Memory) and the tensor core accumulates
+// O_t += P_t V_j in Tensor Memory.  The two query tiles alternate so that
+// one tile's softmax overlaps the other tile's MMAs ("FlashAttention-4
+// explained", "Forward pass fixes", "Ping-pong scheduling").  The output
+// accumulator is rescaled only when the running row max grows by more than
+// a threshold ("Conditional rescaling").  The score matrix never leaves the
+// SM ("Enter Tri Dao and FlashAttention").
+//
+// Issue order on the tensor pipe per key tile j:
+//   PV_0(j), S_0(j+1), PV_1(j), S_1(j+1)
+// so each softmax warpgroup has the other tile's two MMAs to hide behind.
+// S_t(j+1) overwrites the Tensor Memory that P_t(j) occupies; it is issued
+// after PV_t(j) by the same thread and tcgen05 MMAs execute in issue order.
+//
+// Every mbarrier wait is bounded by a time budget; on expiry the kernel
+// records ATTN_ERR_TIMEOUT in the device status word, drains its own
+// in-flight copies and MMAs, frees Tensor Memory and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "attn_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace attn {
+
+namespace {
+
+// Three warpgroups: two softmax warpgroups and one producer warpgroup whose
+// warps 8 and 9 load and issue MMAs (warps 10 and 11 only hand their
+// registers to the softmax warpgroups).  384 threads launch with 168
+// registers each; the producer warpgroup drops to kRegsProducer and the
+// softmax warpgroups grow to kRegsSoftmax, which uses the same total:
+// 256 * 224 + 128 * 56 = 384 * 168.
+constexpr int kLoadWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 384;
+constexpr int kRegsSoftmax = 224;
+constexpr int kRegsProducer = 56;
+static_assert(256 * kRegsSoftmax + 128 * kRegsProducer <= kThreads * 168, "register split");
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Failure sites recorded in DeviceStatus::where.
+enum Site : int {
+  kSiteHeader = 1,
+  kSiteLoadQEmpty = 10,
+  kSiteLoadKvEmpty = 11,
+  kSiteMmaQFull = 20,
+  kSiteMmaKvFull = 21,
+  kSiteMmaPFull = 22,
+  kSiteMmaOEmpty = 23,
+  kSiteMmaDrain = 24,
+  kSiteSmxSFull = 30,
+  kSiteSmxOFull = 31,
+};
+
+template <int D>
+struct Cfg {
+  static constexpr int kHalfBytes = kTileM * 64 * 2;  // 128 rows x 64 bf16, 128-byte swizzle
+  static constexpr int kHalves = D / 64;
+  static constexpr int kTileBytes = kHalves * kHalfBytes;
+  static constexpr int kStages = (D == 128) ? 4 : 8;
+  static constexpr int kOCol = 256;  // O_t at column 256 + t * D; S_t at t * 128
+  static constexpr int kSmemQ = 0;
+  static constexpr int kSmemKV = kSmemQ + 2 * kTileBytes;
+  static constexpr int kSmemBar = kSmemKV + kStages * kTileBytes;
+  // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2]
+  //           o_full[2] o_empty[2] drain
+  static constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 2 + 2 + 2 + 1;
+  static constexpr int kSmemMisc = kSmemBar + 8 * kNumBars;
+  static constexpr int kSmemDoc = (kSmemMisc + 16 + 15) / 16 * 16;  // int sdoc[2][128]
+  static constexpr int kSmemBytes = kSmemDoc + 2 * kTileN * 4;
+  static constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
+};
+
+struct KParams {
+  CUtensorMap tmap_q;
+  CUtensorMap tmap_k;
+  CUtensorMap tmap_v;
+  __nv_bfloat16* out;
+  float* lse;
+  int B, H, H_kv, S_q, S_k, group;
+  float scale;
+  float scale_log2;  // scale * log2(e)
+  uint32_t mask_flags;
+  int window, q_offset;
+  const int32_t* doc_ids;
+  const int32_t* prefix_len;
+  const float* alibi_slopes;
+  float softcap;
+  const BlockMaskHeader* hdr;
+  const int32_t* order;
+  const int32_t* cnt;
+  const uint32_t* list;
+  int nK, nP, bm, n_entries, n_items;
+  int force_partial;
+  DeviceStatus* status;
+  float tau;
+  uint64_t budget_ns;
+};
+
+struct Ctl {
+  volatile int* abort;
+  DeviceStatus* status;
+  uint64_t budget_ns;
+};
+
+__device__ __noinline__ void report(const Ctl& c, int code, int site, int detail) {
+  if (atomicCAS(&c.status->code, 0, code) == 0) {
+    c.status->where = site;
+    c.status->block = blockIdx.x;
+    c.status->detail = detail;
+  }
+  *c.abort = 1;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false when the wait was given
+// up (timeout here, or another role already aborted).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c, int site) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (true) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*c.abort) return false;
+    if (ptx::globaltimer_ns() - t0 > c.budget_ns) {
+      report(c, ATTN_ERR_TIMEOUT, site, (int)parity);
+      return false;
+    }
+  }
+}
+
+// Item w -> (batch, head, entry).  Entries are (mask batch, query-tile pair)
+// ordered by descending work; when every entry has the same work the pairs
+// of one (batch, head) run next to each other so their K/V stay in L2.
+struct Item {
+  int b, h, e, pair;
+};
+__device__ __forceinline__ Item decode_item(const KParams& p, int w, int uniform) {
+  Item it;
+  const int nb = p.B / p.bm;  // batches sharing one mask entry
+  int b_local;
+  if (uniform) {
+    it.e = w % p.n_entries;
+    int rest = w / p.n_entries;
+    b_local = rest / p.H;
+    it.h = rest % p.H;
+  } else {
+    const int nbh = nb * p.H;
+    int r = w / nbh;
+    int rem = w % nbh;
+    it.e = p.order[r];
+    b_local = rem / p.H;
+    it.h = rem % p.H;
+  }
+  const int bb = it.e / p.nP;
+  it.pair = it.e % p.nP;
+  it.b = (p.bm == 1) ? b_local : bb;
+  return it;
+}
+
+// Static snake schedule over the items: round r gives CTA c item
+// r*G + c (even r) or r*G + G-1-c (odd r).
+__device__ __forceinline__ int item_of(int r) {
+  const int G = gridDim.x, c = blockIdx.x;
+  return r * G + ((r & 1) ? (G - 1 - c) : c);
+}
+
+template <int D>
+__device__ __forceinline__ void issue_s(uint32_t tmem_s, uint32_t q_base, uint32_t k_base) {
+  constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTileM, kTileN, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint32_t off = (uint32_t)((kk / 4) * Cfg<D>::kHalfBytes + (kk % 4) * 32);
+    const uint64_t a = ptx::smem_desc_sw128(q_base + off, 16, 1024);
+    const uint64_t b = ptx::smem_desc_sw128(k_base + off, 16, 1024);
+    ptx::mma_ss(tmem_s, a, b, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_base,
+                                         bool accumulate) {
+  constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTileM, D, true);
+#pragma unroll
+  for (int kk = 0; kk < kTileN / 16; ++kk) {
+    // 16 keys per MMA: 16 rows of V (2 KB of the swizzled tile), 8 packed
+    // bf16 columns of P.
+    const uint64_t b =
+        ptx::smem_desc_sw128(v_base + (uint32_t)(kk * 16 * 128), Cfg<D>::kHalfBytes, 1024);
+    ptx::mma_ts(tmem_o, tmem_p + (uint32_t)(kk * 8), b, idesc, (accumulate || kk > 0) ? 1u : 0u);
+  }
+}
+
+template <int D, bool ALIBI, bool SOFTCAP>
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ KParams p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_addr(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- block-mask consistency (uniform across the CTA) -------------------
+  const BlockMaskHeader* hdr = p.hdr;
+  const bool hdr_ok = hdr->magic == kBlockMaskMagic && hdr->version == kBlockMaskVersion &&
+                      hdr->B == p.B && hdr->S_q == p.S_q && hdr->S_k == p.S_k &&
+                      hdr->mask_flags == p.mask_flags && hdr->nP == p.nP && hdr->bm == p.bm &&
+                      hdr->nK == p.nK &&
+                      (!(p.mask_flags & ATTN_MASK_WINDOW) || hdr->window == p.window) &&
+                      hdr->q_offset == p.q_offset &&
+                      hdr->doc_ptr == reinterpret_cast<uint64_t>(p.doc_ids) &&
+                      hdr->prefix_ptr == reinterpret_cast<uint64_t>(p.prefix_len);
+  if (!hdr_ok) {
+    if (threadIdx.x == 0 && atomicCAS(&p.status->code, 0, ATTN_ERR_DEVICE_CHECK) == 0) {
+      p.status->where = kSiteHeader;
+      p.status->block = blockIdx.x;
+      p.status->detail = 0;
+    }
+    return;
+  }
+  const int uniform = hdr->uniform;
+
+  // ---- shared memory map ------------------------------------------------
+  auto bar = [&](int i) { return sbase + (uint32_t)(C::kSmemBar + 8 * i); };
+  const int B_QF = 0, B_QE = 2, B_KVF = 4, B_KVE = 4 + C::kStages, B_SF = 4 + 2 * C::kStages,
+            B_PF = B_SF + 2, B_OF = B_PF + 2, B_OE = B_OF + 2, B_DRAIN = B_OE + 2;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kSmemMisc);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kSmemMisc + 4);
+  int* s_doc = reinterpret_cast<int*>(smem + C::kSmemDoc);
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(B_QF + 0), 1);
+    ptx::mbar_init(bar(B_QF + 1), 1);
+    ptx::mbar_init(bar(B_QE + 0), 1);
+    ptx::mbar_init(bar(B_QE + 1), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      ptx::mbar_init(bar(B_KVF + s), 1);
+      ptx::mbar_init(bar(B_KVE + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      ptx::mbar_init(bar(B_SF + t), 1);
+      ptx::mbar_init(bar(B_PF + t), 4);  // one arrival per softmax warp
+      ptx::mbar_init(bar(B_OF + t), 1);
+      ptx::mbar_init(bar(B_OE + t), 4);
+    }
+    ptx::mbar_init(bar(B_DRAIN), 1);
+    *s_abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_addr(s_tmem), kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  Ctl ctl{s_abort, p.status, p.budget_ns};
+
+  if (warp >= 8) {
+    // Producer warpgroup: give registers away first (whole warpgroup).
+    ptx::setmaxnreg_dec<kRegsProducer>();
+    if (warp == kLoadWarp && lane == 0) {
+      // ===================== TMA producer ================================
+
+      ptx::prefetch_tmap(&p.tmap_q);
+      ptx::prefetch_tmap(&p.tmap_k);
+      ptx::prefetch_tmap(&p.tmap_v);
+      const uint64_t pol_kv = ptx::policy_evict_last();
+      const uint64_t pol_q = ptx::policy_evict_first();
+      uint32_t kv_cnt = 0;
+      int act = 0;
+      bool ok = true;
+      int q_phase[2] = {-1, -1};  // parity of the last Q_t load issued
+      for (int r = 0; ok; ++r) {
+        const int w = item_of(r);
+        if (w >= p.n_items) break;
+        const Item it = decode_item(p, w, uniform);
+        const int n = p.cnt[it.e];
+        if (n == 0) continue;
+        const uint32_t* lst = p.list + (size_t)it.e * p.nK;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (act > 0) ok = wait_bar(bar(B_QE + t), (act - 1) & 1, ctl, kSiteLoadQEmpty);
+          if (!ok) break;
+          const int row0 = (2 * it.pair + t) * kTileM;
+          ptx::mbar_arrive_expect_tx(bar(B_QF + t), C::kTileBytes);
+#pragma unroll
+          for (int hx = 0; hx < C::kHalves; ++hx)
+            ptx::tma_load_3d(sbase + C::kSmemQ + t * C::kTileBytes + hx * C::kHalfBytes,
+                             &p.tmap_q, bar(B_QF + t), hx * 64, row0, it.b * p.H + it.h, pol_q);
+          q_phase[t] = act & 1;
+        }
+        const int kvz = it.b * p.H_kv + it.h / p.group;
+        for (int j = 0; j < n && ok; ++j) {
+          const int row0 = (int)entry_tile(lst[j]) * kTileN;
+          for (int which = 0; which < 2; ++which) {
+            const int st = (int)(kv_cnt % C::kStages);
+            if (kv_cnt >= (uint32_t)C::kStages) {
+              ok = wait_bar(bar(B_KVE + st), ((kv_cnt / C::kStages) - 1) & 1, ctl,
+                            kSiteLoadKvEmpty);
+              if (!ok) break;
+            }
+            ptx::mbar_arrive_expect_tx(bar(B_KVF + st), C::kTileBytes);
+            const CUtensorMap* map = which == 0 ? &p.tmap_k : &p.tmap_v;
+#pragma unroll
+            for (int hx = 0; hx < C::kHalves; ++hx)
+              ptx::tma_load_3d(sbase + C::kSmemKV + st * C::kTileBytes + hx * C::kHalfBytes, map,
+                               bar(B_KVF + st), hx * 64, row0, kvz, pol_kv);
+            ++kv_cnt;
+          }
+        }
+        ++act;
+      }
+      if (!ok) {
+        // Let the copies already issued land before the CTA exits: wait (with
+        // a bound) for the last phase issued on every barrier still in use.
+        const uint32_t first = kv_cnt > (uint32_t)C::kStages ? kv_cnt - C::kStages : 0;
+        for (uint32_t c = first; c < kv_cnt; ++c) {
+          const uint64_t t0 = ptx::globaltimer_ns();
+          while (!ptx::mbar_try_wait(bar(B_KVF + (int)(c % C::kStages)), (c / C::kStages) & 1) &&
+                 ptx::globaltimer_ns() - t0 < ctl.budget_ns) {
+          }
+        }
+        for (int t = 0; t < 2; ++t) {
+          if (q_phase[t] < 0) continue;
+          const uint64_t t0 = ptx::globaltimer_ns();
+          while (!ptx::mbar_try_wait(bar(B_QF + t), (uint32_t)q_phase[t]) &&
+                 ptx::globaltimer_ns() - t0 < ctl.budget_ns) {
+          }
+        }
+      }
+    } else if (warp == kMmaWarp && lane == 0) {
+      // ===================== MMA issuer ==================================
+      auto tS = [&](int t) { return tmem + (uint32_t)(t * kTileN); };
+      auto tO = [&](int t) { return tmem + (uint32_t)(C::kOCol + t * D); };
+      auto sQ = [&](int t) { return sbase + (uint32_t)(C::kSmemQ + t * C::kTileBytes); };
+      auto sKV = [&](uint32_t idx) {
+        return sbase + (uint32_t)C::kSmemKV + (idx % C::kStages) * (uint32_t)C::kTileBytes;
+      };
+      auto kv_full = [&](uint32_t idx) { return bar(B_KVF + (int)(idx % C::kStages)); };
+      auto kv_empty = [&](uint32_t idx) { return bar(B_KVE + (int)(idx % C::kStages)); };
+      auto kv_par = [&](uint32_t idx) { return (idx / C::kStages) & 1; };
+      uint32_t kv_cnt = 0;
+      uint32_t p_cnt[2] = {0, 0};
+      int act = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int w = item_of(r);
+        if (w >= p.n_items) break;
+        const Item it = decode_item(p, w, uniform);
+        const int n = p.cnt[it.e];
+        if (n == 0) continue;
+        // S_t(0) for both tiles from K_0.
+        const uint32_t k0 = kv_cnt;
+        ok = wait_bar(kv_full(k0), kv_par(k0), ctl, kSiteMmaKvFull);
+        for (int t = 0; t < 2 && ok; ++t) {
+          ok = wait_bar(bar(B_QF + t), act & 1, ctl, kSiteMmaQFull);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          issue_s<D>(tS(t), sQ(t), sKV(k0));
+          ptx::mma_commit(bar(B_SF + t));
+          if (n == 1) ptx::mma_commit(bar(B_QE + t));
+        }
+        if (!ok) break;
+        ptx::mma_commit(kv_empty(k0));
+        for (int j = 0; j < n && ok; ++j) {
+          const uint32_t vi = k0 + 2 * j + 1;  // V_j
+          const uint32_t ki = k0 + 2 * j + 2;  // K_{j+1}
+          const bool has_next = (j + 1 < n);
+          ok = wait_bar(kv_full(vi), kv_par(vi), ctl, kSiteMmaKvFull);
+          for (int t = 0; t < 2 && ok; ++t) {
+            ok = wait_bar(bar(B_PF + t), p_cnt[t] & 1, ctl, kSiteMmaPFull);
+            if (!ok) break;
+            ++p_cnt[t];
+            if (j == 0 && act > 0) {
+              ok = wait_bar(bar(B_OE + t), (act - 1) & 1, ctl, kSiteMmaOEmpty);
+              if (!ok) break;
+            }
+            ptx::tc_fence_after();
+            issue_pv<D>(tO(t), tS(t), sKV(vi), j > 0);
+            if (t == 1) ptx::mma_commit(kv_empty(vi));
+            if (has_next) {
+              if (t == 0) {
+                ok = wait_bar(kv_full(ki), kv_par(ki), ctl, kSiteMmaKvFull);
+                if (!ok) break;
+              }
+              issue_s<D>(tS(t), sQ(t), sKV(ki));
+              ptx::mma_commit(bar(B_SF + t));
+              if (j + 2 == n) ptx::mma_commit(bar(B_QE + t));
+              if (t == 1) ptx::mma_commit(kv_empty(ki));
+            } else {
+              ptx::mma_commit(bar(B_OF + t));
+            }
+          }
+        }
+        kv_cnt = k0 + 2 * (uint32_t)n;
+        ++act;
+      }
+      // Wait for every MMA this thread issued before Tensor Memory is freed.
+      ptx::mma_commit(bar(B_DRAIN));
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (!ptx::mbar_try_wait(bar(B_DRAIN), 0)) {
+        if (ptx::globaltimer_ns() - t0 > p.budget_ns) {
+          report(ctl, ATTN_ERR_TIMEOUT, kSiteMmaDrain, 0);
+          break;
+        }
+      }
+    }
+  } else {
+    ptx::setmaxnreg_inc<kRegsSoftmax>();
+    // ===================== softmax warpgroups ============================
+    const int t = warp >> 2;          // query tile of this warpgroup
+    const int wq = warp & 3;          // lane quarter of Tensor Memory
+    const int row = wq * 32 + lane;   // row within the query tile
+    const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+    const uint32_t tS = lane_base + (uint32_t)(t * kTileN);
+    const uint32_t tO = lane_base + (uint32_t)(C::kOCol + t * D);
+    int* sdoc = s_doc + t * kTileN;
+    const float tau = p.tau;
+    uint32_t s_cnt = 0;
+    int act = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int w = item_of(r);
+      if (w >= p.n_items) break;
+      const Item it = decode_item(p, w, uniform);
+      const int n = p.cnt[it.e];
+      const int i = (2 * it.pair + t) * kTileM + row;  // query row
+      const bool valid = i < p.S_q;
+      const size_t row_id = ((size_t)it.b * p.H + it.h) * (size_t)p.S_q + (size_t)i;
+      __nv_bfloat16* orow = p.out + row_id * D;
+      if (n == 0) {
+        if (valid) {
+          uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(orow)[c] = z;
+          if (p.lse) p.lse[row_id] = -INFINITY;
+        }
+        continue;
+      }
+      const uint32_t* lst = p.list + (size_t)it.e * p.nK;
+
+      // Row constants.
+      const int qpos = i + p.q_offset;
+      int lo = 0, hi = p.S_k - 1;
+      if (p.mask_flags & ATTN_MASK_CAUSAL) hi = min(hi, qpos);
+      if (p.mask_flags & ATTN_MASK_WINDOW) {
+        lo = max(lo, qpos - p.window + 1);
+        hi = min(hi, qpos);
+      }
+      if (p.mask_flags & ATTN_MASK_PREFIX_LM) hi = min(hi, max(qpos, p.prefix_len[it.b] - 1));
+      const bool has_doc = (p.mask_flags & ATTN_MASK_DOCUMENT) != 0;
+      const int* doc_b = has_doc ? p.doc_ids + (size_t)it.b * p.S_k : nullptr;
+      const int doc_i = (has_doc && valid) ? doc_b[i] : 0;
+      float slope2 = 0.f;  // ALiBi slope in the units of the transformed score
+      if constexpr (ALIBI) {
+        float m = p.alibi_slopes ? p.alibi_slopes[it.h]
+                                 : exp2f(-8.0f * (float)(it.h + 1) / (float)p.H);
+        slope2 = SOFTCAP ? m * (2.0f * kLog2e / p.softcap) : m * kLog2e;
+      }
+      // Score transform coefficients.
+      //   plain:   t = s * scale * log2(e)             (folded into the exp)
+      //   ALiBi:   t = s * scale * log2(e) + slope2 * (j - qpos)
+      //   softcap: y = (s * scale + bias) * 2 log2(e) / cap,
+      //            t = cap log2(e) * (1 - 2 / (2^y + 1))
+      const float sc = SOFTCAP ? p.scale * (2.0f * kLog2e / p.softcap) : p.scale_log2;
+      const float capl2 = p.softcap * kLog2e;
+
+      float m_ref = -INFINITY;  // reference max, log2 units
+      float l = 0.f;            // running sum of 2^(t - m_ref)
+
+      for (int j = 0; j < n && ok; ++j) {
+        const uint32_t entry = lst[j];
+        const int kt = (int)entry_tile(entry);
+        const uint32_t cls = entry_cls(entry, t);
+        const int j0 = kt * kTileN;
+        bool got = wait_bar(bar(B_SF + t), s_cnt & 1, ctl, kSiteSmxSFull);
+        ok = __all_sync(0xffffffffu, got);
+        if (!ok) break;
+        ++s_cnt;
+        ptx::tc_fence_after();
+        // Doc ids of this key tile into shared memory (whole warpgroup).  S_t(j)
+        // is issued only after all four warps released P_t(j-1), so no warp is
+        // still reading the previous tile's ids.
+        if (has_doc && cls == kPartial) {
+          const int jj = j0 + row;
+          sdoc[row] = (jj < p.S_k) ? doc_b[jj] : INT32_MIN;
+          ptx::named_bar_sync(1 + t, 128);
+        }
+
+        if (cls == kEmpty) {
+          uint32_t z[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) z[c] = 0u;
+          ptx::tmem_st32(tS, z);
+          ptx::tmem_st32(tS + 32, z);
+          ptx::tmem_wait_st();
+        } else {
+          float tv[kTileN];
+          {
+            uint32_t raw[32];
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+              ptx::tmem_ld32(tS + (uint32_t)(c4 * 32), raw);
+              ptx::tmem_wait_ld();
+#pragma unroll
+              for (int c = 0; c < 32; ++c) tv[c4 * 32 + c] = __uint_as_float(raw[c]);
+            }
+          }
+          // score mods
+          if constexpr (ALIBI || SOFTCAP) {
+            const float b0 = ALIBI ? slope2 * (float)(j0 - qpos) : 0.f;
+#pragma unroll
+            for (int c = 0; c < kTileN; ++c) {
+              const float bias = ALIBI ? fmaf(slope2, (float)c, b0) : 0.f;
+              float x = fmaf(tv[c], sc, bias);
+              if constexpr (SOFTCAP) {
+                const float e = ptx::ex2_approx(x);
+                x = fmaf(-2.0f * capl2, ptx::rcp_approx(e + 1.0f), capl2);
+              }
+              tv[c] = x;
+            }
+          }
+          // mask (partial tiles only)
+          if (cls == kPartial) {
+            const int clo = lo - j0, chi = hi - j0;
+            if (has_doc) {
+#pragma unroll
+              for (int c = 0; c < kTileN; ++c) {
+                const bool vis = (c >= clo) & (c <= chi) & (sdoc[c] == doc_i);
+                tv[c] = vis ? tv[c] : -INFINITY;
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < kTileN; ++c) {
+                const bool vis = (c >= clo) & (c <= chi);
+                tv[c] = vis ? tv[c] : -INFINITY;
+              }
+            }
+          }
+          // row max
+          float mx0 = tv[0], mx1 = tv[1], mx2 = tv[2], mx3 = tv[3];
+#pragma unroll
+          for (int c = 4; c < kTileN; c += 4) {
+            mx0 = fmaxf(mx0, tv[c]);
+            mx1 = fmaxf(mx1, tv[c + 1]);
+            mx2 = fmaxf(mx2, tv[c + 2]);
+            mx3 = fmaxf(mx3, tv[c + 3]);
+          }
+          float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+          constexpr bool kPlain = !ALIBI && !SOFTCAP;
+          const float xs = kPlain ? p.scale_log2 : 1.0f;  // raw scores still need the scale
+          mx = kPlain ? mx * xs : mx;
+          // conditional rescale
+          const float m_new = fmaxf(m_ref, mx);
+          const bool need = m_new > m_ref + tau;
+          const bool had = m_ref != -INFINITY;
+          float factor = 1.0f;
+          if (need) {
+            factor = ptx::ex2_approx(m_ref - m_new);
+            l *= factor;
+            m_ref = m_new;
+          }
+          const bool resc = need && had;
+          if (__any_sync(0xffffffffu, resc)) {
+            const float f = resc ? factor : 1.0f;
+#pragma unroll
+            for (int c4 = 0; c4 < D / 32; ++c4) {
+              uint32_t o[32];
+              ptx::tmem_ld32(tO + (uint32_t)(c4 * 32), o);
+              ptx::tmem_wait_ld();
+#pragma unroll
+              for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
+              ptx::tmem_st32(tO + (uint32_t)(c4 * 32), o);
+            }
+          }
+          const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+          // exponentials, row sum, bf16 P written over S
+          float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              const float pa = ptx::ex2_approx(fmaf(tv[h2 * 64 + 2 * c], xs, -m_use));
+              const float pb = ptx::ex2_approx(fmaf(tv[h2 * 64 + 2 * c + 1], xs, -m_use));
+              l0 += pa;
+              l1 += pb;
+              pk[c] = ptx::pack_bf16x2(pa, pb);
+            }
+            ptx::tmem_st32(tS + (uint32_t)(h2 * 32), pk);
+          }
+          l += l0 + l1;
+          ptx::tmem_wait_st();
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(B_PF + t));
+      }
+      if (!ok) break;
+
+      // ---- epilogue: O / l -> bf16, LSE --------------------------------
+      {
+        bool got = wait_bar(bar(B_OF + t), act & 1, ctl, kSiteSmxOFull);
+        ok = __all_sync(0xffffffffu, got);
+        if (!ok) break;
+      }
+      ptx::tc_fence_after();
+      const float inv_l = (l > 0.f) ? 1.0f / l : 0.f;
+#pragma unroll
+      for (int c4 = 0; c4 < D / 32; ++c4) {
+        uint32_t o[32];
+        ptx::tmem_ld32(tO + (uint32_t)(c4 * 32), o);
+        ptx::tmem_wait_ld();
+        if (valid) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            pk[c] = ptx::pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
+                                     __uint_as_float(o[2 * c + 1]) * inv_l);
+          uint4* dst = reinterpret_cast<uint4*>(orow + c4 * 32);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(B_OE + t));
+      if (valid && p.lse) p.lse[row_id] = (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+      ++act;
+    }
+  }
+
+  // ---- teardown --------------------------------------------------------
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host ----
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// [rows_outer][S][D] bf16 viewed as 3-D (D, S, rows_outer); box 64 x 128 x 1
+// with 128-byte swizzle.  Rows beyond S read as zero.
+bool make_map(CUtensorMap* map, const void* ptr, int D, int S, int outer) {
+  EncodeTiledFn enc = get_encode_tiled();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)outer};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * (cuuint64_t)D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)kTileM, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int D, bool ALIBI, bool SOFTCAP>
+cudaError_t launch_variant(const KParams& kp, int grid, cudaStream_t stream) {
+  auto kern = attn_fwd_kernel<D, ALIBI, SOFTCAP>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         Cfg<D>::kSmemAlloc);
+  if (err != cudaSuccess) return err;
+  kern<<<grid, kThreads, Cfg<D>::kSmemAlloc, stream>>>(kp);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const KParams& kp, bool alibi, bool softcap, int grid, cudaStream_t s) {
+  if (alibi && softcap) return launch_variant<D, true, true>(kp, grid, s);
+  if (alibi) return launch_variant<D, true, false>(kp, grid, s);
+  if (softcap) return launch_variant<D, false, true>(kp, grid, s);
+  return launch_variant<D, false, false>(kp, grid, s);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
+  KParams kp;
+  memset(&kp, 0, sizeof(kp));
+  if (!make_map(&kp.tmap_q, a.q, a.D, a.S_q, a.B * a.H) ||
+      !make_map(&kp.tmap_k, a.k, a.D, a.S_k, a.B * a.H_kv) ||
+      !make_map(&kp.tmap_v, a.v, a.D, a.S_k, a.B * a.H_kv))
+    return cudaErrorInvalidValue;
+  BlockMaskGeom g = block_mask_geom(a.B, a.S_q, a.S_k, a.mask.flags);
+  kp.out = reinterpret_cast<__nv_bfloat16*>(a.out);
+  kp.lse = a.lse;
+  kp.B = a.B;
+  kp.H = a.H;
+  kp.H_kv = a.H_kv;
+  kp.S_q = a.S_q;
+  kp.S_k = a.S_k;
+  kp.group = a.H / a.H_kv;
+  kp.scale = a.scale;
+  kp.scale_log2 = a.scale * kLog2e;
+  kp.mask_flags = a.mask.flags;
+  kp.window = a.mask.window;
+  kp.q_offset = a.mask.q_offset;
+  kp.doc_ids = a.mask.doc_ids;
+  kp.prefix_len = a.mask.prefix_len;
+  kp.alibi_slopes = a.alibi_slopes;
+  kp.softcap = (a.score_flags & ATTN_SCORE_SOFTCAP) ? a.softcap : 0.f;
+  const char* base = reinterpret_cast<const char*>(a.block_mask);
+  kp.hdr = reinterpret_cast<const BlockMaskHeader*>(base);
+  kp.order = reinterpret_cast<const int32_t*>(base + g.order_off);
+  kp.cnt = reinterpret_cast<const int32_t*>(base + g.cnt_off);
+  kp.list = reinterpret_cast<const uint32_t*>(base + g.list_off);
+  kp.nK = g.nK;
+  kp.nP = g.nP;
+  kp.bm = g.bm;
+  kp.n_entries = g.n_entries;
+  kp.n_items = g.n_entries * (a.B / g.bm) * a.H;
+  kp.status = a.status;
+  kp.tau = a.rescale_threshold;
+  kp.budget_ns = (uint64_t)(a.wait_budget_ms * 1.0e6);
+
+  int dev = 0, sms = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  int grid = a.num_ctas > 0 ? a.num_ctas : sms;
+  if (grid > kp.n_items) grid = kp.n_items;
+  if (grid < 1) grid = 1;
+
+  const bool alibi = (a.score_flags & ATTN_SCORE_ALIBI) != 0;
+  const bool softcap = (a.score_flags & ATTN_SCORE_SOFTCAP) != 0;
+  if (a.D == 128) return launch_d<128>(kp, alibi, softcap, grid, stream);
+  if (a.D == 64) return launch_d<64>(kp, alibi, softcap, grid, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

@@ -1,0 +1,123 @@
+// attn_internal.h -- layouts and parameters shared by the host launcher, the
+// block-mask builder and the forward kernel (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/attn.h"
+
+namespace attn {
+
+// Tile shape: 128 query rows x 128 keys.  A work item is a pair of query
+// tiles (256 rows) processed in ping-pong by two softmax warpgroups.
+constexpr int kTileM = 128;
+constexpr int kTileN = 128;
+constexpr int kTilesPerItem = 2;
+
+// Tile classes.
+enum TileClass : uint32_t { kEmpty = 0, kPartial = 1, kFull = 2 };
+
+// Entry of a pair's key-tile list: key tile index in bits 0..23, the class
+// for the first query tile in bits 24..25, for the second in bits 26..27.
+constexpr uint32_t kListIdxMask = 0x00FFFFFFu;
+__host__ __device__ inline uint32_t list_entry(uint32_t kt, uint32_t c0, uint32_t c1) {
+  return kt | (c0 << 24) | (c1 << 26);
+}
+__host__ __device__ inline uint32_t entry_tile(uint32_t e) { return e & kListIdxMask; }
+__host__ __device__ inline uint32_t entry_cls(uint32_t e, int t) { return (e >> (24 + 2 * t)) & 3u; }
+
+constexpr uint32_t kBlockMaskMagic = 0x4B4D4241u;  // "ABMK"
+constexpr uint32_t kBlockMaskVersion = 1u;
+
+// Device block-mask buffer: header, then order[], cnt[], list[][nK].
+struct BlockMaskHeader {
+  uint32_t magic;
+  uint32_t version;
+  int32_t B, S_q, S_k;
+  int32_t nQ, nK, nP;       // query tiles, key tiles, query-tile pairs
+  int32_t bm;               // batches the mask depends on (B or 1)
+  int32_t n_entries;        // bm * nP
+  uint32_t mask_flags;
+  int32_t window;
+  int32_t q_offset;
+  int32_t force_partial;
+  int32_t uniform;          // 1 when every entry has the same tile count
+  int32_t max_cnt;
+  uint64_t doc_ptr;         // mask arrays the mask was built from
+  uint64_t prefix_ptr;
+  uint64_t order_off, cnt_off, list_off;  // byte offsets from the header
+  uint64_t total_bytes;
+};
+static_assert(sizeof(BlockMaskHeader) % 16 == 0, "header alignment");
+
+struct BlockMaskGeom {
+  int nQ, nK, nP, bm, n_entries;
+  size_t order_off, cnt_off, list_off, total;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline BlockMaskGeom block_mask_geom(int B, int S_q, int S_k, uint32_t mask_flags) {
+  BlockMaskGeom g;
+  g.nQ = (S_q + kTileM - 1) / kTileM;
+  g.nK = (S_k + kTileN - 1) / kTileN;
+  g.nP = (g.nQ + kTilesPerItem - 1) / kTilesPerItem;
+  g.bm = (mask_flags & (ATTN_MASK_DOCUMENT | ATTN_MASK_PREFIX_LM)) ? B : 1;
+  g.n_entries = g.bm * g.nP;
+  g.order_off = align_up(sizeof(BlockMaskHeader), 16);
+  g.cnt_off = align_up(g.order_off + sizeof(int32_t) * (size_t)g.n_entries, 16);
+  g.list_off = align_up(g.cnt_off + sizeof(int32_t) * (size_t)g.n_entries, 16);
+  g.total = align_up(g.list_off + sizeof(uint32_t) * (size_t)g.n_entries * (size_t)g.nK, 16);
+  return g;
+}
+
+// Mask parameters as the kernels see them.
+struct MaskParams {
+  uint32_t flags;
+  int32_t window;
+  int32_t q_offset;
+  int32_t S_q, S_k;
+  const int32_t* doc_ids;     // [B][S_k]
+  const int32_t* prefix_len;  // [B]
+};
+
+// Status codes the device writes (first error wins).
+struct DeviceStatus {
+  int32_t code;        // attn_status
+  int32_t where;       // site id of the failure
+  int32_t block;       // blockIdx.x
+  int32_t detail;
+};
+
+// Launchers (defined in the .cu files, called by the host API).
+cudaError_t launch_build_block_mask(int B, int S_q, int S_k, const MaskParams& mp,
+                                    int force_partial, void* dst, cudaStream_t stream);
+
+struct FwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* out;
+  float* lse;
+  int B, H, H_kv, S_q, S_k, D;
+  float scale;
+  MaskParams mask;
+  uint32_t score_flags;
+  float softcap;
+  const float* alibi_slopes;
+  const void* block_mask;      // device, built for this call
+  int n_entries;
+  int bm;
+  int nP;
+  DeviceStatus* status;        // device
+  float rescale_threshold;
+  double wait_budget_ms;
+  int num_ctas;                // 0 = SM count
+  float poly_fraction;
+};
+
+cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream);
+
+}  // namespace attn

@@ -1,0 +1,417 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-per-workload]
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+the block-mask build (tile classification + work order) and the fused
+forward kernel, through the C ABI, on inputs already resident in HBM.
+
+Metric: useful TFLOPS = 4 * D * (visible (query, key) pairs) / time, so the
+two GEMMs are counted only on unmasked pairs; softmax work is not counted.
+The headline workload is dense B=4 H=16 S=4096 D=128; the other named
+workloads are reported per mask type under "per_workload".
+
+One JSON line is printed by rank 0.  With N > 1 (torchrun, one process per
+GPU) every rank runs an independent replica of the workload ("scaling":
+"weak"): the path has no exchange step, so no collective is used.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+
+
+def visible_pairs(w: workloads.Workload, doc_ids=None, prefix_len=None) -> int:
+    """Exact number of visible (query, key) pairs summed over batch and heads."""
+    total = 0
+    for b in range(w.B):
+        i = np.arange(w.S_q, dtype=np.int64)
+        qpos = i + w.q_offset
+        lo = np.zeros(w.S_q, dtype=np.int64)
+        hi = np.full(w.S_q, w.S_k - 1, dtype=np.int64)
+        if w.causal:
+            hi = np.minimum(hi, qpos)
+        if w.window:
+            lo = np.maximum(lo, qpos - w.window + 1)
+            hi = np.minimum(hi, qpos)
+        if prefix_len is not None:
+            hi = np.minimum(hi, np.maximum(qpos, int(prefix_len[b]) - 1))
+        if doc_ids is not None:
+            ids = np.asarray(doc_ids[b])
+            # packed documents: row i sees the keys of its own document
+            starts = np.searchsorted(ids, ids, side="left")
+            ends = np.searchsorted(ids, ids, side="right") - 1
+            lo = np.maximum(lo, starts[:w.S_q])
+            hi = np.minimum(hi, ends[:w.S_q])
+        total += int(np.clip(hi - lo + 1, 0, None).sum())
+    return total * w.H
+
+
+def useful_flops(w, pairs):
+    return 4.0 * w.D * pairs
+
+
+def algorithmic_bytes(w):
+    """Q, K, V read once; O and LSE written once."""
+    return (2 * (w.B * w.H * w.S_q * w.D) * 2 + 2 * (w.B * w.H_kv * w.S_k * w.D) * 2
+            + 4 * w.B * w.H * w.S_q)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in (self.out or "").splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        # samples under load: the upper part of the distribution
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def mods_of(w, inp, dev):
+    kw = {}
+    if w.causal:
+        kw["causal"] = True
+    if w.window:
+        kw["window"] = w.window
+    if w.document:
+        kw["doc_ids"] = inp["doc_ids"].to(dev)
+    if w.prefix_lm:
+        kw["prefix_len"] = inp["prefix_len"].to(dev)
+    if w.alibi:
+        kw["alibi"] = True
+    if w.softcap:
+        kw["softcap"] = w.softcap
+    if w.q_offset:
+        kw["q_offset"] = w.q_offset
+    return kw
+
+
+def time_workload(attn, w, inp, dev, steps, warmup):
+    """Device timing of `steps` whole steps (block mask + forward) on resident
+    inputs, plus the forward kernel's own average duration."""
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    kw = mods_of(w, inp, dev)
+    mask_kw = {n: kw[n] for n in ("causal", "window", "doc_ids", "prefix_len", "q_offset") if n in kw}
+    score_kw = {n: kw[n] for n in ("alibi", "softcap") if n in kw}
+    o = torch.empty((w.B, w.H, w.S_q, w.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H, w.S_q), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    bm = attn.build_block_mask(w.B, w.H, w.S_q, w.S_k, device=dev, **mask_kw)
+
+    def step(ev_a=None, ev_b=None):
+        bm.rebuild(stream)  # a1: tile classes + work order, into the same buffer
+        if ev_a is not None:
+            ev_a.record(stream)
+        attn.attn_fwd_into(q, k, v, o, lse, scale=w.scale, block_mask=bm, stream=stream,
+                           **mask_kw, **score_kw)
+        if ev_b is not None:
+            ev_b.record(stream)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for a, b in evs:
+        step(a, b)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    total_ms = start.elapsed_time(end)
+    kern_ms = [a.elapsed_time(b) for a, b in evs]
+    st = attn.get_device_status(device=dev)
+    if st != 0:
+        raise RuntimeError("device status %s" % attn.status_string(st))
+    return total_ms / steps, statistics.mean(kern_ms), statistics.median(kern_ms)
+
+
+def time_e2e(attn, w, inp, dev, steps, warmup):
+    """Same metric through the public API from pinned host memory: H2D of
+    Q, K, V (+ mask arrays), the forward, D2H of O and LSE, every step."""
+    hq, hk, hv = (inp[n].pin_memory() for n in ("q", "k", "v"))
+    extra = {n: inp[n].pin_memory() for n in ("doc_ids", "prefix_len") if n in inp}
+    ho = torch.empty((w.B, w.H, w.S_q, w.D), dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty((w.B, w.H, w.S_q), dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        q = hq.to(dev, non_blocking=True)
+        k = hk.to(dev, non_blocking=True)
+        v = hv.to(dev, non_blocking=True)
+        dinp = {n: t.to(dev, non_blocking=True) for n, t in extra.items()}
+        kw = mods_of(w, dinp, dev)
+        o, lse = attn.attn_fwd(q, k, v, scale=w.scale, **kw)
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        step()
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, *extra.values()))
+    d2h = ho.numel() * 2 + hl.numel() * 4
+    return start.elapsed_time(end) / steps, h2d, d2h
+
+
+def oracle_sample(w, inp, target_s=15.0, seed=5):
+    """Time the fp64 oracle on a bounded row sample; returns (TFLOPS, rows, secs, cores)."""
+    import oracle
+    cores = oracle.num_threads()
+    g = torch.Generator().manual_seed(seed)
+    N = w.B * w.H * w.S_q
+    # calibrate on a few rows, then size the sample to ~target_s seconds
+    probe = torch.randperm(N, generator=g)[:max(cores, 16)].numpy()
+    t0 = time.perf_counter()
+    oracle.attn_workload_rows(w, inp, rows=probe)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    n = int(min(N, max(len(probe), len(probe) * target_s / dt)))
+    rows = torch.randperm(N, generator=g)[:n].numpy()
+    t0 = time.perf_counter()
+    oracle.attn_workload_rows(w, inp, rows=rows)
+    secs = time.perf_counter() - t0
+    # useful pairs in the sample: each sampled row contributes its visible keys
+    pairs_per_row = visible_pairs(w, inp.get("doc_ids"), inp.get("prefix_len")) / N
+    flops = useful_flops(w, pairs_per_row * n)
+    return flops / secs / 1e12, n, secs, cores
+
+
+def run_reference(args, world, rank):
+    """Reference arm: the fp64 CPU oracle, as it stands, on the host cores."""
+    if rank != 0:
+        return
+    w = workloads.get(args.workload)
+    inp = workloads.generate(w)
+    vals = []
+    cores = None
+    n_rows = 0
+    for i in range(args.warmup + args.steps):
+        tf, n, secs, cores = oracle_sample(w, inp, target_s=args.ref_seconds, seed=100 + i)
+        if i >= args.warmup:
+            vals.append(tf)
+            n_rows = n
+    value = statistics.mean(vals)
+    pairs = visible_pairs(w, inp.get("doc_ids"), inp.get("prefix_len"))
+    ms = useful_flops(w, pairs) / (value * 1e12) * 1e3
+    line = {
+        "impl": "reference", "metric": "attention fwd useful TFLOPS (%s)" % w.name,
+        "value": value, "unit": "TFLOPS", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.H_kv, "S": w.S_q,
+                   "D": w.D},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                         "sample": "%d seeded query rows per step of %s (of %d); "
+                                   "ms_per_step extrapolates to the whole workload"
+                                   % (n_rows, w.name, w.B * w.H * w.S_q)},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=workloads.HEADLINE, choices=list(workloads.WORKLOADS))
+    ap.add_argument("--no-per-workload", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=8.0)
+    args = ap.parse_args()
+    world, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    import attention_attn_fwd_04_gb300 as attn
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    peaks, peak_kind = load_peaks()
+
+    w = workloads.get(args.workload)
+    inp = workloads.generate(w)
+    pairs = visible_pairs(w, inp.get("doc_ids"), inp.get("prefix_len"))
+    flops = useful_flops(w, pairs)
+
+    barrier(world)
+    with ClockSampler(local) as clk:
+        ms_step, kern_ms_mean, kern_ms_med = time_workload(attn, w, inp, dev, args.steps,
+                                                           args.warmup)
+    clocks = clk.summary()
+    ms_step_max = max_over_ranks(ms_step, world)
+    value = world * flops / (ms_step_max * 1e-3) / 1e12
+
+    timed_s = ms_step * args.steps / 1e3
+    peak = peaks["bf16_tflops_sustained"] if timed_s > 1.0 else peaks["bf16_tflops"]
+    achieved = flops / (kern_ms_mean * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": None,
+                "kernel": "attn_fwd_kernel", "kernel_ms_mean": kern_ms_mean,
+                "kernel_ms_median": kern_ms_med,
+                "peak_kind": "%s %s" % (peak_kind, "sustained" if timed_s > 1.0 else "burst")}
+
+    e2e_ms, h2d, d2h = time_e2e(attn, w, inp, dev, max(3, args.steps // 2), args.warmup)
+    e2e_ms = max_over_ranks(e2e_ms, world)
+    e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    per = {}
+    if not args.no_per_workload:
+        for name, wx in workloads.WORKLOADS.items():
+            if name == w.name:
+                per[name] = {"tflops": value / world, "kernel_tflops": achieved,
+                             "ms_per_step": ms_step, "frac": achieved / peak}
+                continue
+            ix = workloads.generate(wx)
+            px = visible_pairs(wx, ix.get("doc_ids"), ix.get("prefix_len"))
+            fx = useful_flops(wx, px)
+            msx, kx, _ = time_workload(attn, wx, ix, dev, max(5, args.steps // 2), 3)
+            per[name] = {"tflops": fx / (msx * 1e-3) / 1e12,
+                         "kernel_tflops": fx / (kx * 1e-3) / 1e12,
+                         "ms_per_step": msx, "kernel_ms": kx,
+                         "frac": fx / (kx * 1e-3) / 1e12 / peak,
+                         "hbm_gbs": algorithmic_bytes(wx) / (kx * 1e-3) / 1e9}
+            del ix
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, n, secs, cores = oracle_sample(w, inp, target_s=15.0)
+        cpu = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+               "sample": "%d seeded query rows of %s (%.1f s)" % (n, w.name, secs)}
+
+    if rank == 0:
+        line = {
+            "metric": "attention fwd useful TFLOPS (%s)" % w.name,
+            "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step_max, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.H_kv, "S": w.S_q,
+                       "D": w.D, "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "inputs larger than L2 (%d MB of Q/K/V)"
+                             % (algorithmic_bytes(w) // 2**20),
+                       "useful_flops": flops, "visible_pairs": pairs},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "clocks": clocks,
+            "gpu_launches": 3 * args.steps,
+            "per_workload": per,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

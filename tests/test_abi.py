@@ -1,0 +1,114 @@
+"""The C-ABI library loads, exports every symbol the header declares, and
+rejects bad arguments on the host (no GPU needed: nothing is enqueued)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def attn():
+    from attention_attn_fwd_04_gb300 import build as b
+    b.build()
+    import attention_attn_fwd_04_gb300 as a
+    return a
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[a-z_][\w \*]*?\b(attn_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_block_mask_bytes", "attn_build_block_mask",
+              "attn_get_device_status", "attn_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(attn):
+    lib = ctypes.CDLL(attn.library_path())
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_abi_version(attn):
+    lib = attn.lib()
+    assert lib.attn_abi_version() == 1
+    assert attn.status_string(0) == "ATTN_OK"
+    assert attn.status_string(4) == "ATTN_ERR_TIMEOUT"
+    assert attn.status_string(99) == "ATTN_ERR_UNKNOWN"
+
+
+def _call(attn, q=16, k=16, v=16, out=32, lse=None, B=1, H=2, H_kv=2, S_q=128, S_k=128, D=64,
+          scale=0.125, mod=None):
+    lib = attn.lib()
+    return lib.attn_fwd(q, k, v, out, lse, B, H, H_kv, S_q, S_k, D, scale,
+                        ctypes.byref(mod) if mod is not None else None, None)
+
+
+def test_host_validation_rejects_bad_arguments(attn):
+    # fake, aligned, non-overlapping "device" addresses: validation fails
+    # before any CUDA call, so nothing is dereferenced
+    big = 1 << 40
+    ok = dict(q=big, k=2 * big, v=3 * big, out=4 * big)
+    INVALID, UNSUP = 1, 2
+    assert _call(attn, **{**ok, "q": None}) == INVALID
+    assert _call(attn, **{**ok, "out": None}) == INVALID
+    assert _call(attn, **{**ok, "q": big + 8}) == INVALID          # not 16-byte aligned
+    assert _call(attn, **ok, D=96) == UNSUP
+    assert _call(attn, **ok, H=3, H_kv=2) == INVALID                # H % H_kv
+    assert _call(attn, **ok, S_q=0) == INVALID
+    assert _call(attn, **ok, B=-1) == INVALID
+    assert _call(attn, **ok, scale=0.0) == INVALID
+    assert _call(attn, **ok, scale=float("nan")) == INVALID
+    assert _call(attn, **{**ok, "out": big}) == INVALID              # out aliases q
+    m = attn.ModDesc()
+    m.version = 7
+    assert _call(attn, **ok, mod=m) == INVALID                      # bad version
+    m.version = 1
+    m.mask_flags = attn.MASK_WINDOW
+    m.window = 0
+    assert _call(attn, **ok, mod=m) == INVALID                      # window <= 0
+    m.mask_flags = attn.MASK_DOCUMENT
+    assert _call(attn, **ok, mod=m) == INVALID                      # doc_ids NULL
+    m.doc_ids = 5 * big
+    assert _call(attn, **ok, S_k=256, mod=m) == INVALID             # S_q != S_k
+    m.mask_flags = 0
+    m.score_flags = attn.SCORE_SOFTCAP
+    m.softcap = -1.0
+    assert _call(attn, **ok, mod=m) == INVALID                      # softcap <= 0
+    m.score_flags = 0
+    m.mask_flags = 1 << 9
+    assert _call(attn, **ok, mod=m) == INVALID                      # unknown flag
+    m.mask_flags = attn.MASK_PREFIX_LM
+    assert _call(attn, **ok, mod=m) == INVALID                      # prefix_len NULL
+
+
+def test_block_mask_bytes_is_host_only(attn):
+    lib = attn.lib()
+    m = attn.ModDesc()
+    m.version = 1
+    m.mask_flags = attn.MASK_CAUSAL
+    n = lib.attn_block_mask_bytes(2, 32, 8192, 8192, ctypes.byref(m))
+    assert n > 0 and n % 16 == 0
+    # 64 query tiles -> 32 pairs; 64 key tiles per list entry row
+    assert n >= 32 * 64 * 4
+    assert lib.attn_block_mask_bytes(0, 1, 8, 8, None) == 0
+
+
+def test_options_round_trip(attn):
+    old = attn.get_option("rescale_threshold")
+    attn.set_option("rescale_threshold", 0.0)
+    assert attn.get_option("rescale_threshold") == 0.0
+    attn.set_option("rescale_threshold", old)
+    with pytest.raises(attn.AttnError):
+        attn.set_option("exp_poly_fraction", 2.0)
+    with pytest.raises(attn.AttnError):
+        attn.set_option("force_partial", 0.5)

@@ -1,0 +1,288 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle.
+
+Tolerances (element by element, on unit-normal inputs): max |dO| <= 1e-2,
+mean |dO| <= 1e-3, max |dLSE| <= 1e-3.  O from the GPU is bf16; the oracle's
+is unrounded fp64.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+TOL_MAX_O, TOL_MEAN_O, TOL_LSE = 1e-2, 1e-3, 1e-3
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module")
+def attn():
+    import attention_attn_fwd_04_gb300 as a
+    return a
+
+
+def rand_inputs(B, H, Hkv, Sq, Sk, D, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((B, H, Sq, D), generator=g).to(torch.bfloat16)
+    k = torch.randn((B, Hkv, Sk, D), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, Hkv, Sk, D), generator=g).to(torch.bfloat16)
+    return q, k, v
+
+
+def to_dev(kw):
+    out = {}
+    for n, x in kw.items():
+        out[n] = x.to(DEV) if isinstance(x, torch.Tensor) else x
+    return out
+
+
+def oracle_kw(kw):
+    ok = {}
+    for n in ("causal", "window", "doc_ids", "prefix_len", "softcap", "q_offset"):
+        if n in kw and kw[n] is not None:
+            ok[n] = kw[n]
+    if kw.get("alibi"):
+        ok["alibi"] = True
+    if kw.get("alibi_slopes") is not None:
+        ok["alibi_slopes"] = kw["alibi_slopes"].double().tolist()
+    return ok
+
+
+def compare(go, gl, ro, rl, what=""):
+    go = np.asarray(go, dtype=np.float64)
+    gl = np.asarray(gl, dtype=np.float64)
+    fin = np.isfinite(rl)
+    assert np.array_equal(np.isfinite(gl), fin), what + ": -inf rows differ"
+    assert np.all(go[~fin] == 0), what + ": masked rows must be 0"
+    d_o = np.abs(go - ro)
+    d_l = np.abs(gl[fin] - rl[fin]) if fin.any() else np.zeros(1)
+    msg = "%s max|dO|=%.3g mean|dO|=%.3g max|dLSE|=%.3g" % (what, d_o.max(), d_o.mean(), d_l.max())
+    assert d_o.max() <= TOL_MAX_O and d_o.mean() <= TOL_MEAN_O and d_l.max() <= TOL_LSE, msg
+    return msg
+
+
+def run_and_compare(attn, q, k, v, scale, rows=None, **kw):
+    o, lse = attn.attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), scale=scale, **to_dev(kw))
+    st = attn.get_device_status(device=DEV)
+    assert st == 0, attn.status_string(st)
+    D = q.shape[-1]
+    ro, rl = oracle.attn_rows(q, k, v, scale=scale, rows=rows, **oracle_kw(kw))
+    go = o.float().cpu().numpy().reshape(-1, D)
+    gl = lse.cpu().numpy().reshape(-1)
+    if rows is not None:
+        go, gl = go[rows], gl[rows]
+    return compare(go, gl, ro, rl), o, lse
+
+
+# ------------------------------------------------------------ small cases ---
+
+SMALL = [
+    # B H Hkv Sq Sk D  mods
+    (1, 1, 1, 1, 1, 64, {}),
+    (1, 2, 2, 128, 128, 64, {"causal": True}),
+    (1, 2, 1, 129, 129, 64, {"causal": True}),
+    (2, 2, 2, 127, 200, 128, {}),
+    (1, 4, 2, 200, 200, 128, {"causal": True}),
+    (1, 2, 2, 300, 300, 128, {"causal": True}),                 # odd number of q tiles
+    (2, 3, 1, 257, 513, 64, {"causal": True, "q_offset": 256}),  # bottom-right
+    (1, 2, 2, 640, 640, 128, {"window": 200}),
+    (1, 2, 2, 640, 640, 128, {"window": 130, "causal": True}),
+    (1, 2, 2, 700, 700, 64, {"softcap": 5.0}),
+    (1, 2, 2, 640, 640, 128, {"causal": True, "softcap": 30.0}),
+    (1, 4, 4, 600, 600, 128, {"causal": True, "alibi": True}),
+    (1, 2, 2, 520, 520, 64, {"alibi": True, "softcap": 2.0}),
+    (1, 2, 2, 384, 384, 128, {"causal": True, "q_offset": -100}),  # rows with no key
+]
+
+
+@pytest.mark.parametrize("case", range(len(SMALL)))
+def test_small_shapes(attn, case):
+    B, H, Hkv, Sq, Sk, D, mods = SMALL[case]
+    q, k, v = rand_inputs(B, H, Hkv, Sq, Sk, D, seed=100 + case)
+    run_and_compare(attn, q, k, v, 1.0 / math.sqrt(D), **mods)
+
+
+def test_documents_and_prefix(attn):
+    B, H, S, D = 2, 2, 777, 128
+    q, k, v = rand_inputs(B, H, H, S, S, D, seed=7)
+    g = torch.Generator().manual_seed(3)
+    docs = []
+    for b in range(B):
+        cuts = sorted(torch.randint(1, S, (5,), generator=g).tolist())
+        ids = torch.zeros(S, dtype=torch.int32)
+        for c in cuts:
+            ids[c:] += 1
+        docs.append(ids)
+    doc_ids = torch.stack(docs).contiguous()
+    for causal in (False, True):
+        run_and_compare(attn, q, k, v, 1 / math.sqrt(D), doc_ids=doc_ids, causal=causal)
+    prefix = torch.tensor([0, 300], dtype=torch.int32)
+    run_and_compare(attn, q, k, v, 1 / math.sqrt(D), prefix_len=prefix)
+    run_and_compare(attn, q, k, v, 1 / math.sqrt(D), doc_ids=doc_ids, causal=True, alibi=True,
+                    softcap=20.0)
+
+
+def test_unsorted_document_ids(attn):
+    # Ids need not be packed: equality is what the mask tests.
+    B, H, S, D = 1, 2, 400, 64
+    q, k, v = rand_inputs(B, H, H, S, S, D, seed=8)
+    g = torch.Generator().manual_seed(4)
+    doc_ids = torch.randint(0, 3, (1, S), generator=g).to(torch.int32)
+    run_and_compare(attn, q, k, v, 0.125, doc_ids=doc_ids)
+
+
+def test_explicit_alibi_slopes(attn):
+    B, H, S, D = 1, 4, 300, 128
+    q, k, v = rand_inputs(B, H, H, S, S, D, seed=9)
+    slopes = torch.tensor([0.3, 0.05, 1.0, 0.0], dtype=torch.float32)
+    run_and_compare(attn, q, k, v, 1 / math.sqrt(D), causal=True, alibi_slopes=slopes)
+
+
+# ------------------------------------------------------------ block mask ---
+
+def expected_classes(B, S_q, S_k, mods):
+    """Tile classes from the oracle's visibility (Q = K = 0 makes every
+    visible probability positive and every hidden one exactly 0)."""
+    q = torch.zeros((B, 1, S_q, 1), dtype=torch.bfloat16)
+    k = torch.zeros((B, 1, S_k, 1), dtype=torch.bfloat16)
+    _, _, p = oracle.attn_rows(q, k, k, scale=1.0, want_probs=True, **oracle_kw(mods))
+    vis = (p > 0).reshape(B, S_q, S_k)
+    nQ, nK = -(-S_q // 128), -(-S_k // 128)
+    cls = np.zeros((B, nQ, nK), dtype=np.int8)
+    for b in range(B):
+        for qt in range(nQ):
+            for kt in range(nK):
+                blk = vis[b, qt * 128:(qt + 1) * 128, kt * 128:(kt + 1) * 128]
+                if not blk.any():
+                    cls[b, qt, kt] = 0
+                elif blk.all() and blk.shape[1] == 128:
+                    cls[b, qt, kt] = 2
+                else:
+                    cls[b, qt, kt] = 1
+    return cls
+
+
+MASK_CASES = [
+    (1, 640, 640, {}),
+    (1, 700, 700, {"causal": True}),
+    (1, 640, 900, {"causal": True, "q_offset": 260}),
+    (1, 1000, 1000, {"window": 300}),
+    (2, 900, 900, {"doc_ids": "packed", "causal": True}),
+    (2, 900, 900, {"doc_ids": "packed"}),
+    (2, 800, 800, {"prefix_len": [0, 333]}),
+    (1, 520, 520, {"causal": True, "q_offset": -200}),
+]
+
+
+@pytest.mark.parametrize("case", range(len(MASK_CASES)))
+def test_block_mask_exact(attn, case):
+    B, S_q, S_k, mods = MASK_CASES[case]
+    mods = dict(mods)
+    if mods.get("doc_ids") == "packed":
+        ids = torch.stack([workloads.doc_ids_for(S_k, seed=10 + b, lo=64, hi=300)
+                           for b in range(B)]).contiguous()
+        mods["doc_ids"] = ids
+    if "prefix_len" in mods:
+        mods["prefix_len"] = torch.tensor(mods["prefix_len"], dtype=torch.int32)
+    want = expected_classes(B, S_q, S_k, mods)
+    bm = attn.build_block_mask(B, 1, S_q, S_k, device=DEV, **to_dev(mods))
+    got = attn.decode_block_mask(bm)
+    cls = got["cls"]
+    if cls.shape[0] == 1:  # batch-independent mask: stored once
+        assert all(np.array_equal(want[0], w_) for w_ in want)
+        want = want[:1]
+    np.testing.assert_array_equal(cls, want)
+    # lists are the non-empty key tiles of each pair, descending
+    nP = got["nP"]
+    for e in range(got["n_entries"]):
+        b, p = divmod(e, nP)
+        lst = [int(x) & 0xFFFFFF for x in got["list"][e, :got["cnt"][e]]]
+        rows = [2 * p + t for t in range(2) if 2 * p + t < got["nQ"]]
+        nonempty = sorted({kt for kt in range(got["nK"]) for r in rows if want[b, r, kt] != 0},
+                          reverse=True)
+        assert lst == nonempty
+    # order is a permutation sorted by descending count
+    order = got["order"]
+    assert sorted(order.tolist()) == list(range(got["n_entries"]))
+    c = got["cnt"][order]
+    assert np.all(np.diff(c) <= 0)
+
+
+# ------------------------------------------------- invariants of the path ---
+
+def test_force_partial_is_bit_identical(attn):
+    B, H, S, D = 1, 4, 1024, 128
+    q, k, v = rand_inputs(B, H, H, S, S, D, seed=11)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    for mods in ({}, {"causal": True}, {"window": 256}):
+        o1, l1 = attn.attn_fwd(qd, kd, vd, **mods)
+        attn.set_option("force_partial", 1)
+        try:
+            o2, l2 = attn.attn_fwd(qd, kd, vd, **mods)
+        finally:
+            attn.set_option("force_partial", 0)
+        assert torch.equal(o1, o2) and torch.equal(l1, l2), mods
+
+
+def test_rescale_threshold_does_not_change_results(attn):
+    B, H, S, D = 1, 2, 1024, 128
+    q, k, v = rand_inputs(B, H, H, S, S, D, seed=12)
+    q = (q.float() * 3).to(torch.bfloat16)  # larger score range -> more rescales
+    old = attn.get_option("rescale_threshold")
+    try:
+        for tau in (0.0, 4.0, 8.0):
+            attn.set_option("rescale_threshold", tau)
+            run_and_compare(attn, q, k, v, 1 / math.sqrt(D), causal=True)
+    finally:
+        attn.set_option("rescale_threshold", old)
+
+
+def test_prebuilt_block_mask_matches_internal(attn):
+    B, H, S, D = 2, 4, 900, 128
+    q, k, v = rand_inputs(B, H, H, S, S, D, seed=13)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    o1, l1 = attn.attn_fwd(qd, kd, vd, causal=True)
+    bm = attn.build_block_mask(B, H, S, S, device=DEV, causal=True)
+    o2, l2 = attn.attn_fwd(qd, kd, vd, causal=True, block_mask=bm)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_mismatched_block_mask_is_reported(attn):
+    B, H, S, D = 1, 2, 512, 64
+    q, k, v = rand_inputs(B, H, H, S, S, D, seed=14)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    bm = attn.build_block_mask(B, H, S, S, device=DEV)  # dense mask...
+    attn.attn_fwd(qd, kd, vd, causal=True, block_mask=bm)  # ...used for a causal call
+    assert attn.get_device_status(device=DEV) == 5       # ATTN_ERR_DEVICE_CHECK
+    assert attn.get_device_status(device=DEV) == 0       # cleared
+
+
+def test_gqa_equals_repeated_kv(attn):
+    B, H, Hkv, S, D = 1, 8, 2, 333, 128
+    q, k, v = rand_inputs(B, H, Hkv, S, S, D, seed=15)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    o1, l1 = attn.attn_fwd(qd, kd, vd, causal=True)
+    kr = kd.repeat_interleave(H // Hkv, dim=1).contiguous()
+    vr = vd.repeat_interleave(H // Hkv, dim=1).contiguous()
+    o2, l2 = attn.attn_fwd(qd, kr, vr, causal=True)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+# ----------------------------------------------------- the named workloads ---
+
+@pytest.mark.parametrize("name", list(workloads.WORKLOADS))
+def test_workload_parity(attn, name):
+    w = workloads.get(name)
+    inp = workloads.generate(w)
+    rows = workloads.sample_rows(w, 4096, doc_ids=inp.get("doc_ids"))
+    kw = dict(causal=w.causal, window=w.window or None, doc_ids=inp.get("doc_ids"),
+              prefix_len=inp.get("prefix_len"), alibi=w.alibi, softcap=w.softcap or None,
+              q_offset=w.q_offset)
+    kw = {k_: v_ for k_, v_ in kw.items() if v_ is not None and v_ is not False}
+    msg, _, _ = run_and_compare(attn, inp["q"], inp["k"], inp["v"], w.scale,
+                                rows=rows.numpy(), **kw)
+    print(name, msg)
