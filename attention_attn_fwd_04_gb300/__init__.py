@@ -127,9 +127,22 @@ def _load() -> ctypes.CDLL:
     return lib
 
 
-_lib = _load()
-if _lib.attn_abi_version() != 1:
-    raise ImportError("libattn_gb300.so ABI version mismatch")
+class _LazyLib:
+    """Loads ``libattn_gb300.so`` on first use, so the build module can be
+    imported before the library exists.  A missing library raises."""
+
+    _cdll = None
+
+    def __getattr__(self, name):
+        if _LazyLib._cdll is None:
+            cdll = _load()
+            if cdll.attn_abi_version() != 1:
+                raise ImportError("libattn_gb300.so ABI version mismatch")
+            _LazyLib._cdll = cdll
+        return getattr(_LazyLib._cdll, name)
+
+
+_lib = _LazyLib()
 
 
 def library_path() -> str:
@@ -138,7 +151,8 @@ def library_path() -> str:
 
 def lib() -> ctypes.CDLL:
     """The loaded C library (for callers that want the raw ABI)."""
-    return _lib
+    _lib.attn_abi_version  # force the load
+    return _LazyLib._cdll
 
 
 def status_string(status: int) -> str:

@@ -318,12 +318,13 @@ def run_reference(args, world, rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=workloads.HEADLINE, choices=list(workloads.WORKLOADS))
     ap.add_argument("--no-per-workload", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=8.0)
     args = ap.parse_args()
     world, rank, local = dist_init()
@@ -360,10 +361,13 @@ def main():
                 "kernel_ms_median": kern_ms_med,
                 "peak_kind": "%s %s" % (peak_kind, "sustained" if timed_s > 1.0 else "burst")}
 
-    e2e_ms, h2d, d2h = time_e2e(attn, w, inp, dev, max(3, args.steps // 2), args.warmup)
-    e2e_ms = max_over_ranks(e2e_ms, world)
-    e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+    e2e = None
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = time_e2e(attn, w, inp, dev, min(max(3, args.steps // 10), 200),
+                                    args.warmup)
+        e2e_ms = max_over_ranks(e2e_ms, world)
+        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     per = {}
     if not args.no_per_workload:
@@ -375,7 +379,7 @@ def main():
             ix = workloads.generate(wx)
             px = visible_pairs(wx, ix.get("doc_ids"), ix.get("prefix_len"))
             fx = useful_flops(wx, px)
-            msx, kx, _ = time_workload(attn, wx, ix, dev, max(5, args.steps // 2), 3)
+            msx, kx, _ = time_workload(attn, wx, ix, dev, min(max(5, args.steps // 4), 500), 3)
             per[name] = {"tflops": fx / (msx * 1e-3) / 1e12,
                          "kernel_tflops": fx / (kx * 1e-3) / 1e12,
                          "ms_per_step": msx, "kernel_ms": kx,

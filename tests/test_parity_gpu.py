@@ -1,8 +1,14 @@
 """GPU parity: the CUDA path through the C ABI against the fp64 oracle.
 
-Tolerances (element by element, on unit-normal inputs): max |dO| <= 1e-2,
-mean |dO| <= 1e-3, max |dLSE| <= 1e-3.  O from the GPU is bf16; the oracle's
-is unrounded fp64.
+Tolerances (element by element, on unit-normal inputs):
+    |dO| <= 1e-2 + 2^-8 |O|,   mean |dO| <= 1e-3,   max |dLSE| <= 1e-3.
+O from the GPU is bf16 and the oracle's is unrounded fp64.  Two roundings
+scale with |O| and no bf16 kernel avoids them: the output itself (half a
+bf16 spacing, 2^-9 |O|: 0.0156 once |O| >= 4) and the bf16 P fed to the PV
+MMA (<= 2^-9 sum_j w_j |v_j|, about 2^-9 |O| when a row's weight sits on
+one key).  Rows whose weight sits on a few keys reach |O| of 2-4, where a plain
+1e-2 bound is below one bf16 spacing; the 2^-8 |O| term allows exactly
+those two roundings.  The messages also count elements above a plain 1e-2.
 """
 import math
 
@@ -60,8 +66,11 @@ def compare(go, gl, ro, rl, what=""):
     assert np.all(go[~fin] == 0), what + ": masked rows must be 0"
     d_o = np.abs(go - ro)
     d_l = np.abs(gl[fin] - rl[fin]) if fin.any() else np.zeros(1)
-    msg = "%s max|dO|=%.3g mean|dO|=%.3g max|dLSE|=%.3g" % (what, d_o.max(), d_o.mean(), d_l.max())
-    assert d_o.max() <= TOL_MAX_O and d_o.mean() <= TOL_MEAN_O and d_l.max() <= TOL_LSE, msg
+    excess = d_o - (TOL_MAX_O + 2.0 ** -8 * np.abs(ro))  # > 0 where the bound fails
+    msg = "%s max|dO|=%.3g (max over bound %.3g, %d of %d above 1e-2) mean|dO|=%.3g " \
+          "max|dLSE|=%.3g" % (what, d_o.max(), excess.max(), int((d_o > TOL_MAX_O).sum()),
+                              d_o.size, d_o.mean(), d_l.max())
+    assert excess.max() <= 0 and d_o.mean() <= TOL_MEAN_O and d_l.max() <= TOL_LSE, msg
     return msg
 
 
@@ -228,15 +237,40 @@ def test_force_partial_is_bit_identical(attn):
         assert torch.equal(o1, o2) and torch.equal(l1, l2), mods
 
 
-def test_rescale_threshold_does_not_change_results(attn):
+def compare_bound(go, gl, ro, ro_abs, rl, what=""):
+    """Sharp-attention check against an error bound of the arithmetic.
+
+    The kernel rounds P to bf16 (relative error <= 2^-9 per term) before the
+    PV product and rounds O to bf16 at the end (<= 2^-9 |O|); everything else
+    is fp32.  So |O_gpu - O| <= 2^-9 sum_j p_j |v_j| + 2^-9 |O| up to fp32
+    noise; the test allows twice that.  sum_j p_j |v_j| is the oracle's output
+    for |V| (exact in bf16).  LSE keeps its absolute tolerance."""
+    go = np.asarray(go, dtype=np.float64)
+    bound = 2.0 ** -8 * (ro_abs + np.abs(ro)) + 1e-6
+    excess = np.abs(go - ro) / bound
+    fin = np.isfinite(rl)
+    d_l = np.abs(np.asarray(gl)[fin] - rl[fin]).max()
+    assert excess.max() <= 1.0 and d_l <= TOL_LSE, \
+        "%s max |dO|/bound=%.2f max|dO|=%.3g max|dLSE|=%.3g" % (
+            what, excess.max(), np.abs(go - ro).max(), d_l)
+
+
+@pytest.mark.parametrize("tau", [0.0, 4.0, 8.0])
+def test_rescale_threshold_does_not_change_results(attn, tau):
     B, H, S, D = 1, 2, 1024, 128
     q, k, v = rand_inputs(B, H, H, S, S, D, seed=12)
-    q = (q.float() * 3).to(torch.bfloat16)  # larger score range -> more rescales
     old = attn.get_option("rescale_threshold")
     try:
-        for tau in (0.0, 4.0, 8.0):
-            attn.set_option("rescale_threshold", tau)
-            run_and_compare(attn, q, k, v, 1 / math.sqrt(D), causal=True)
+        attn.set_option("rescale_threshold", tau)
+        run_and_compare(attn, q, k, v, 1 / math.sqrt(D), causal=True)
+        # sharper attention (scores ~ N(0, 9)) rescales far more often
+        q3 = (q.float() * 3).to(torch.bfloat16)
+        o, lse = attn.attn_fwd(q3.to(DEV), k.to(DEV), v.to(DEV), scale=1 / math.sqrt(D),
+                               causal=True)
+        ro, rl = oracle.attn_rows(q3, k, v, scale=1 / math.sqrt(D), causal=True)
+        ra, _ = oracle.attn_rows(q3, k, v.abs(), scale=1 / math.sqrt(D), causal=True)
+        compare_bound(o.float().cpu().numpy().reshape(-1, D), lse.cpu().numpy().reshape(-1),
+                      ro, ra, rl, what="tau=%g" % tau)
     finally:
         attn.set_option("rescale_threshold", old)
 
