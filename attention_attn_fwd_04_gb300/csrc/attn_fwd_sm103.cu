@@ -6,7 +6,8 @@
 //   warps 0-3  softmax warpgroup for query tile 0 (one thread per row)
 //   warps 4-7  softmax warpgroup for query tile 1
 //   warp  8    TMA producer: Q tiles and a ring of K / V tiles
-//   warp  9    Tensor Memory owner and MMA issuer (one elected thread)
+//   warp  9    Tensor Memory owner; MMA issuer for query tile 0
+//   warp 10    MMA issuer for query tile 1
 //
 // Per key tile j the tensor core computes S_t = Q_t K_j^T into Tensor Memory
 // (fp32), the softmax warpgroup of tile t turns S_t into P_t (bf16, written
@@ -18,11 +19,12 @@
 // a threshold ("Conditional rescaling").  The score matrix never leaves the
 // SM ("Enter Tri Dao and FlashAttention").
 //
-// Issue order on the tensor pipe per key tile j:
-//   PV_0(j), S_0(j+1), PV_1(j), S_1(j+1)
-// so each softmax warpgroup has the other tile's two MMAs to hide behind.
-// S_t(j+1) overwrites the Tensor Memory that P_t(j) occupies; it is issued
-// after PV_t(j) by the same thread and tcgen05 MMAs execute in issue order.
+// Each query tile has its own issuing thread with the chain
+//   S_t(j), [P_t(j) ready] PV_t(j), S_t(j+1), ...
+// and the tensor pipe interleaves the two chains, so each softmax
+// warpgroup hides behind the other tile's MMAs.  S_t(j+1) overwrites the
+// Tensor Memory that P_t(j) occupies; it is issued after PV_t(j) by the same
+// thread and tcgen05 MMAs execute in issue order.
 //
 // Every mbarrier wait is bounded by a time budget; on expiry the kernel
 // records ATTN_ERR_TIMEOUT in the device status word, drains its own
@@ -40,7 +42,7 @@ namespace attn {
 namespace {
 
 // Three warpgroups: two softmax warpgroups and one producer warpgroup whose
-// warps 8 and 9 load and issue MMAs (warps 10 and 11 only hand their
+// warp 8 loads and warps 9 and 10 issue MMAs (warp 11 only hands its
 // registers to the softmax warpgroups).  384 threads launch with 168
 // registers each; the producer warpgroup drops to kRegsProducer and the
 // softmax warpgroups grow to kRegsSoftmax, which uses the same total:
@@ -70,6 +72,7 @@ enum Site : int {
   kSiteMmaPFull = 22,
   kSiteMmaOEmpty = 23,
   kSiteMmaDrain = 24,
+  kSiteMmaTurn = 25,
   kSiteSmxSFull = 30,
   kSiteSmxOFull = 31,
 };
@@ -250,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             B_PF = B_SF + 2, B_OF = B_PF + 4, B_OE = B_OF + 2, B_DRAIN = B_OE + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kSmemMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kSmemMisc + 4);
+  volatile int* s_turn = reinterpret_cast<volatile int*>(smem + C::kSmemMisc + 8);
   int* s_doc = reinterpret_cast<int*>(smem + C::kSmemDoc);
 
   if (threadIdx.x == 0) {
@@ -259,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     ptx::mbar_init(bar(B_QE + 1), 1);
     for (int s = 0; s < C::kStages; ++s) {
       ptx::mbar_init(bar(B_KVF + s), 1);
-      ptx::mbar_init(bar(B_KVE + s), 1);
+      ptx::mbar_init(bar(B_KVE + s), 2);  // one commit per MMA issuer
     }
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(bar(B_SF + t), 1);
@@ -268,8 +272,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       ptx::mbar_init(bar(B_OF + t), 1);
       ptx::mbar_init(bar(B_OE + t), 4);
     }
-    ptx::mbar_init(bar(B_DRAIN), 1);
+    ptx::mbar_init(bar(B_DRAIN), 2);
     *s_abort = 0;
+    *s_turn = 0;
     ptx::fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -355,11 +360,43 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           }
         }
       }
-    } else if (warp == kMmaWarp && lane == 0) {
-      // ===================== MMA issuer ==================================
-      auto tS = [&](int t) { return tmem + (uint32_t)(t * kTileN); };
-      auto tO = [&](int t) { return tmem + (uint32_t)(C::kOCol + t * D); };
-      auto sQ = [&](int t) { return sbase + (uint32_t)(C::kSmemQ + t * C::kTileBytes); };
+    } else if ((warp == kMmaWarp || warp == kMmaWarp + 1) && lane == 0) {
+      // ===================== MMA issuers =================================
+      // Two issuing threads, one per query tile.  Issue blocks until the
+      // tensor pipe accepts the MMA and every mbarrier wait costs a few
+      // hundred cycles even when the phase is already complete, so a single
+      // issuer leaves the pipe idle during its waits; with one issuer per
+      // tile the other tile's MMAs fill those gaps.  Each tile's chain
+      //   S_t(0), PV_t(0), S_t(1), PV_t(1), ...
+      // stays in issue order on one thread, which keeps the P_t / S_t
+      // aliasing safe.  K/V stages are released once both issuers commit.
+      // A turn token makes the two tiles' MMA groups alternate on the pipe
+      // (tile 0 group k, tile 1 group k, tile 0 group k+1, ...) so that each
+      // tile's S finishes as early as in a strict ping-pong; an issuer does
+      // its barrier waits while the other one issues, then takes its turn.
+      // Every group waits only on earlier groups, so the order cannot
+      // deadlock.
+      const int t = warp - kMmaWarp;
+      int grp = 0;  // groups this issuer has issued
+      auto take_turn = [&]() -> bool {
+        const int want = 2 * grp + t;
+        if (*s_turn == want) return true;
+        const uint64_t t0 = ptx::globaltimer_ns();
+        for (uint32_t spin = 1;; ++spin) {
+          if (*s_turn == want) return true;
+          if ((spin & 255) == 0) {
+            if (*s_abort) return false;
+            if (ptx::globaltimer_ns() - t0 > p.budget_ns) {
+              report(ctl, ATTN_ERR_TIMEOUT, kSiteMmaTurn, want);
+              return false;
+            }
+          }
+        }
+      };
+      auto pass_turn = [&]() { *s_turn = 2 * grp + t + 1; ++grp; };
+      const uint32_t tS = tmem + (uint32_t)(t * kTileN);
+      const uint32_t tO = tmem + (uint32_t)(C::kOCol + t * D);
+      const uint32_t sQ = sbase + (uint32_t)(C::kSmemQ + t * C::kTileBytes);
       auto sKV = [&](uint32_t idx) {
         return sbase + (uint32_t)C::kSmemKV + (idx % C::kStages) * (uint32_t)C::kTileBytes;
       };
@@ -367,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       auto kv_empty = [&](uint32_t idx) { return bar(B_KVE + (int)(idx % C::kStages)); };
       auto kv_par = [&](uint32_t idx) { return (idx / C::kStages) & 1; };
       uint32_t kv_cnt = 0;
-      uint32_t p_cnt[2] = {0, 0};
+      uint32_t p_cnt = 0;
       int act = 0;
       bool ok = true;
       for (int r = 0; ok; ++r) {
@@ -376,58 +413,46 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const Item it = decode_item(p, w, uniform);
         const int n = p.cnt[it.e];
         if (n == 0) continue;
-        // S_t(0) for both tiles from K_0.
         const uint32_t k0 = kv_cnt;
-        ok = wait_bar(kv_full(k0), kv_par(k0), ctl, kSiteMmaKvFull);
-        for (int t = 0; t < 2 && ok; ++t) {
-          ok = wait_bar(bar(B_QF + t), act & 1, ctl, kSiteMmaQFull);
-          if (!ok) break;
-          ptx::tc_fence_after();
-          issue_s<D>(tS(t), sQ(t), sKV(k0));
-          ptx::mma_commit(bar(B_SF + t));
-          if (n == 1) ptx::mma_commit(bar(B_QE + t));
-        }
+        ok = wait_bar(bar(B_QF + t), act & 1, ctl, kSiteMmaQFull) &&
+             wait_bar(kv_full(k0), kv_par(k0), ctl, kSiteMmaKvFull) && take_turn();
         if (!ok) break;
+        ptx::tc_fence_after();
+        issue_s<D>(tS, sQ, sKV(k0));
+        pass_turn();
+        ptx::mma_commit(bar(B_SF + t));
+        if (n == 1) ptx::mma_commit(bar(B_QE + t));
         ptx::mma_commit(kv_empty(k0));
         for (int j = 0; j < n && ok; ++j) {
           const uint32_t vi = k0 + 2 * j + 1;  // V_j
           const uint32_t ki = k0 + 2 * j + 2;  // K_{j+1}
-          const bool has_next = (j + 1 < n);
-          ok = wait_bar(kv_full(vi), kv_par(vi), ctl, kSiteMmaKvFull);
-          for (int t = 0; t < 2 && ok; ++t) {
-            if (j == 0 && act > 0) {
-              ok = wait_bar(bar(B_OE + t), (act - 1) & 1, ctl, kSiteMmaOEmpty);
-              if (!ok) break;
-            }
-            for (int h = 0; h < 2 && ok; ++h) {
-              if (kSplitP || h == 0) {
-                ok = wait_bar(bar(B_PF + 2 * t + h), p_cnt[t] & 1, ctl, kSiteMmaPFull);
-                if (!ok) break;
-                ptx::tc_fence_after();
-              }
-              issue_pv_half<D>(tO(t), tS(t), sKV(vi), h, j > 0);
-            }
-            if (!ok) break;
-            ++p_cnt[t];
-            if (t == 1) ptx::mma_commit(kv_empty(vi));
-            if (has_next) {
-              if (t == 0) {
-                ok = wait_bar(kv_full(ki), kv_par(ki), ctl, kSiteMmaKvFull);
-                if (!ok) break;
-              }
-              issue_s<D>(tS(t), sQ(t), sKV(ki));
-              ptx::mma_commit(bar(B_SF + t));
-              if (j + 2 == n) ptx::mma_commit(bar(B_QE + t));
-              if (t == 1) ptx::mma_commit(kv_empty(ki));
-            } else {
-              ptx::mma_commit(bar(B_OF + t));
-            }
+          const bool has_next = j + 1 < n;
+          ok = wait_bar(bar(B_PF + 2 * t), p_cnt & 1, ctl, kSiteMmaPFull) &&
+               wait_bar(kv_full(vi), kv_par(vi), ctl, kSiteMmaKvFull);
+          if (ok && j == 0 && act > 0)
+            ok = wait_bar(bar(B_OE + t), (act - 1) & 1, ctl, kSiteMmaOEmpty);
+          if (ok && has_next) ok = wait_bar(kv_full(ki), kv_par(ki), ctl, kSiteMmaKvFull);
+          if (ok) ok = take_turn();
+          if (!ok) break;
+          ++p_cnt;
+          ptx::tc_fence_after();
+          issue_pv_half<D>(tO, tS, sKV(vi), 0, j > 0);
+          issue_pv_half<D>(tO, tS, sKV(vi), 1, true);
+          if (has_next) issue_s<D>(tS, sQ, sKV(ki));
+          pass_turn();
+          ptx::mma_commit(kv_empty(vi));
+          if (has_next) {
+            ptx::mma_commit(bar(B_SF + t));
+            if (j + 2 == n) ptx::mma_commit(bar(B_QE + t));
+            ptx::mma_commit(kv_empty(ki));
+          } else {
+            ptx::mma_commit(bar(B_OF + t));
           }
         }
         kv_cnt = k0 + 2 * (uint32_t)n;
         ++act;
       }
-      // Wait for every MMA this thread issued before Tensor Memory is freed.
+      // Wait for every MMA of both issuers before Tensor Memory is freed.
       ptx::mma_commit(bar(B_DRAIN));
       const uint64_t t0 = ptx::globaltimer_ns();
       while (!ptx::mbar_try_wait(bar(B_DRAIN), 0)) {
