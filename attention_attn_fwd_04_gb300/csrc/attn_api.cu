@@ -125,6 +125,40 @@ MaskParams mask_params(int S_q, int S_k, const attn_mod_desc* mod) {
 }
 
 }  // namespace
+
+// ---- scratch for attn_fwd_noalloc ----------------------------------------
+// Some callers may not allocate device memory on the call path: code that
+// runs while a stream is being captured into a CUDA graph, runtimes that own
+// all device memory through their own pool or budget, and latency-critical
+// paths that cannot take the device-wide synchronisation cudaMalloc/cudaFree
+// may cause.  attn_fwd allocates its status word and grows its block-mask
+// buffer on first need; attn_fwd_noalloc instead uses this fixed array,
+// which every GPU that loads the library holds until the process exits.
+// Layout: a DeviceStatus in the first kNoAllocStatusBytes, the block mask
+// after it.  Host code must not pass the symbol itself to a kernel (on the
+// host it names a stand-in, not device memory); the device address comes
+// from cudaGetSymbolAddress, once per device.
+namespace {
+constexpr size_t kNoAllocStatusBytes = 256;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on device `dev` (the current device).
+attn_status noalloc_scratch(int dev, void** out) {
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+      return ATTN_ERR_CUDA;
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return ATTN_OK;
+}
+}  // namespace
 }  // namespace attn
 
 using namespace attn;
@@ -352,6 +386,83 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, flo
   a.bm = g.bm;
   a.nP = g.nP;
   a.status = scr->status;
+  a.rescale_threshold = (float)o.rescale_threshold;
+  a.wait_budget_ms = o.wait_budget_ms;
+  a.num_ctas = (int)o.num_ctas;
+  a.poly_fraction = (float)o.poly_fraction;
+  return launch_attn_fwd(a, s) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse,
+                             int B, int H, int H_kv, int S_q, int S_k, int D, float scale,
+                             const attn_mod_desc* mod, attn_stream_t stream) {
+  // ---- host-side validation (same rules as attn_fwd) -----------------------
+  attn_status st = check_problem(B, H, S_q, S_k, mod);
+  if (st != ATTN_OK) return st;
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (H_kv <= 0 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!(isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+    return ATTN_ERR_INVALID_ARG;
+  if (lse != nullptr && !aligned(lse, 4)) return ATTN_ERR_INVALID_ARG;
+  const size_t qb = (size_t)B * H * S_q * D * 2, kb = (size_t)B * H_kv * S_k * D * 2;
+  if ((size_t)B * H > (size_t)INT32_MAX || (size_t)B * H_kv * (size_t)S_k > (size_t)INT32_MAX * 128)
+    return ATTN_ERR_INVALID_ARG;
+  if (overlaps(out, qb, q, qb) || overlaps(out, qb, k, kb) || overlaps(out, qb, v, kb))
+    return ATTN_ERR_INVALID_ARG;
+  if (lse != nullptr) {
+    const size_t lb = (size_t)B * H * S_q * 4;
+    if (overlaps(lse, lb, q, qb) || overlaps(lse, lb, k, kb) || overlaps(lse, lb, v, kb) ||
+        overlaps(lse, lb, out, qb))
+      return ATTN_ERR_INVALID_ARG;
+  }
+  // The block mask is always built into the fixed scratch array.
+  if (mod != nullptr && mod->block_mask != nullptr) return ATTN_ERR_INVALID_ARG;
+  const uint32_t mflags = mod ? mod->mask_flags : 0u;
+  const BlockMaskGeom g = block_mask_geom(B, S_q, S_k, mflags);
+  if (g.total > ATTN_NOALLOC_SCRATCH_BYTES - kNoAllocStatusBytes) return ATTN_ERR_UNSUPPORTED;
+
+  // ---- device work: no allocation from here on ----------------------------
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  void* scratch = nullptr;
+  st = noalloc_scratch(dev, &scratch);
+  if (st != ATTN_OK) return st;
+  DeviceStatus* status = static_cast<DeviceStatus*>(scratch);
+  void* bmask = static_cast<char*>(scratch) + kNoAllocStatusBytes;
+  // The status word must start at zero; the block mask is rewritten whole.
+  if (cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s) != cudaSuccess) return ATTN_ERR_CUDA;
+  const Options o = options_snapshot();
+  const MaskParams mp = mask_params(S_q, S_k, mod);
+  if (launch_build_block_mask(B, S_q, S_k, mp, o.force_partial != 0.0 ? 1 : 0, bmask, s) !=
+      cudaSuccess)
+    return ATTN_ERR_CUDA;
+
+  FwdArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.H_kv = H_kv;
+  a.S_q = S_q;
+  a.S_k = S_k;
+  a.D = D;
+  a.scale = scale;
+  a.mask = mp;
+  a.score_flags = mod ? mod->score_flags : 0u;
+  a.softcap = mod ? mod->softcap : 0.f;
+  a.alibi_slopes = (mod && (mod->score_flags & ATTN_SCORE_ALIBI)) ? mod->alibi_slopes : nullptr;
+  a.block_mask = bmask;
+  a.n_entries = g.n_entries;
+  a.bm = g.bm;
+  a.nP = g.nP;
+  a.status = status;
   a.rescale_threshold = (float)o.rescale_threshold;
   a.wait_budget_ms = o.wait_budget_ms;
   a.num_ctas = (int)o.num_ctas;

@@ -206,6 +206,48 @@ attn_status attn_block_mask_stats(const void *block_mask, size_t bytes,
  */
 attn_status attn_get_device_status(attn_stream_t stream);
 
+/*
+ * attn_fwd_noalloc -- attn_fwd for callers that must not allocate device
+ * memory on the call path.
+ *
+ * No counterpart on the pages this library follows: this entry point exists
+ * for callers, not for the method.  attn_fwd allocates a status word and a
+ * block-mask buffer on first use (and grows the buffer, with a device-wide
+ * synchronisation, when a larger problem arrives).  Callers that cannot do
+ * that -- code running while a stream is captured into a CUDA graph,
+ * runtimes that own all device memory through their own pool or budget,
+ * latency-critical paths that cannot take the synchronisation of
+ * cudaMalloc/cudaFree -- use this entry point instead.  It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *
+ * Arguments, layouts, results and errors are those of attn_fwd, except:
+ *  - mod->block_mask must be NULL (the block mask is always built by the
+ *    call), else ATTN_ERR_INVALID_ARG;
+ *  - its scratch (status word and block mask) lives in one fixed array of
+ *    ATTN_NOALLOC_SCRATCH_BYTES bytes in the library, which every GPU that
+ *    loads the library holds until the process exits.  A problem whose
+ *    block mask needs more (about 4 * nP * nK bytes per mask batch, with
+ *    nK = ceil(S_k / 128) and nP = ceil(S_q / 256); e.g. S_q = S_k = 131072
+ *    needs 2 MiB) is rejected with ATTN_ERR_UNSUPPORTED before anything is
+ *    enqueued;
+ *  - the first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress, which may load the library's device code);
+ *    make that first call before any stream capture begins;
+ *  - every call on a device shares the one array and leaves its contents
+ *    behind (each call clears the status word and rewrites the block mask
+ *    before its forward kernel runs), so calls whose work overlaps on the
+ *    GPU -- on different streams, or from different threads without
+ *    ordering -- race and may produce wrong results;
+ *  - device-side failures (a pipeline wait that ran out of time) are
+ *    recorded in that array's status word, which attn_get_device_status
+ *    does not read; the outputs of such a call are unspecified.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+attn_status attn_fwd_noalloc(const void *q, const void *k, const void *v,
+                             void *out, float *lse, int B, int H, int H_kv,
+                             int S_q, int S_k, int D, float scale,
+                             const attn_mod_desc *mod, attn_stream_t stream);
+
 /* Tuning options.  Process-wide; set them before enqueuing work. */
 typedef enum attn_option {
     /* Rescale O only when the running row max grows by more than this many
