@@ -53,11 +53,7 @@ constexpr int kThreads = 384;
 constexpr int kRegsSoftmax = 216;
 constexpr int kRegsProducer = 72;
 static_assert(256 * kRegsSoftmax + 128 * kRegsProducer <= kThreads * 168, "register split");
-// Release P to the MMA warp in two halves (keys 0-63, 64-127) so the first
-// half of O += P V could start while the second half is still being computed.
-// Measured slower on GB300 (the extra Tensor Memory store wait sits on the
-// softmax critical path), so P is released whole.
-constexpr bool kSplitP = false;
+
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -87,9 +83,9 @@ struct Cfg {
   static constexpr int kSmemQ = 0;
   static constexpr int kSmemKV = kSmemQ + 2 * kTileBytes;
   static constexpr int kSmemBar = kSmemKV + kStages * kTileBytes;
-  // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2]
-  //           p_full[2][2] (per tile, per half of P) o_full[2] o_empty[2] drain
-  static constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 4 + 2 + 2 + 1;
+  // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2]
+  //           o_full[2] o_empty[2] drain
+  static constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 2 + 2 + 2 + 1;
   static constexpr int kSmemMisc = kSmemBar + 8 * kNumBars;
   static constexpr int kSmemDoc = (kSmemMisc + 16 + 15) / 16 * 16;  // int sdoc[2][128]
   static constexpr int kSmemBytes = kSmemDoc + 2 * kTileN * 4;
@@ -120,6 +116,7 @@ struct KParams {
   DeviceStatus* status;
   float tau;
   uint64_t budget_ns;
+  int poly_chunks;  // 16-column chunks per row (of 8) whose exp2 uses the polynomial
 };
 
 struct Ctl {
@@ -250,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   // ---- shared memory map ------------------------------------------------
   auto bar = [&](int i) { return sbase + (uint32_t)(C::kSmemBar + 8 * i); };
   const int B_QF = 0, B_QE = 2, B_KVF = 4, B_KVE = 4 + C::kStages, B_SF = 4 + 2 * C::kStages,
-            B_PF = B_SF + 2, B_OF = B_PF + 4, B_OE = B_OF + 2, B_DRAIN = B_OE + 2;
+            B_PF = B_SF + 2, B_OF = B_PF + 2, B_OE = B_OF + 2, B_DRAIN = B_OE + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kSmemMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kSmemMisc + 4);
   volatile int* s_turn = reinterpret_cast<volatile int*>(smem + C::kSmemMisc + 8);
@@ -267,8 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(bar(B_SF + t), 1);
-      ptx::mbar_init(bar(B_PF + 2 * t), 4);  // one arrival per softmax warp
-      ptx::mbar_init(bar(B_PF + 2 * t + 1), 4);
+      ptx::mbar_init(bar(B_PF + t), 4);  // one arrival per softmax warp
       ptx::mbar_init(bar(B_OF + t), 1);
       ptx::mbar_init(bar(B_OE + t), 4);
     }
@@ -427,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const uint32_t vi = k0 + 2 * j + 1;  // V_j
           const uint32_t ki = k0 + 2 * j + 2;  // K_{j+1}
           const bool has_next = j + 1 < n;
-          ok = wait_bar(bar(B_PF + 2 * t), p_cnt & 1, ctl, kSiteMmaPFull) &&
+          ok = wait_bar(bar(B_PF + t), p_cnt & 1, ctl, kSiteMmaPFull) &&
                wait_bar(kv_full(vi), kv_par(vi), ctl, kSiteMmaKvFull);
           if (ok && j == 0 && act > 0)
             ok = wait_bar(bar(B_OE + t), (act - 1) & 1, ctl, kSiteMmaOEmpty);
@@ -548,16 +544,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           uint32_t z[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) z[c] = 0u;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            ptx::tmem_st32(tS + (uint32_t)(h * 32), z);
-            if (kSplitP || h == 1) {
-              ptx::tmem_wait_st();
-              ptx::tc_fence_before();
-              __syncwarp();
-              if (lane == 0) ptx::mbar_arrive(bar(B_PF + 2 * t + (kSplitP ? h : 0)));
-            }
-          }
+          ptx::tmem_st32(tS, z);
+          ptx::tmem_st32(tS + 32u, z);
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bar(B_PF + t));
         } else {
           float tv[kTileN];
           {
@@ -646,28 +638,62 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             }
           }
           const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-          // exponentials, row sum, bf16 P written over S; each half of P
-          // is released to the MMA warp as soon as it is in Tensor Memory
+          // exponentials, row sum, bf16 P written over S.  The first
+          // poly_chunks 16-column chunks of the row evaluate exp2 with the
+          // FMA polynomial, the rest with the hardware unit ("FlashAttention-4
+          // explained", "Forward pass fixes", "Software-emulated
+          // exponentials"); the choice is uniform across the warp.
           float la[4] = {0.f, 0.f, 0.f, 0.f};
+          const int npc = p.poly_chunks;
+          if (npc == 0) {
+            // hardware exp2 only: one straight-line loop (the chunked form
+            // below schedules measurably worse)
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              uint32_t pk[32];
+#pragma unroll
+              for (int c = 0; c < 32; ++c) {
+                const float pa = ptx::ex2_approx(fmaf(tv[h2 * 64 + 2 * c], xs, -m_use));
+                const float pb = ptx::ex2_approx(fmaf(tv[h2 * 64 + 2 * c + 1], xs, -m_use));
+                la[(c & 1) * 2] += pa;
+                la[(c & 1) * 2 + 1] += pb;
+                pk[c] = ptx::pack_bf16x2(pa, pb);
+              }
+              ptx::tmem_st32(tS + (uint32_t)(h2 * 32), pk);
+            }
+          } else {
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {
             uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              const float pa = ptx::ex2_approx(fmaf(tv[h2 * 64 + 2 * c], xs, -m_use));
-              const float pb = ptx::ex2_approx(fmaf(tv[h2 * 64 + 2 * c + 1], xs, -m_use));
-              la[(c & 1) * 2] += pa;
-              la[(c & 1) * 2 + 1] += pb;
-              pk[c] = ptx::pack_bf16x2(pa, pb);
+            for (int q4 = 0; q4 < 4; ++q4) {
+              if (h2 * 4 + q4 < npc) {
+#pragma unroll
+                for (int c = q4 * 8; c < q4 * 8 + 8; ++c) {
+                  const float pa = ptx::exp2_poly(fmaf(tv[h2 * 64 + 2 * c], xs, -m_use));
+                  const float pb = ptx::exp2_poly(fmaf(tv[h2 * 64 + 2 * c + 1], xs, -m_use));
+                  la[(c & 1) * 2] += pa;
+                  la[(c & 1) * 2 + 1] += pb;
+                  pk[c] = ptx::pack_bf16x2(pa, pb);
+                }
+              } else {
+#pragma unroll
+                for (int c = q4 * 8; c < q4 * 8 + 8; ++c) {
+                  const float pa = ptx::ex2_approx(fmaf(tv[h2 * 64 + 2 * c], xs, -m_use));
+                  const float pb = ptx::ex2_approx(fmaf(tv[h2 * 64 + 2 * c + 1], xs, -m_use));
+                  la[(c & 1) * 2] += pa;
+                  la[(c & 1) * 2 + 1] += pb;
+                  pk[c] = ptx::pack_bf16x2(pa, pb);
+                }
+              }
             }
             ptx::tmem_st32(tS + (uint32_t)(h2 * 32), pk);
-            if (kSplitP || h2 == 1) {
-              ptx::tmem_wait_st();
-              ptx::tc_fence_before();
-              __syncwarp();
-              if (lane == 0) ptx::mbar_arrive(bar(B_PF + 2 * t + (kSplitP ? h2 : 0)));
-            }
           }
+          }
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bar(B_PF + t));
           l += (la[0] + la[1]) + (la[2] + la[3]);
         }
       }
@@ -680,7 +706,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (!ok) break;
       }
       ptx::tc_fence_after();
-      const float inv_l = (l > 0.f) ? 1.0f / l : 0.f;
+      // A row that never saw a visible key keeps m_ref = -inf: O = 0 and
+      // LSE = -inf (l itself may hold the polynomial's tiny values).
+      const bool seen = m_ref != -INFINITY && l > 0.f;
+      const float inv_l = seen ? 1.0f / l : 0.f;
 #pragma unroll
       for (int c4 = 0; c4 < D / 32; ++c4) {
         uint32_t o[32];
@@ -701,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(B_OE + t));
-      if (valid && p.lse) p.lse[row_id] = (l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+      if (valid && p.lse) p.lse[row_id] = seen ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
       ++act;
     }
   }
@@ -809,6 +838,9 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
   kp.status = a.status;
   kp.tau = a.rescale_threshold;
   kp.budget_ns = (uint64_t)(a.wait_budget_ms * 1.0e6);
+  kp.poly_chunks = (int)lrintf(a.poly_fraction * 8.0f);
+  if (kp.poly_chunks < 0) kp.poly_chunks = 0;
+  if (kp.poly_chunks > 8) kp.poly_chunks = 8;
 
   int dev = 0, sms = 0;
   cudaError_t err = cudaGetDevice(&dev);

@@ -264,7 +264,9 @@ typedef enum attn_option {
     /* Persistent CTAs to launch; 0 (default) = one per SM. */
     ATTN_OPT_NUM_CTAS = 4,
     /* Fraction of the softmax exponentials evaluated with an FMA polynomial
-     * instead of the hardware exp2 unit, in [0, 1] (default 0).
+     * instead of the hardware exp2 unit, in [0, 1] (default 0), applied in
+     * steps of 1/8 of each row's 128 columns.  Relative error of the
+     * polynomial is below 1e-4, far under the bf16 rounding of P.
      * "FlashAttention-4 explained", "Forward pass fixes",
      * "Software-emulated exponentials". */
     ATTN_OPT_EXP_POLY_FRACTION = 5

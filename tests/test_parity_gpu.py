@@ -275,6 +275,23 @@ def test_rescale_threshold_does_not_change_results(attn, tau):
         attn.set_option("rescale_threshold", old)
 
 
+@pytest.mark.parametrize("frac", [0.5, 1.0])
+def test_exp2_polynomial_path(attn, frac):
+    # Part or all of the softmax exponentials on the FMA polynomial: the
+    # same tolerances as the hardware-unit path, including rows without any
+    # visible key (q_offset < 0) and the score mods.
+    old = attn.get_option("exp_poly_fraction")
+    try:
+        attn.set_option("exp_poly_fraction", frac)
+        for case, mods in enumerate(({"causal": True, "q_offset": -100}, {},
+                                     {"causal": True, "alibi": True, "softcap": 20.0},
+                                     {"window": 200})):
+            q, k, v = rand_inputs(1, 2, 2, 520, 520, 128, seed=60 + case)
+            run_and_compare(attn, q, k, v, 1 / math.sqrt(128), **mods)
+    finally:
+        attn.set_option("exp_poly_fraction", old)
+
+
 def test_prebuilt_block_mask_matches_internal(attn):
     B, H, S, D = 2, 4, 900, 128
     q, k, v = rand_inputs(B, H, H, S, S, D, seed=13)
