@@ -185,33 +185,38 @@ __device__ __forceinline__ int item_of(int r) {
   return r * G + ((r & 1) ? (G - 1 - c) : c);
 }
 
+// Descriptor bits that do not depend on the start address: K-major tiles
+// (Q, K) and the MN-major V tile.  A full descriptor is this constant plus
+// (smem address >> 4); all addresses are below 256 KB, so the 14-bit start
+// field never carries into the other fields.
 template <int D>
-__device__ __forceinline__ void issue_s(uint32_t tmem_s, uint32_t q_base, uint32_t k_base) {
+struct Desc {
+  static constexpr uint64_t kKMajor = ptx::smem_desc_sw128(0, 16, 1024);
+  static constexpr uint64_t kVMajor = ptx::smem_desc_sw128(0, Cfg<D>::kHalfBytes, 1024);
+};
+
+// S = Q K^T: D/16 MMAs (K = 16 each) over the two 64-column halves of the
+// swizzled tiles.  Warp-wide; one elected lane issues.
+template <int D>
+__device__ __forceinline__ void issue_s(uint32_t tmem_s, uint64_t q_desc, uint64_t k_desc) {
   constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTileM, kTileN, false);
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t off = (uint32_t)((kk / 4) * Cfg<D>::kHalfBytes + (kk % 4) * 32);
-    const uint64_t a = ptx::smem_desc_sw128(q_base + off, 16, 1024);
-    const uint64_t b = ptx::smem_desc_sw128(k_base + off, 16, 1024);
-    ptx::mma_ss(tmem_s, a, b, idesc, kk > 0 ? 1u : 0u);
+    const uint64_t off = (uint64_t)(((kk / 4) * Cfg<D>::kHalfBytes + (kk % 4) * 32) >> 4);
+    ptx::mma_ss_elect(tmem_s, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
-// O += P[:, 64h : 64h+64] V[64h : 64h+64, :] -- one half of the keys, so the
-// first half can start while the softmax still computes the second.
+// O (+)= P V: 8 MMAs of 16 keys (16 rows of V = 2 KB of the swizzled tile;
+// 8 packed bf16 columns of P in Tensor Memory).  Warp-wide.
 template <int D>
-__device__ __forceinline__ void issue_pv_half(uint32_t tmem_o, uint32_t tmem_p, uint32_t v_base,
-                                              int half, bool accumulate) {
+__device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint64_t v_desc,
+                                         bool accumulate) {
   constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTileM, D, true);
 #pragma unroll
-  for (int k4 = 0; k4 < 4; ++k4) {
-    const int kk = half * 4 + k4;
-    // 16 keys per MMA: 16 rows of V (2 KB of the swizzled tile), 8 packed
-    // bf16 columns of P.
-    const uint64_t b =
-        ptx::smem_desc_sw128(v_base + (uint32_t)(kk * 16 * 128), Cfg<D>::kHalfBytes, 1024);
-    ptx::mma_ts(tmem_o, tmem_p + (uint32_t)(kk * 8), b, idesc, (accumulate || kk > 0) ? 1u : 0u);
-  }
+  for (int kk = 0; kk < kTileN / 16; ++kk)
+    ptx::mma_ts_elect(tmem_o, tmem_p + (uint32_t)(kk * 8), v_desc + (uint64_t)((kk * 2048) >> 4),
+                      idesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 template <int D, bool ALIBI, bool SOFTCAP>
@@ -356,49 +361,67 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           }
         }
       }
-    } else if ((warp == kMmaWarp || warp == kMmaWarp + 1) && lane == 0) {
+    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
       // ===================== MMA issuers =================================
-      // Two issuing threads, one per query tile.  Issue blocks until the
-      // tensor pipe accepts the MMA and every mbarrier wait costs a few
-      // hundred cycles even when the phase is already complete, so a single
-      // issuer leaves the pipe idle during its waits; with one issuer per
-      // tile the other tile's MMAs fill those gaps.  Each tile's chain
+      // Two issuing warps, one per query tile.  tcgen05.mma issue blocks
+      // until the tensor pipe accepts the MMA, and every mbarrier wait costs
+      // a few hundred cycles even when the phase is already complete, so a
+      // single issuer leaves the pipe idle during its waits; with one issuer
+      // per tile the other tile's MMAs fill those gaps.  Each tile's chain
       //   S_t(0), PV_t(0), S_t(1), PV_t(1), ...
-      // stays in issue order on one thread, which keeps the P_t / S_t
-      // aliasing safe.  K/V stages are released once both issuers commit.
-      // A turn token makes the two tiles' MMA groups alternate on the pipe
-      // (tile 0 group k, tile 1 group k, tile 0 group k+1, ...) so that each
-      // tile's S finishes as early as in a strict ping-pong; an issuer does
-      // its barrier waits while the other one issues, then takes its turn.
+      // stays in issue order on one warp, which keeps the P_t / S_t aliasing
+      // safe.  K/V stages are released once both issuers commit.  A turn
+      // token makes the two tiles' MMA groups alternate on the pipe (tile 0
+      // group k, tile 1 group k, tile 0 group k+1, ...) so each tile's S
+      // finishes as early as in a strict ping-pong; an issuer does its
+      // barrier waits while the other one issues, then takes its turn.
       // Every group waits only on earlier groups, so the order cannot
-      // deadlock.
+      // deadlock.  The loop is warp-uniform (all lanes wait and compute the
+      // same descriptors, one elected lane issues), which keeps descriptors
+      // in uniform registers and the MMAs back to back.
       const int t = warp - kMmaWarp;
+      const uint32_t tS = tmem + (uint32_t)(t * kTileN);
+      const uint32_t tO = tmem + (uint32_t)(C::kOCol + t * D);
+      const uint64_t q_desc = Desc<D>::kKMajor + ((sbase + C::kSmemQ + t * C::kTileBytes) >> 4);
+      const uint64_t kv0 = (sbase + C::kSmemKV) >> 4;
+      auto stage = [&](uint32_t idx) { return idx % C::kStages; };
+      auto k_desc = [&](uint32_t idx) {
+        return Desc<D>::kKMajor + kv0 + (uint64_t)(stage(idx) * (C::kTileBytes >> 4));
+      };
+      auto v_desc = [&](uint32_t idx) {
+        return Desc<D>::kVMajor + kv0 + (uint64_t)(stage(idx) * (C::kTileBytes >> 4));
+      };
+      auto kv_full = [&](uint32_t idx) { return bar(B_KVF + (int)stage(idx)); };
+      auto kv_empty = [&](uint32_t idx) { return bar(B_KVE + (int)stage(idx)); };
+      auto kv_par = [&](uint32_t idx) { return (idx / C::kStages) & 1; };
+      auto wait_all = [&](uint32_t b, uint32_t par, int site) {
+        return __all_sync(0xffffffffu, wait_bar(b, par, ctl, site));
+      };
       int grp = 0;  // groups this issuer has issued
       auto take_turn = [&]() -> bool {
         const int want = 2 * grp + t;
-        if (*s_turn == want) return true;
-        const uint64_t t0 = ptx::globaltimer_ns();
-        for (uint32_t spin = 1;; ++spin) {
-          if (*s_turn == want) return true;
-          if ((spin & 255) == 0) {
-            if (*s_abort) return false;
-            if (ptx::globaltimer_ns() - t0 > p.budget_ns) {
-              report(ctl, ATTN_ERR_TIMEOUT, kSiteMmaTurn, want);
-              return false;
+        bool got = true;
+        if (*s_turn != want) {
+          const uint64_t t0 = ptx::globaltimer_ns();
+          for (uint32_t spin = 1;; ++spin) {
+            if (*s_turn == want) break;
+            if ((spin & 255) == 0) {
+              if (*s_abort) { got = false; break; }
+              if (ptx::globaltimer_ns() - t0 > p.budget_ns) {
+                if (lane == 0) report(ctl, ATTN_ERR_TIMEOUT, kSiteMmaTurn, want);
+                got = false;
+                break;
+              }
             }
           }
         }
+        return __all_sync(0xffffffffu, got);
       };
-      auto pass_turn = [&]() { *s_turn = 2 * grp + t + 1; ++grp; };
-      const uint32_t tS = tmem + (uint32_t)(t * kTileN);
-      const uint32_t tO = tmem + (uint32_t)(C::kOCol + t * D);
-      const uint32_t sQ = sbase + (uint32_t)(C::kSmemQ + t * C::kTileBytes);
-      auto sKV = [&](uint32_t idx) {
-        return sbase + (uint32_t)C::kSmemKV + (idx % C::kStages) * (uint32_t)C::kTileBytes;
+      auto pass_turn = [&]() {
+        __syncwarp();
+        if (lane == 0) *s_turn = 2 * grp + t + 1;
+        ++grp;
       };
-      auto kv_full = [&](uint32_t idx) { return bar(B_KVF + (int)(idx % C::kStages)); };
-      auto kv_empty = [&](uint32_t idx) { return bar(B_KVE + (int)(idx % C::kStages)); };
-      auto kv_par = [&](uint32_t idx) { return (idx / C::kStages) & 1; };
       uint32_t kv_cnt = 0;
       uint32_t p_cnt = 0;
       int act = 0;
@@ -410,53 +433,55 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const int n = p.cnt[it.e];
         if (n == 0) continue;
         const uint32_t k0 = kv_cnt;
-        ok = wait_bar(bar(B_QF + t), act & 1, ctl, kSiteMmaQFull) &&
-             wait_bar(kv_full(k0), kv_par(k0), ctl, kSiteMmaKvFull) && take_turn();
+        ok = wait_all(bar(B_QF + t), act & 1, kSiteMmaQFull) &&
+             wait_all(kv_full(k0), kv_par(k0), kSiteMmaKvFull) && take_turn();
         if (!ok) break;
         ptx::tc_fence_after();
-        issue_s<D>(tS, sQ, sKV(k0));
+        issue_s<D>(tS, q_desc, k_desc(k0));
         pass_turn();
-        ptx::mma_commit(bar(B_SF + t));
-        if (n == 1) ptx::mma_commit(bar(B_QE + t));
-        ptx::mma_commit(kv_empty(k0));
+        ptx::mma_commit_elect(bar(B_SF + t));
+        if (n == 1) ptx::mma_commit_elect(bar(B_QE + t));
+        ptx::mma_commit_elect(kv_empty(k0));
         for (int j = 0; j < n && ok; ++j) {
           const uint32_t vi = k0 + 2 * j + 1;  // V_j
           const uint32_t ki = k0 + 2 * j + 2;  // K_{j+1}
           const bool has_next = j + 1 < n;
-          ok = wait_bar(bar(B_PF + t), p_cnt & 1, ctl, kSiteMmaPFull) &&
-               wait_bar(kv_full(vi), kv_par(vi), ctl, kSiteMmaKvFull);
-          if (ok && j == 0 && act > 0)
-            ok = wait_bar(bar(B_OE + t), (act - 1) & 1, ctl, kSiteMmaOEmpty);
-          if (ok && has_next) ok = wait_bar(kv_full(ki), kv_par(ki), ctl, kSiteMmaKvFull);
+          ok = wait_all(bar(B_PF + t), p_cnt & 1, kSiteMmaPFull) &&
+               wait_all(kv_full(vi), kv_par(vi), kSiteMmaKvFull);
+          if (ok && j == 0 && act > 0) ok = wait_all(bar(B_OE + t), (act - 1) & 1, kSiteMmaOEmpty);
+          if (ok && has_next) ok = wait_all(kv_full(ki), kv_par(ki), kSiteMmaKvFull);
           if (ok) ok = take_turn();
           if (!ok) break;
           ++p_cnt;
           ptx::tc_fence_after();
-          issue_pv_half<D>(tO, tS, sKV(vi), 0, j > 0);
-          issue_pv_half<D>(tO, tS, sKV(vi), 1, true);
-          if (has_next) issue_s<D>(tS, sQ, sKV(ki));
+          issue_pv<D>(tO, tS, v_desc(vi), j > 0);
+          if (has_next) issue_s<D>(tS, q_desc, k_desc(ki));
           pass_turn();
-          ptx::mma_commit(kv_empty(vi));
+          ptx::mma_commit_elect(kv_empty(vi));
           if (has_next) {
-            ptx::mma_commit(bar(B_SF + t));
-            if (j + 2 == n) ptx::mma_commit(bar(B_QE + t));
-            ptx::mma_commit(kv_empty(ki));
+            ptx::mma_commit_elect(bar(B_SF + t));
+            if (j + 2 == n) ptx::mma_commit_elect(bar(B_QE + t));
+            ptx::mma_commit_elect(kv_empty(ki));
           } else {
-            ptx::mma_commit(bar(B_OF + t));
+            ptx::mma_commit_elect(bar(B_OF + t));
           }
         }
         kv_cnt = k0 + 2 * (uint32_t)n;
         ++act;
       }
       // Wait for every MMA of both issuers before Tensor Memory is freed.
-      ptx::mma_commit(bar(B_DRAIN));
+      __syncwarp();
+      ptx::mma_commit_elect(bar(B_DRAIN));
       const uint64_t t0 = ptx::globaltimer_ns();
+      bool drained = true;
       while (!ptx::mbar_try_wait(bar(B_DRAIN), 0)) {
         if (ptx::globaltimer_ns() - t0 > p.budget_ns) {
-          report(ctl, ATTN_ERR_TIMEOUT, kSiteMmaDrain, 0);
+          drained = false;
           break;
         }
       }
+      if (!__all_sync(0xffffffffu, drained) && lane == 0)
+        report(ctl, ATTN_ERR_TIMEOUT, kSiteMmaDrain, 0);
     }
   } else {
     ptx::setmaxnreg_inc<kRegsSoftmax>();
@@ -647,20 +672,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const int npc = p.poly_chunks;
           if (npc == 0) {
             // hardware exp2 only: one straight-line loop (the chunked form
-            // below schedules measurably worse)
+            // below schedules measurably worse).  The softmax is bound by
+            // instruction issue, so the scale-and-subtract and the row sum use
+            // paired fp32 instructions (two columns per instruction).
+            const uint64_t xs2 = ptx::f2(xs, xs), nm2 = ptx::f2(-m_use, -m_use);
+            uint64_t acc2[2] = {0ull, 0ull};
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
               uint32_t pk[32];
 #pragma unroll
               for (int c = 0; c < 32; ++c) {
-                const float pa = ptx::ex2_approx(fmaf(tv[h2 * 64 + 2 * c], xs, -m_use));
-                const float pb = ptx::ex2_approx(fmaf(tv[h2 * 64 + 2 * c + 1], xs, -m_use));
-                la[(c & 1) * 2] += pa;
-                la[(c & 1) * 2 + 1] += pb;
+                float pa, pb;
+                ptx::f2_split(ptx::ffma2(ptx::f2(tv[h2 * 64 + 2 * c], tv[h2 * 64 + 2 * c + 1]),
+                                         xs2, nm2),
+                              pa, pb);
+                pa = ptx::ex2_approx(pa);
+                pb = ptx::ex2_approx(pb);
+                acc2[c & 1] = ptx::fadd2(acc2[c & 1], ptx::f2(pa, pb));
                 pk[c] = ptx::pack_bf16x2(pa, pb);
               }
               ptx::tmem_st32(tS + (uint32_t)(h2 * 32), pk);
             }
+            ptx::f2_split(acc2[0], la[0], la[1]);
+            ptx::f2_split(acc2[1], la[2], la[3]);
           } else {
 #pragma unroll
           for (int h2 = 0; h2 < 2; ++h2) {

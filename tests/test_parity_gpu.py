@@ -275,6 +275,25 @@ def test_rescale_threshold_does_not_change_results(attn, tau):
         attn.set_option("rescale_threshold", old)
 
 
+@pytest.mark.parametrize("mods", [{"causal": True}, {"causal": True, "alibi": True},
+                                  {"causal": True, "softcap": 30.0}])
+def test_late_large_score_forces_rescale(attn, mods):
+    # Key 0 scores ~10 above every other key.  Key tiles are processed from
+    # the diagonal down, so rows past the first tile meet key 0 last: their
+    # max jumps by far more than the rescale threshold on that tile, which
+    # forces the tile to be redone and O to be rescaled.
+    B, H, S, D = 1, 2, 700, 128
+    q, k, v = rand_inputs(B, H, H, S, S, D, seed=70)
+    q = q.float()
+    q[..., 0] += 2.0
+    q = q.to(torch.bfloat16)
+    k = k.float()
+    k[:, :, 0, :] = 0.0
+    k[:, :, 0, 0] = 60.0
+    k = k.to(torch.bfloat16)
+    run_and_compare(attn, q, k, v, 1 / math.sqrt(D), **mods)
+
+
 @pytest.mark.parametrize("frac", [0.5, 1.0])
 def test_exp2_polynomial_path(attn, frac):
     # Part or all of the softmax exponentials on the FMA polynomial: the
