@@ -405,6 +405,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const uint64_t t0 = ptx::globaltimer_ns();
           for (uint32_t spin = 1;; ++spin) {
             if (*s_turn == want) break;
+            // back off: a tight poll steals issue slots from the two softmax
+            // warps that share this SM sub-partition
+            __nanosleep(32);
             if ((spin & 255) == 0) {
               if (*s_abort) { got = false; break; }
               if (ptx::globaltimer_ns() - t0 > p.budget_ns) {
@@ -595,16 +598,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           }
           // score mods
           if constexpr (ALIBI || SOFTCAP) {
+            // paired fp32 instructions, two columns at a time
             const float b0 = ALIBI ? slope2 * (float)(j0 - qpos) : 0.f;
+            const uint64_t sc2 = ptx::f2(sc, sc), sl2 = ptx::f2(slope2, slope2),
+                           b02 = ptx::f2(b0, b0), one2 = ptx::f2(1.0f, 1.0f),
+                           m2c2 = ptx::f2(-2.0f * capl2, -2.0f * capl2),
+                           c2 = ptx::f2(capl2, capl2);
 #pragma unroll
-            for (int c = 0; c < kTileN; ++c) {
-              const float bias = ALIBI ? fmaf(slope2, (float)c, b0) : 0.f;
-              float x = fmaf(tv[c], sc, bias);
+            for (int c = 0; c < kTileN; c += 2) {
+              const uint64_t bias2 =
+                  ALIBI ? ptx::ffma2(sl2, ptx::f2((float)c, (float)(c + 1)), b02) : 0ull;
+              uint64_t x2 = ptx::ffma2(ptx::f2(tv[c], tv[c + 1]), sc2, bias2);
               if constexpr (SOFTCAP) {
-                const float e = ptx::ex2_approx(x);
-                x = fmaf(-2.0f * capl2, ptx::rcp_approx(e + 1.0f), capl2);
+                float ea, eb;
+                ptx::f2_split(x2, ea, eb);
+                ea = ptx::ex2_approx(ea);
+                eb = ptx::ex2_approx(eb);
+                float da, db;
+                ptx::f2_split(ptx::fadd2(ptx::f2(ea, eb), one2), da, db);
+                x2 = ptx::ffma2(m2c2, ptx::f2(ptx::rcp_approx(da), ptx::rcp_approx(db)), c2);
               }
-              tv[c] = x;
+              ptx::f2_split(x2, tv[c], tv[c + 1]);
             }
           }
           // mask (partial tiles only)
