@@ -339,7 +339,7 @@ def get_option(name: str) -> float:
     return v.value
 
 
-_HDR_FMT = "<IIiiiiiiiiIiiiiiQQQQQQ"  # mirrors the device block-mask header
+_HDR_FMT = "<IIiiiiiiiiIiiiiiQQQQQQQii"  # mirrors the device block-mask header
 
 
 def decode_block_mask(bm: BlockMask) -> dict:
@@ -356,7 +356,8 @@ def decode_block_mask(bm: BlockMask) -> dict:
     f = struct.unpack(_HDR_FMT, raw[:hsz].tobytes())
     keys = ("magic", "version", "B", "S_q", "S_k", "nQ", "nK", "nP", "bm", "n_entries",
             "mask_flags", "window", "q_offset", "force_partial", "uniform", "max_cnt",
-            "doc_ptr", "prefix_ptr", "order_off", "cnt_off", "list_off", "total_bytes")
+            "doc_ptr", "prefix_ptr", "order_off", "cnt_off", "list_off", "total_bytes",
+            "doc_off", "docs_sorted", "pad")
     h = dict(zip(keys, f))
     n, nK, nP, nQ = h["n_entries"], h["nK"], h["nP"], h["nQ"]
     order = raw[h["order_off"]:h["order_off"] + 4 * n].view(np.int32).copy()

@@ -111,6 +111,8 @@ struct KParams {
   const int32_t* order;
   const int32_t* cnt;
   const uint32_t* list;
+  const int32_t* doc_lo;  // [bm][S_k] first key of each token's document
+  const int32_t* doc_hi;  // [bm][S_k] last key
   int nK, nP, bm, n_entries, n_items;
   int force_partial;
   DeviceStatus* status;
@@ -248,6 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     return;
   }
   const int uniform = hdr->uniform;
+  const int docs_sorted = hdr->docs_sorted;
 
   // ---- shared memory map ------------------------------------------------
   auto bar = [&](int i) { return sbase + (uint32_t)(C::kSmemBar + 8 * i); };
@@ -529,7 +532,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         hi = min(hi, qpos);
       }
       if (p.mask_flags & ATTN_MASK_PREFIX_LM) hi = min(hi, max(qpos, p.prefix_len[it.b] - 1));
-      const bool has_doc = (p.mask_flags & ATTN_MASK_DOCUMENT) != 0;
+      // Documents: with packed (non-decreasing) ids the keys of row i's
+      // document form the interval [doc_lo[i], doc_hi[i]], folded into the
+      // row's bounds; other ids are compared element by element.
+      const bool has_doc = (p.mask_flags & ATTN_MASK_DOCUMENT) != 0 && !docs_sorted;
+      if ((p.mask_flags & ATTN_MASK_DOCUMENT) && docs_sorted && valid) {
+        const size_t di = (size_t)it.b * p.S_k + (size_t)i;
+        lo = max(lo, p.doc_lo[di]);
+        hi = min(hi, p.doc_hi[di]);
+      }
       const int* doc_b = has_doc ? p.doc_ids + (size_t)it.b * p.S_k : nullptr;
       const int doc_i = (has_doc && valid) ? doc_b[i] : 0;
       float slope2 = 0.f;  // ALiBi slope in the units of the transformed score
@@ -878,6 +889,10 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
   kp.order = reinterpret_cast<const int32_t*>(base + g.order_off);
   kp.cnt = reinterpret_cast<const int32_t*>(base + g.cnt_off);
   kp.list = reinterpret_cast<const uint32_t*>(base + g.list_off);
+  if (g.doc_off != 0) {
+    kp.doc_lo = reinterpret_cast<const int32_t*>(base + g.doc_off);
+    kp.doc_hi = kp.doc_lo + (size_t)g.bm * a.S_k;
+  }
   kp.nK = g.nK;
   kp.nP = g.nP;
   kp.bm = g.bm;

@@ -49,12 +49,18 @@ struct BlockMaskHeader {
   uint64_t prefix_ptr;
   uint64_t order_off, cnt_off, list_off;  // byte offsets from the header
   uint64_t total_bytes;
+  uint64_t doc_off;         // DOCUMENT: int32 doc_lo[bm][S_k], doc_hi[bm][S_k]
+  int32_t docs_sorted;      // 1: every batch's doc ids are non-decreasing
+  int32_t pad_;
 };
 static_assert(sizeof(BlockMaskHeader) % 16 == 0, "header alignment");
 
 struct BlockMaskGeom {
   int nQ, nK, nP, bm, n_entries;
-  size_t order_off, cnt_off, list_off, total;
+  size_t order_off, cnt_off, list_off;
+  size_t doc_off;   // DOCUMENT only: per-token document key interval
+  size_t flag_off;  // DOCUMENT only: int32 "ids out of order" flag
+  size_t total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -70,6 +76,14 @@ inline BlockMaskGeom block_mask_geom(int B, int S_q, int S_k, uint32_t mask_flag
   g.cnt_off = align_up(g.order_off + sizeof(int32_t) * (size_t)g.n_entries, 16);
   g.list_off = align_up(g.cnt_off + sizeof(int32_t) * (size_t)g.n_entries, 16);
   g.total = align_up(g.list_off + sizeof(uint32_t) * (size_t)g.n_entries * (size_t)g.nK, 16);
+  g.doc_off = g.flag_off = 0;
+  if (mask_flags & ATTN_MASK_DOCUMENT) {
+    // [bm][S_k] first and last key of each token's document (valid when the
+    // ids are non-decreasing), then the out-of-order flag
+    g.doc_off = g.total;
+    g.flag_off = align_up(g.doc_off + 2 * sizeof(int32_t) * (size_t)g.bm * (size_t)S_k, 16);
+    g.total = g.flag_off + 16;
+  }
   return g;
 }
 

@@ -80,19 +80,17 @@ __device__ Range doc_range(const int32_t* ids, int a, int e) {
 // One block per (batch entry, query-tile pair).  Writes cnt[e] and the
 // compacted list of non-empty key tiles in descending key-tile order.
 __global__ void __launch_bounds__(kBuildThreads) classify_kernel(BlockMaskHeader* hdr_out,
-                                                                  MaskParams mp, int B, int nQ,
-                                                                  int nK, int nP, int bm,
+                                                                  MaskParams mp, BlockMaskGeom g,
                                                                   int force_partial) {
+  const int nQ = g.nQ, nK = g.nK, nP = g.nP;
   const int e = blockIdx.x;
   const int bb = e / nP;  // batch of this entry (0 when the mask is batch-independent)
   const int p = e % nP;
   char* base = reinterpret_cast<char*>(hdr_out);
-  // offsets as in block_mask_geom()
-  size_t order_off = (sizeof(BlockMaskHeader) + 15) / 16 * 16;
-  size_t cnt_off = (order_off + sizeof(int32_t) * (size_t)bm * nP + 15) / 16 * 16;
-  size_t list_off = (cnt_off + sizeof(int32_t) * (size_t)bm * nP + 15) / 16 * 16;
-  int32_t* cnt = reinterpret_cast<int32_t*>(base + cnt_off);
-  uint32_t* list = reinterpret_cast<uint32_t*>(base + list_off) + (size_t)e * nK;
+  int32_t* cnt = reinterpret_cast<int32_t*>(base + g.cnt_off);
+  uint32_t* list = reinterpret_cast<uint32_t*>(base + g.list_off) + (size_t)e * nK;
+  if (e == 0 && threadIdx.x == 0 && g.flag_off != 0)
+    *reinterpret_cast<int32_t*>(base + g.flag_off) = 0;  // set by doc_ranges_kernel
 
   __shared__ Range s_dq[2];
   __shared__ int s_total;
@@ -144,21 +142,49 @@ __global__ void __launch_bounds__(kBuildThreads) classify_kernel(BlockMaskHeader
     __syncthreads();
   }
   if (threadIdx.x == 0) cnt[e] = s_total;
-  (void)B;
+}
+
+// For every token of every mask batch: the first and last key of its
+// document, by binary search over the ids (meaningful when the ids are
+// non-decreasing, i.e. packed documents), and a flag raised when some
+// batch's ids are out of order.  With packed ids, "key j is in query i's
+// document" is exactly j in [doc_lo[i], doc_hi[i]].
+__global__ void __launch_bounds__(kBuildThreads) doc_ranges_kernel(const int32_t* ids, int S,
+                                                                    int bm, char* base,
+                                                                    BlockMaskGeom g) {
+  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (long long)bm * S) return;
+  const int b = (int)(idx / S), i = (int)(idx % S);
+  const int32_t* row = ids + (size_t)b * S;
+  const int32_t x = row[i];
+  if (i + 1 < S && row[i + 1] < x) atomicOr(reinterpret_cast<int32_t*>(base + g.flag_off), 1);
+  int lo = 0, hi = S;  // first position with row[pos] >= x
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (row[mid] < x) lo = mid + 1; else hi = mid;
+  }
+  const int first = lo;
+  lo = i;
+  hi = S;  // first position with row[pos] > x, searching from i
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (row[mid] <= x) lo = mid + 1; else hi = mid;
+  }
+  int32_t* dlo = reinterpret_cast<int32_t*>(base + g.doc_off);
+  dlo[idx] = first;
+  dlo[(size_t)bm * S + idx] = lo - 1;
 }
 
 // order[]: entries sorted by descending count (ties by entry index), so the
 // heaviest work is scheduled first.  Block 0 also fills the header.
 __global__ void __launch_bounds__(kBuildThreads) order_kernel(BlockMaskHeader* hdr, int B,
-                                                              MaskParams mp, int nQ, int nK,
-                                                              int nP, int bm, int force_partial) {
+                                                              MaskParams mp, BlockMaskGeom g,
+                                                              int force_partial) {
+  const int nQ = g.nQ, nK = g.nK, nP = g.nP, bm = g.bm;
   const int n = bm * nP;
   char* base = reinterpret_cast<char*>(hdr);
-  size_t order_off = (sizeof(BlockMaskHeader) + 15) / 16 * 16;
-  size_t cnt_off = (order_off + sizeof(int32_t) * (size_t)n + 15) / 16 * 16;
-  size_t list_off = (cnt_off + sizeof(int32_t) * (size_t)n + 15) / 16 * 16;
-  int32_t* order = reinterpret_cast<int32_t*>(base + order_off);
-  const int32_t* cnt = reinterpret_cast<const int32_t*>(base + cnt_off);
+  int32_t* order = reinterpret_cast<int32_t*>(base + g.order_off);
+  const int32_t* cnt = reinterpret_cast<const int32_t*>(base + g.cnt_off);
 
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   __shared__ int s_cnt[kBuildThreads];
@@ -199,10 +225,14 @@ __global__ void __launch_bounds__(kBuildThreads) order_kernel(BlockMaskHeader* h
     h.max_cnt = mx;
     h.doc_ptr = reinterpret_cast<uint64_t>(mp.doc_ids);
     h.prefix_ptr = reinterpret_cast<uint64_t>(mp.prefix_len);
-    h.order_off = order_off;
-    h.cnt_off = cnt_off;
-    h.list_off = list_off;
-    h.total_bytes = (list_off + sizeof(uint32_t) * (size_t)n * nK + 15) / 16 * 16;
+    h.order_off = g.order_off;
+    h.cnt_off = g.cnt_off;
+    h.list_off = g.list_off;
+    h.total_bytes = g.total;
+    h.doc_off = g.doc_off;
+    h.docs_sorted =
+        (g.flag_off != 0) ? (*reinterpret_cast<const int32_t*>(base + g.flag_off) == 0) : 0;
+    h.pad_ = 0;
     *hdr = h;
   }
 }
@@ -213,13 +243,18 @@ cudaError_t launch_build_block_mask(int B, int S_q, int S_k, const MaskParams& m
                                     int force_partial, void* dst, cudaStream_t stream) {
   BlockMaskGeom g = block_mask_geom(B, S_q, S_k, mp.flags);
   BlockMaskHeader* hdr = reinterpret_cast<BlockMaskHeader*>(dst);
-  classify_kernel<<<g.n_entries, kBuildThreads, 0, stream>>>(hdr, mp, B, g.nQ, g.nK, g.nP, g.bm,
-                                                             force_partial);
+  classify_kernel<<<g.n_entries, kBuildThreads, 0, stream>>>(hdr, mp, g, force_partial);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  if (g.flag_off != 0) {
+    const long long toks = (long long)g.bm * S_k;
+    doc_ranges_kernel<<<(unsigned)((toks + kBuildThreads - 1) / kBuildThreads), kBuildThreads, 0,
+                        stream>>>(mp.doc_ids, S_k, g.bm, reinterpret_cast<char*>(dst), g);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
   int blocks = (g.n_entries + kBuildThreads - 1) / kBuildThreads;
-  order_kernel<<<blocks, kBuildThreads, 0, stream>>>(hdr, B, mp, g.nQ, g.nK, g.nP, g.bm,
-                                                     force_partial);
+  order_kernel<<<blocks, kBuildThreads, 0, stream>>>(hdr, B, mp, g, force_partial);
   return cudaGetLastError();
 }
 

@@ -141,7 +141,10 @@ def test_unsorted_document_ids(attn):
     q, k, v = rand_inputs(B, H, H, S, S, D, seed=8)
     g = torch.Generator().manual_seed(4)
     doc_ids = torch.randint(0, 3, (1, S), generator=g).to(torch.int32)
+    bm = attn.build_block_mask(B, H, S, S, device=DEV, doc_ids=doc_ids.to(DEV))
+    assert attn.decode_block_mask(bm)["docs_sorted"] == 0  # element-wise equality path
     run_and_compare(attn, q, k, v, 0.125, doc_ids=doc_ids)
+    run_and_compare(attn, q, k, v, 0.125, doc_ids=doc_ids, causal=True)
 
 
 def test_explicit_alibi_slopes(attn):
@@ -200,6 +203,8 @@ def test_block_mask_exact(attn, case):
     want = expected_classes(B, S_q, S_k, mods)
     bm = attn.build_block_mask(B, 1, S_q, S_k, device=DEV, **to_dev(mods))
     got = attn.decode_block_mask(bm)
+    # packed ids take the interval form of the document mask
+    assert got["docs_sorted"] == (1 if "doc_ids" in mods else 0)
     cls = got["cls"]
     if cls.shape[0] == 1:  # batch-independent mask: stored once
         assert all(np.array_equal(want[0], w_) for w_ in want)
