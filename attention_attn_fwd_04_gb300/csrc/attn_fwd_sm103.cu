@@ -5,9 +5,10 @@
 //
 //   warps 0-3  softmax warpgroup for query tile 0 (one thread per row)
 //   warps 4-7  softmax warpgroup for query tile 1
-//   warp  8    TMA producer: Q tiles and a ring of K / V tiles
+//   warp  8    TMA producer: a ring of K / V tiles
 //   warp  9    Tensor Memory owner; MMA issuer for query tile 0
 //   warp 10    MMA issuer for query tile 1
+//   warp 11    TMA producer: Q tiles
 //
 // Per key tile j the tensor core computes S_t = Q_t K_j^T into Tensor Memory
 // (fp32), the softmax warpgroup of tile t turns S_t into P_t (bf16, written
@@ -42,13 +43,13 @@ namespace attn {
 namespace {
 
 // Three warpgroups: two softmax warpgroups and one producer warpgroup whose
-// warp 8 loads and warps 9 and 10 issue MMAs (warp 11 only hands its
-// registers to the softmax warpgroups).  384 threads launch with 168
+// warp 8 loads K/V, warps 9 and 10 issue MMAs and warp 11 loads Q.  384 threads launch with 168
 // registers each; the producer warpgroup drops to kRegsProducer and the
 // softmax warpgroups grow to kRegsSoftmax, which uses the same total:
 // 256 * 216 + 128 * 72 = 384 * 168.
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
+constexpr int kQLoadWarp = 11;
 constexpr int kThreads = 384;
 constexpr int kRegsSoftmax = 216;
 constexpr int kRegsProducer = 72;
@@ -296,17 +297,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     // Producer warpgroup: give registers away first (whole warpgroup).
     ptx::setmaxnreg_dec<kRegsProducer>();
     if (warp == kLoadWarp && lane == 0) {
-      // ===================== TMA producer ================================
-
-      ptx::prefetch_tmap(&p.tmap_q);
+      // ===================== TMA producer: K / V ring ====================
+      // Streams the key/value tiles of every item back to back, so the next
+      // item's first tiles load while the current item finishes.
       ptx::prefetch_tmap(&p.tmap_k);
       ptx::prefetch_tmap(&p.tmap_v);
       const uint64_t pol_kv = ptx::policy_evict_last();
-      const uint64_t pol_q = ptx::policy_evict_first();
       uint32_t kv_cnt = 0;
-      int act = 0;
       bool ok = true;
-      int q_phase[2] = {-1, -1};  // parity of the last Q_t load issued
       for (int r = 0; ok; ++r) {
         const int w = item_of(r);
         if (w >= p.n_items) break;
@@ -314,17 +312,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const int n = p.cnt[it.e];
         if (n == 0) continue;
         const uint32_t* lst = p.list + (size_t)it.e * p.nK;
-        for (int t = 0; t < 2 && ok; ++t) {
-          if (act > 0) ok = wait_bar(bar(B_QE + t), (act - 1) & 1, ctl, kSiteLoadQEmpty);
-          if (!ok) break;
-          const int row0 = (2 * it.pair + t) * kTileM;
-          ptx::mbar_arrive_expect_tx(bar(B_QF + t), C::kTileBytes);
-#pragma unroll
-          for (int hx = 0; hx < C::kHalves; ++hx)
-            ptx::tma_load_3d(sbase + C::kSmemQ + t * C::kTileBytes + hx * C::kHalfBytes,
-                             &p.tmap_q, bar(B_QF + t), hx * 64, row0, it.b * p.H + it.h, pol_q);
-          q_phase[t] = act & 1;
-        }
         const int kvz = it.b * p.H_kv + it.h / p.group;
         for (int j = 0; j < n && ok; ++j) {
           const int row0 = (int)entry_tile(lst[j]) * kTileN;
@@ -344,11 +331,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             ++kv_cnt;
           }
         }
-        ++act;
       }
       if (!ok) {
         // Let the copies already issued land before the CTA exits: wait (with
-        // a bound) for the last phase issued on every barrier still in use.
+        // a bound) for the last phase issued on every stage still in use.
         const uint32_t first = kv_cnt > (uint32_t)C::kStages ? kv_cnt - C::kStages : 0;
         for (uint32_t c = first; c < kv_cnt; ++c) {
           const uint64_t t0 = ptx::globaltimer_ns();
@@ -356,6 +342,35 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                  ptx::globaltimer_ns() - t0 < ctl.budget_ns) {
           }
         }
+      }
+    } else if (warp == kQLoadWarp && lane == 0) {
+      // ===================== TMA producer: Q tiles =======================
+      // Loads Q_t of the next item as soon as the last S_t MMA of the
+      // current item has read its buffer, independently of the K/V stream.
+      ptx::prefetch_tmap(&p.tmap_q);
+      const uint64_t pol_q = ptx::policy_evict_first();
+      int act = 0;
+      bool ok = true;
+      int q_phase[2] = {-1, -1};  // parity of the last Q_t load issued
+      for (int r = 0; ok; ++r) {
+        const int w = item_of(r);
+        if (w >= p.n_items) break;
+        const Item it = decode_item(p, w, uniform);
+        if (p.cnt[it.e] == 0) continue;
+        for (int t = 0; t < 2 && ok; ++t) {
+          if (act > 0) ok = wait_bar(bar(B_QE + t), (act - 1) & 1, ctl, kSiteLoadQEmpty);
+          if (!ok) break;
+          const int row0 = (2 * it.pair + t) * kTileM;
+          ptx::mbar_arrive_expect_tx(bar(B_QF + t), C::kTileBytes);
+#pragma unroll
+          for (int hx = 0; hx < C::kHalves; ++hx)
+            ptx::tma_load_3d(sbase + C::kSmemQ + t * C::kTileBytes + hx * C::kHalfBytes,
+                             &p.tmap_q, bar(B_QF + t), hx * 64, row0, it.b * p.H + it.h, pol_q);
+          q_phase[t] = act & 1;
+        }
+        ++act;
+      }
+      if (!ok) {
         for (int t = 0; t < 2; ++t) {
           if (q_phase[t] < 0) continue;
           const uint64_t t0 = ptx::globaltimer_ns();
