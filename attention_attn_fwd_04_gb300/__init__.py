@@ -52,12 +52,14 @@ OPT_FORCE_PARTIAL = 2
 OPT_WAIT_BUDGET_MS = 3
 OPT_NUM_CTAS = 4
 OPT_EXP_POLY_FRACTION = 5
+OPT_DEBUG_STALL = 6
 _OPTIONS = {
     "rescale_threshold": OPT_RESCALE_THRESHOLD,
     "force_partial": OPT_FORCE_PARTIAL,
     "wait_budget_ms": OPT_WAIT_BUDGET_MS,
     "num_ctas": OPT_NUM_CTAS,
     "exp_poly_fraction": OPT_EXP_POLY_FRACTION,
+    "debug_stall": OPT_DEBUG_STALL,
 }
 
 STATUS_NAMES = {

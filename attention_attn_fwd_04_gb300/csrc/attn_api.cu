@@ -21,6 +21,7 @@ struct Options {
   double wait_budget_ms = 2000.0;
   double num_ctas = 0.0;
   double poly_fraction = 0.0;
+  double debug_stall = 0.0;
 };
 Options g_opts;
 std::mutex g_opts_mu;
@@ -209,6 +210,10 @@ attn_status attn_set_option(attn_option opt, double value) {
       if (value < 0.0 || value > 1.0) return ATTN_ERR_INVALID_ARG;
       g_opts.poly_fraction = value;
       return ATTN_OK;
+    case ATTN_OPT_DEBUG_STALL:
+      if (value != 0.0 && value != 1.0) return ATTN_ERR_INVALID_ARG;
+      g_opts.debug_stall = value;
+      return ATTN_OK;
   }
   return ATTN_ERR_INVALID_ARG;
 }
@@ -231,6 +236,9 @@ attn_status attn_get_option(attn_option opt, double* value) {
       return ATTN_OK;
     case ATTN_OPT_EXP_POLY_FRACTION:
       *value = g_opts.poly_fraction;
+      return ATTN_OK;
+    case ATTN_OPT_DEBUG_STALL:
+      *value = g_opts.debug_stall;
       return ATTN_OK;
   }
   return ATTN_ERR_INVALID_ARG;
@@ -390,6 +398,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, flo
   a.wait_budget_ms = o.wait_budget_ms;
   a.num_ctas = (int)o.num_ctas;
   a.poly_fraction = (float)o.poly_fraction;
+  a.debug_stall = o.debug_stall != 0.0 ? 1 : 0;
   return launch_attn_fwd(a, s) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -467,6 +476,7 @@ attn_status attn_fwd_noalloc(const void* q, const void* k, const void* v, void* 
   a.wait_budget_ms = o.wait_budget_ms;
   a.num_ctas = (int)o.num_ctas;
   a.poly_fraction = (float)o.poly_fraction;
+  a.debug_stall = o.debug_stall != 0.0 ? 1 : 0;
   return launch_attn_fwd(a, s) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -70,6 +70,7 @@ enum Site : int {
   kSiteMmaOEmpty = 23,
   kSiteMmaDrain = 24,
   kSiteMmaTurn = 25,
+  kSiteMmaDebugStall = 26,
   kSiteSmxSFull = 30,
   kSiteSmxOFull = 31,
 };
@@ -85,8 +86,8 @@ struct Cfg {
   static constexpr int kSmemKV = kSmemQ + 2 * kTileBytes;
   static constexpr int kSmemBar = kSmemKV + kStages * kTileBytes;
   // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2]
-  //           o_full[2] o_empty[2] drain
-  static constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 2 + 2 + 2 + 1;
+  //           o_full[2] o_empty[2] drain never (the test hook's)
+  static constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 2 + 2 + 2 + 1 + 1;
   static constexpr int kSmemMisc = kSmemBar + 8 * kNumBars;
   static constexpr int kSmemDoc = (kSmemMisc + 16 + 15) / 16 * 16;  // int sdoc[2][128]
   static constexpr int kSmemBytes = kSmemDoc + 2 * kTileN * 4;
@@ -120,6 +121,7 @@ struct KParams {
   float tau;
   uint64_t budget_ns;
   int poly_chunks;  // 16-column chunks per row (of 8) whose exp2 uses the polynomial
+  int debug_stall;  // test hook (see ATTN_OPT_DEBUG_STALL)
 };
 
 struct Ctl {
@@ -256,7 +258,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   // ---- shared memory map ------------------------------------------------
   auto bar = [&](int i) { return sbase + (uint32_t)(C::kSmemBar + 8 * i); };
   const int B_QF = 0, B_QE = 2, B_KVF = 4, B_KVE = 4 + C::kStages, B_SF = 4 + 2 * C::kStages,
-            B_PF = B_SF + 2, B_OF = B_PF + 2, B_OE = B_OF + 2, B_DRAIN = B_OE + 2;
+            B_PF = B_SF + 2, B_OF = B_PF + 2, B_OE = B_OF + 2, B_DRAIN = B_OE + 2,
+            B_NEVER = B_DRAIN + 1;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kSmemMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kSmemMisc + 4);
   volatile int* s_turn = reinterpret_cast<volatile int*>(smem + C::kSmemMisc + 8);
@@ -278,6 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       ptx::mbar_init(bar(B_OE + t), 4);
     }
     ptx::mbar_init(bar(B_DRAIN), 2);
+    ptx::mbar_init(bar(B_NEVER), 1);
     *s_abort = 0;
     *s_turn = 0;
     ptx::fence_mbar_init();
@@ -454,6 +458,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const int n = p.cnt[it.e];
         if (n == 0) continue;
         const uint32_t k0 = kv_cnt;
+        if (p.debug_stall) {  // test hook: a wait nothing ever completes
+          ok = wait_all(bar(B_NEVER), 0, kSiteMmaDebugStall);
+          if (!ok) break;
+        }
         ok = wait_all(bar(B_QF + t), act & 1, kSiteMmaQFull) &&
              wait_all(kv_full(k0), kv_par(k0), kSiteMmaKvFull) && take_turn();
         if (!ok) break;
@@ -916,6 +924,7 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
   kp.status = a.status;
   kp.tau = a.rescale_threshold;
   kp.budget_ns = (uint64_t)(a.wait_budget_ms * 1.0e6);
+  kp.debug_stall = a.debug_stall;
   kp.poly_chunks = (int)lrintf(a.poly_fraction * 8.0f);
   if (kp.poly_chunks < 0) kp.poly_chunks = 0;
   if (kp.poly_chunks > 8) kp.poly_chunks = 8;

@@ -130,6 +130,7 @@ struct FwdArgs {
   double wait_budget_ms;
   int num_ctas;                // 0 = SM count
   float poly_fraction;
+  int debug_stall;             // test hook: MMA issuers wait on a barrier nothing arrives on
 };
 
 cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream);

@@ -269,7 +269,14 @@ typedef enum attn_option {
      * polynomial is below 1e-4, far under the bf16 rounding of P.
      * "FlashAttention-4 explained", "Forward pass fixes",
      * "Software-emulated exponentials". */
-    ATTN_OPT_EXP_POLY_FRACTION = 5
+    ATTN_OPT_EXP_POLY_FRACTION = 5,
+    /* Test hook, default 0.  1: the forward kernel's MMA issuers wait on a
+     * barrier that nothing ever arrives on, so their bounded wait runs out
+     * after ATTN_OPT_WAIT_BUDGET_MS: the kernel records ATTN_ERR_TIMEOUT,
+     * lets its in-flight copies land, frees Tensor Memory and returns, with
+     * unspecified outputs.  Lets tests exercise the timeout path without any
+     * real fault or hang. */
+    ATTN_OPT_DEBUG_STALL = 6
 } attn_option;
 
 attn_status attn_set_option(attn_option opt, double value);

@@ -112,3 +112,6 @@ def test_options_round_trip(attn):
         attn.set_option("exp_poly_fraction", 2.0)
     with pytest.raises(attn.AttnError):
         attn.set_option("force_partial", 0.5)
+    with pytest.raises(attn.AttnError):
+        attn.set_option("debug_stall", 2)
+    assert attn.get_option("debug_stall") == 0

@@ -336,6 +336,26 @@ def test_mismatched_block_mask_is_reported(attn):
     assert attn.get_device_status(device=DEV) == 0       # cleared
 
 
+def test_wait_timeout_is_reported_and_context_survives(attn):
+    # The test hook makes the MMA issuers wait on a barrier nothing arrives
+    # on: the bounded wait must run out, the kernel must record
+    # ATTN_ERR_TIMEOUT and return (no trap, no hang), and the next call on
+    # the same context must be correct.
+    B, H, S, D = 1, 2, 512, 128
+    q, k, v = rand_inputs(B, H, H, S, S, D, seed=16)
+    old_budget = attn.get_option("wait_budget_ms")
+    try:
+        attn.set_option("wait_budget_ms", 20)
+        attn.set_option("debug_stall", 1)
+        attn.attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=True)
+        assert attn.get_device_status(device=DEV) == 4  # ATTN_ERR_TIMEOUT
+    finally:
+        attn.set_option("debug_stall", 0)
+        attn.set_option("wait_budget_ms", old_budget)
+    assert attn.get_device_status(device=DEV) == 0
+    run_and_compare(attn, q, k, v, 1 / math.sqrt(D), causal=True)
+
+
 def test_gqa_equals_repeated_kv(attn):
     B, H, Hkv, S, D = 1, 8, 2, 333, 128
     q, k, v = rand_inputs(B, H, Hkv, S, S, D, seed=15)
