@@ -475,10 +475,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const uint32_t vi = k0 + 2 * j + 1;  // V_j
           const uint32_t ki = k0 + 2 * j + 2;  // K_{j+1}
           const bool has_next = j + 1 < n;
-          ok = wait_all(bar(B_PF + t), p_cnt & 1, kSiteMmaPFull) &&
-               wait_all(kv_full(vi), kv_par(vi), kSiteMmaKvFull);
-          if (ok && j == 0 && act > 0) ok = wait_all(bar(B_OE + t), (act - 1) & 1, kSiteMmaOEmpty);
+          // Each mbarrier check costs a few hundred cycles even when the phase
+          // has long completed, so the checks that are normally satisfied
+          // early (K/V landed, O free) come first and P -- normally the last
+          // to arrive -- comes last, right before the turn.
+          ok = wait_all(kv_full(vi), kv_par(vi), kSiteMmaKvFull);
           if (ok && has_next) ok = wait_all(kv_full(ki), kv_par(ki), kSiteMmaKvFull);
+          if (ok && j == 0 && act > 0) ok = wait_all(bar(B_OE + t), (act - 1) & 1, kSiteMmaOEmpty);
+          if (ok) ok = wait_all(bar(B_PF + t), p_cnt & 1, kSiteMmaPFull);
           if (ok) ok = take_turn();
           if (!ok) break;
           ++p_cnt;
