@@ -125,7 +125,8 @@ struct KParams {
 };
 
 struct Ctl {
-  volatile int* abort;
+  volatile int* abort;   // generic pointer, for stores
+  uint32_t abort_smem;   // the same flag's shared-memory address, for polling
   DeviceStatus* status;
   uint64_t budget_ns;
 };
@@ -140,16 +141,26 @@ __device__ __noinline__ void report(const Ctl& c, int code, int site, int detail
 }
 
 // Bounded wait on an mbarrier phase.  Returns false when the wait was given
-// up (timeout here, or another role already aborted).
+// up (timeout here, or another role already aborted).  A waiting warp shares
+// its SM sub-partition with a softmax warp that is working, so the wait
+// sleeps in hardware (try_wait with a suspend hint, resumed as soon as the
+// phase completes) and checks the abort flag and the time budget only every
+// 16 suspensions, instead of spinning through the issue slots.
+constexpr uint32_t kSuspendHintNs = 20000;
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c, int site) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = ptx::globaltimer_ns();
-  while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (*c.abort) return false;
-    if (ptx::globaltimer_ns() - t0 > c.budget_ns) {
-      report(c, ATTN_ERR_TIMEOUT, site, (int)parity);
-      return false;
+  uint64_t t0 = 0;
+  for (uint32_t spin = 1;; ++spin) {
+    if (ptx::mbar_try_wait_hint(bar, parity, kSuspendHintNs)) return true;
+    if ((spin & 15) == 0) {
+      if (ptx::ld_volatile_shared(c.abort_smem)) return false;
+      const uint64_t now = ptx::globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > c.budget_ns) {
+        report(c, ATTN_ERR_TIMEOUT, site, (int)parity);
+        return false;
+      }
     }
   }
 }
@@ -295,7 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   ptx::tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  Ctl ctl{s_abort, p.status, p.budget_ns};
+  Ctl ctl{s_abort, sbase + (uint32_t)(C::kSmemMisc + 4), p.status, p.budget_ns};
+  const uint32_t s_turn_smem = sbase + (uint32_t)(C::kSmemMisc + 8);
 
   if (warp >= 8) {
     // Producer warpgroup: give registers away first (whole warpgroup).
@@ -423,15 +435,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       auto take_turn = [&]() -> bool {
         const int want = 2 * grp + t;
         bool got = true;
-        if (*s_turn != want) {
+        if (ptx::ld_volatile_shared(s_turn_smem) != want) {
           const uint64_t t0 = ptx::globaltimer_ns();
           for (uint32_t spin = 1;; ++spin) {
-            if (*s_turn == want) break;
+            if (ptx::ld_volatile_shared(s_turn_smem) == want) break;
             // back off: a tight poll steals issue slots from the two softmax
             // warps that share this SM sub-partition
             __nanosleep(32);
             if ((spin & 255) == 0) {
-              if (*s_abort) { got = false; break; }
+              if (ptx::ld_volatile_shared(ctl.abort_smem)) { got = false; break; }
               if (ptx::globaltimer_ns() - t0 > p.budget_ns) {
                 if (lane == 0) report(ctl, ATTN_ERR_TIMEOUT, kSiteMmaTurn, want);
                 got = false;

@@ -57,6 +57,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
+// As mbar_try_wait, but the thread may stay suspended in hardware for up to
+// `hint_ns` nanoseconds waiting for the phase (it resumes as soon as the
+// phase completes), instead of spinning through the issue slots.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ int ld_volatile_shared(uint32_t addr) {
+  int v;
+  asm volatile("ld.volatile.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
 // ----------------------------------------------------------------- TMA ----
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
