@@ -346,9 +346,10 @@ _HDR_FMT = "<IIiiiiiiiiIiiiiiQQQQQQQii"  # mirrors the device block-mask header
 
 def decode_block_mask(bm: BlockMask) -> dict:
     """Host copy of a block mask for inspection: header fields, per-entry
-    counts, work order, key-tile lists and the class grid
-    ``cls[mask_batch][q_tile][k_tile]`` (0 EMPTY, 1 PARTIAL, 2 FULL).
-    Synchronises the device."""
+    counts, work order, key-tile lists, the class grid
+    ``cls[mask_batch][q_tile][k_tile]`` (0 EMPTY, 1 PARTIAL, 2 FULL) and, with
+    a document mask, ``doc_lo`` / ``doc_hi[mask_batch][token]`` (the run of
+    equal ids holding each token).  Synchronises the device."""
     import struct
 
     import numpy as np
@@ -374,4 +375,8 @@ def decode_block_mask(bm: BlockMask) -> dict:
                 if 2 * p + t < nQ:
                     cls[b, 2 * p + t, kt] = (int(x) >> (24 + 2 * t)) & 3
     h.update(order=order, cnt=cnt, list=lst, cls=cls)
+    if h["doc_off"]:  # document mask: first / last key of each token's run of equal ids
+        bm_, S = h["bm"], h["S_k"]
+        d = raw[h["doc_off"]:h["doc_off"] + 8 * bm_ * S].view(np.int32).reshape(2, bm_, S)
+        h.update(doc_lo=d[0].copy(), doc_hi=d[1].copy())
     return h

@@ -245,6 +245,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // Launched with programmatic stream serialization: this CTA may start while
+  // the kernel before it (normally the block-mask build) finishes, and reads
+  // no global memory until that kernel's writes are visible.
+  ptx::griddep_wait();
+
   // ---- block-mask consistency (uniform across the CTA) -------------------
   const BlockMaskHeader* hdr = p.hdr;
   const bool hdr_ok = hdr->magic == kBlockMaskMagic && hdr->version == kBlockMaskVersion &&
@@ -884,8 +889,17 @@ cudaError_t launch_variant(const KParams& kp, int grid, cudaStream_t stream) {
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg<D>::kSmemAlloc);
   if (err != cudaSuccess) return err;
-  kern<<<grid, kThreads, Cfg<D>::kSmemAlloc, stream>>>(kp);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<D>::kSmemAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, kp);
 }
 
 template <int D>

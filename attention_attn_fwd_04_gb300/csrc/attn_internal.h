@@ -59,9 +59,14 @@ struct BlockMaskGeom {
   int nQ, nK, nP, bm, n_entries;
   size_t order_off, cnt_off, list_off;
   size_t doc_off;   // DOCUMENT only: per-token document key interval
-  size_t flag_off;  // DOCUMENT only: int32 "ids out of order" flag
+  size_t tile_off;  // DOCUMENT only: smallest / largest id of every 128-token tile
+  size_t flag_off;  // DOCUMENT only: int32 "ids out of order" flag per prep block
+  int n_flags;
   size_t total;
 };
+
+// Tokens per block of the document preparation pass (a multiple of kTileN).
+constexpr int kDocPrepTokens = 1024;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -76,13 +81,17 @@ inline BlockMaskGeom block_mask_geom(int B, int S_q, int S_k, uint32_t mask_flag
   g.cnt_off = align_up(g.order_off + sizeof(int32_t) * (size_t)g.n_entries, 16);
   g.list_off = align_up(g.cnt_off + sizeof(int32_t) * (size_t)g.n_entries, 16);
   g.total = align_up(g.list_off + sizeof(uint32_t) * (size_t)g.n_entries * (size_t)g.nK, 16);
-  g.doc_off = g.flag_off = 0;
+  g.doc_off = g.tile_off = g.flag_off = 0;
+  g.n_flags = 0;
   if (mask_flags & ATTN_MASK_DOCUMENT) {
-    // [bm][S_k] first and last key of each token's document (valid when the
-    // ids are non-decreasing), then the out-of-order flag
+    // int32 [bm][S_k] first and last key of each token's document (valid
+    // when the ids are non-decreasing), then int32 [bm][nK] id range of each
+    // key tile (lo, then hi), then one out-of-order flag per prep block
     g.doc_off = g.total;
-    g.flag_off = align_up(g.doc_off + 2 * sizeof(int32_t) * (size_t)g.bm * (size_t)S_k, 16);
-    g.total = g.flag_off + 16;
+    g.tile_off = align_up(g.doc_off + 2 * sizeof(int32_t) * (size_t)g.bm * (size_t)S_k, 16);
+    g.flag_off = align_up(g.tile_off + 2 * sizeof(int32_t) * (size_t)g.bm * (size_t)g.nK, 16);
+    g.n_flags = g.bm * ((S_k + kDocPrepTokens - 1) / kDocPrepTokens);
+    g.total = align_up(g.flag_off + sizeof(int32_t) * (size_t)g.n_flags, 16);
   }
   return g;
 }

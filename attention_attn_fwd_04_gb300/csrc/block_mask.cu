@@ -17,49 +17,74 @@
 #include <stdint.h>
 
 #include "attn_internal.h"
+#include "sm103_ptx.cuh"
 
 namespace attn {
 
 namespace {
 
-constexpr int kBuildThreads = 256;
+constexpr int kBuildThreads = 256;     // order kernel
+constexpr int kClassifyThreads = 256;   // classify kernel: one key tile per thread
 
 struct Range {
   int lo, hi;
 };
 
-// Visible key interval [lo, hi] of query row i from the interval masks.
-__device__ __forceinline__ Range row_interval(int i, int b, const MaskParams& mp) {
-  int qpos = i + mp.q_offset;
-  int lo = 0, hi = mp.S_k - 1;
+// Visible key interval [lo, hi] of query row i from the interval masks
+// (pl: the batch's prefix length).  64-bit, so no window or offset overflows.
+__device__ __forceinline__ void row_interval(long long i, long long pl, const MaskParams& mp,
+                                             long long& lo, long long& hi) {
+  const long long qpos = i + mp.q_offset;
+  lo = 0;
+  hi = mp.S_k - 1;
   if (mp.flags & ATTN_MASK_CAUSAL) hi = min(hi, qpos);
   if (mp.flags & ATTN_MASK_WINDOW) {
     lo = max(lo, qpos - mp.window + 1);
     hi = min(hi, qpos);
   }
-  if (mp.flags & ATTN_MASK_PREFIX_LM) hi = min(hi, max(qpos, mp.prefix_len[b] - 1));
-  return Range{lo, hi};
+  if (mp.flags & ATTN_MASK_PREFIX_LM) hi = min(hi, max(qpos, pl - 1));
 }
 
-// Class of (query rows [r0, r1], key tile starting at c0) for batch b.
-// dq/dk: document-id ranges of the rows and of the keys (DOCUMENT only).
-__device__ uint32_t classify(int r0, int r1, int c0, int b, const MaskParams& mp, Range dq,
-                             Range dk) {
+__device__ __forceinline__ bool row_meets(long long i, long long pl, int c0, int c1,
+                                          const MaskParams& mp) {
+  long long lo, hi;
+  row_interval(i, pl, mp, lo, hi);
+  return max(lo, (long long)c0) <= min(hi, (long long)c1);
+}
+
+// Class of (query rows [r0, r1], key tile starting at c0), in O(1).
+//
+// Every interval mask gives row i a visible key interval [lo(i), hi(i)]
+// whose ends never decrease as i grows.  Hence
+//  * FULL: all rows see the whole tile  <=>  lo(r1) <= c0 and
+//    hi(r0) >= c0 + 127 (and the tile is not cut by S_k);
+//  * non-EMPTY: some row meets [c0, c1].  The overlap length
+//    min(hi, c1) - max(lo, c0) is piecewise linear in the row with integer
+//    breakpoints, so its maximum over [r0, r1] is taken at r0, r1 or a
+//    breakpoint: the positions where lo leaves 0 (qpos = W - 1) or passes c0
+//    (qpos = c0 + W - 1), where hi reaches S_k - 1, the prefix end
+//    (qpos = P - 1) or c1.  Testing those rows is exact.
+// Documents (dq/dk: id ranges of the rows and of the keys) are then applied
+// conservatively: EMPTY when the ranges do not meet, FULL only when both are
+// one and the same document.
+__device__ uint32_t classify_tile(int r0, int r1, int c0, long long pl, const MaskParams& mp,
+                                  Range dq, Range dk) {
   if (r0 > r1) return kEmpty;  // no valid query row
   const int c1 = min(c0 + kTileN - 1, mp.S_k - 1);
   const bool ragged = (c1 - c0 + 1) < kTileN;
-  bool any = false, all = !ragged;
-  for (int i = r0; i <= r1; ++i) {
-    Range r = row_interval(i, b, mp);
-    int a = max(r.lo, c0), e = min(r.hi, c1);
-    if (e >= a) {
-      any = true;
-      if (a != c0 || e != c0 + kTileN - 1) all = false;
-    } else {
-      all = false;
-    }
+  const long long w = (mp.flags & ATTN_MASK_WINDOW) ? mp.window : 1;
+  const long long cand[5] = {w - 1, c0 + w - 1, (long long)mp.S_k - 1, pl - 1, c1};
+  bool any = row_meets(r0, pl, c0, c1, mp) || row_meets(r1, pl, c0, c1, mp);
+#pragma unroll
+  for (int k = 0; k < 5; ++k) {
+    const long long i = min(max(cand[k] - mp.q_offset, (long long)r0), (long long)r1);
+    any = any || row_meets(i, pl, c0, c1, mp);
   }
   if (!any) return kEmpty;
+  long long lo1, hi1, lo0, hi0;
+  row_interval(r1, pl, mp, lo1, hi1);
+  row_interval(r0, pl, mp, lo0, hi0);
+  bool all = !ragged && lo1 <= c0 && hi0 >= (long long)c0 + kTileN - 1;
   if (mp.flags & ATTN_MASK_DOCUMENT) {
     if (dk.hi < dq.lo || dq.hi < dk.lo) return kEmpty;
     if (!(dq.lo == dq.hi && dk.lo == dk.hi && dq.lo == dk.lo)) all = false;
@@ -67,21 +92,14 @@ __device__ uint32_t classify(int r0, int r1, int c0, int b, const MaskParams& mp
   return all ? kFull : kPartial;
 }
 
-__device__ Range doc_range(const int32_t* ids, int a, int e) {
-  Range r{INT32_MAX, INT32_MIN};
-  for (int j = a; j <= e; ++j) {
-    int d = ids[j];
-    r.lo = min(r.lo, d);
-    r.hi = max(r.hi, d);
-  }
-  return r;
-}
-
 // One block per (batch entry, query-tile pair).  Writes cnt[e] and the
-// compacted list of non-empty key tiles in descending key-tile order.
-__global__ void __launch_bounds__(kBuildThreads) classify_kernel(BlockMaskHeader* hdr_out,
-                                                                  MaskParams mp, BlockMaskGeom g,
-                                                                  int force_partial) {
+// compacted list of non-empty key tiles in descending key-tile order, one
+// key tile per thread, kClassifyThreads tiles at a time.
+__global__ void __launch_bounds__(kClassifyThreads) classify_kernel(BlockMaskHeader* hdr_out,
+                                                                     MaskParams mp,
+                                                                     BlockMaskGeom g,
+                                                                     int force_partial) {
+  constexpr int kWarps = kClassifyThreads / 32;
   const int nQ = g.nQ, nK = g.nK, nP = g.nP;
   const int e = blockIdx.x;
   const int bb = e / nP;  // batch of this entry (0 when the mask is batch-independent)
@@ -89,90 +107,162 @@ __global__ void __launch_bounds__(kBuildThreads) classify_kernel(BlockMaskHeader
   char* base = reinterpret_cast<char*>(hdr_out);
   int32_t* cnt = reinterpret_cast<int32_t*>(base + g.cnt_off);
   uint32_t* list = reinterpret_cast<uint32_t*>(base + g.list_off) + (size_t)e * nK;
-  if (e == 0 && threadIdx.x == 0 && g.flag_off != 0)
-    *reinterpret_cast<int32_t*>(base + g.flag_off) = 0;  // set by doc_ranges_kernel
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
 
-  __shared__ Range s_dq[2];
-  __shared__ int s_total;
-  __shared__ int s_warp_cnt[kBuildThreads / 32];
-  const int* ids = (mp.flags & ATTN_MASK_DOCUMENT) ? mp.doc_ids + (size_t)bb * mp.S_k : nullptr;
-
-  if (threadIdx.x < 2) {
-    int qt = 2 * p + threadIdx.x;
-    int r0 = qt * kTileM, r1 = min(r0 + kTileM - 1, mp.S_q - 1);
-    s_dq[threadIdx.x] = (ids && r0 <= r1) ? doc_range(ids, r0, r1) : Range{0, 0};
-  }
-  if (threadIdx.x == 0) s_total = 0;
-  __syncthreads();
-
+  __shared__ int s_warp_cnt[kWarps];
+  // DOCUMENT: id range of every key tile of this batch (S_q == S_k, so the
+  // query tiles have the same ranges)
+  const bool docs = (mp.flags & ATTN_MASK_DOCUMENT) != 0;
+  const int32_t* t_lo = docs ? reinterpret_cast<const int32_t*>(base + g.tile_off) + (size_t)bb * nK
+                             : nullptr;
+  const int32_t* t_hi = docs ? t_lo + (size_t)g.bm * nK : nullptr;
+  const long long pl = (mp.flags & ATTN_MASK_PREFIX_LM) ? mp.prefix_len[bb] : 0;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  // Process key tiles from the highest index down, one per thread per chunk.
-  for (int chunk = 0; chunk < nK; chunk += kBuildThreads) {
-    int idx = chunk + threadIdx.x;  // position in descending order
+
+  int r0[2], r1[2];
+  Range dq[2];
+  for (int t = 0; t < 2; ++t) {
+    const int qt = 2 * p + t;
+    r0[t] = qt * kTileM;
+    r1[t] = (qt < nQ) ? min(r0[t] + kTileM - 1, mp.S_q - 1) : r0[t] - 1;
+    dq[t] = (docs && r0[t] <= r1[t]) ? Range{t_lo[qt], t_hi[qt]} : Range{0, 0};
+  }
+
+  int total = 0;
+  for (int chunk = 0; chunk < nK; chunk += kClassifyThreads) {
+    const int idx = chunk + threadIdx.x;  // position in descending key-tile order
     uint32_t entry = 0;
     bool keep = false;
     if (idx < nK) {
-      int kt = nK - 1 - idx;
-      int c0 = kt * kTileN;
-      Range dk{0, 0};
-      if (ids) dk = doc_range(ids, c0, min(c0 + kTileN - 1, mp.S_k - 1));
-      uint32_t cls[2];
-      for (int t = 0; t < 2; ++t) {
-        int qt = 2 * p + t;
-        int r0 = qt * kTileM, r1 = min(r0 + kTileM - 1, mp.S_q - 1);
-        cls[t] = (qt < nQ) ? classify(r0, r1, c0, bb, mp, s_dq[t], dk) : kEmpty;
-        if (force_partial && cls[t] == kFull) cls[t] = kPartial;
+      const int kt = nK - 1 - idx;
+      const int c0 = kt * kTileN;
+      const Range dk = docs ? Range{t_lo[kt], t_hi[kt]} : Range{0, 0};
+      uint32_t c_0 = classify_tile(r0[0], r1[0], c0, pl, mp, dq[0], dk);
+      uint32_t c_1 = classify_tile(r0[1], r1[1], c0, pl, mp, dq[1], dk);
+      if (force_partial) {
+        if (c_0 == kFull) c_0 = kPartial;
+        if (c_1 == kFull) c_1 = kPartial;
       }
-      keep = (cls[0] != kEmpty) || (cls[1] != kEmpty);
-      entry = list_entry((uint32_t)kt, cls[0], cls[1]);
+      keep = (c_0 != kEmpty) || (c_1 != kEmpty);
+      entry = list_entry((uint32_t)kt, c_0, c_1);
     }
     // stable compaction within the chunk: warp ballots + block prefix
-    unsigned ball = __ballot_sync(0xffffffffu, keep);
+    const unsigned ball = __ballot_sync(0xffffffffu, keep);
     if (lane == 0) s_warp_cnt[warp] = __popc(ball);
     __syncthreads();
     int before = 0, chunk_total = 0;
-    for (int w = 0; w < kBuildThreads / 32; ++w) {
+    for (int w = 0; w < kWarps; ++w) {
       if (w < warp) before += s_warp_cnt[w];
       chunk_total += s_warp_cnt[w];
     }
     before += __popc(ball & ((1u << lane) - 1u));
-    if (keep) list[s_total + before] = entry;
-    __syncthreads();
-    if (threadIdx.x == 0) s_total += chunk_total;
-    __syncthreads();
+    if (keep) list[total + before] = entry;
+    total += chunk_total;
+    __syncthreads();  // s_warp_cnt is reused by the next chunk
   }
-  if (threadIdx.x == 0) cnt[e] = s_total;
+  if (threadIdx.x == 0) cnt[e] = total;
 }
 
-// For every token of every mask batch: the first and last key of its
-// document, by binary search over the ids (meaningful when the ids are
-// non-decreasing, i.e. packed documents), and a flag raised when some
-// batch's ids are out of order.  With packed ids, "key j is in query i's
-// document" is exactly j in [doc_lo[i], doc_hi[i]].
-__global__ void __launch_bounds__(kBuildThreads) doc_ranges_kernel(const int32_t* ids, int S,
-                                                                    int bm, char* base,
-                                                                    BlockMaskGeom g) {
-  const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (long long)bm * S) return;
-  const int b = (int)(idx / S), i = (int)(idx % S);
+// First position pos in [lo, hi) with row[pos] > v (strict) or row[pos] >= v,
+// for ids that are non-decreasing on [lo, hi); hi when there is none.  The
+// warp probes 32 evenly spaced positions per step, so a step shrinks the
+// range 32-fold.  Every lane returns the result.  Positions stay in [lo, hi)
+// whatever the ids.
+__device__ int warp_search(const int32_t* row, int lo, int hi, int32_t v, bool strict, int lane) {
+  while (hi > lo) {
+    const long long len = hi - lo;
+    const int p = (len <= 32) ? lo + min(lane, (int)len - 1)
+                              : lo + (int)(((long long)(lane + 1) * len) / 32) - 1;
+    const int32_t x = row[p];
+    const bool pred = (len <= 32 && lane >= len) ? false : (strict ? x > v : x >= v);
+    const unsigned m = __ballot_sync(0xffffffffu, pred);
+    if (m == 0) return hi;
+    const int f = __ffs(m) - 1;
+    const int pf = __shfl_sync(0xffffffffu, p, f);
+    if (len <= 32) return pf;
+    const int prev = __shfl_sync(0xffffffffu, p, f == 0 ? 0 : f - 1);
+    hi = pf + 1;
+    lo = (f == 0) ? lo : prev + 1;
+    if (hi - lo == 1) return lo;  // pred holds at pf and not at pf - 1
+  }
+  return hi;
+}
+
+__global__ void __launch_bounds__(kDocPrepTokens) doc_prep_kernel(const int32_t* ids, int S,
+                                                                   char* base, BlockMaskGeom g) {
+  constexpr int kWarps = kDocPrepTokens / 32;
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+  const int b = blockIdx.y;
+  const int i0 = blockIdx.x * kDocPrepTokens;
+  const int i = i0 + threadIdx.x;
+  const int last = min(i0 + kDocPrepTokens, S) - 1;  // last token of this block
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int32_t* row = ids + (size_t)b * S;
-  const int32_t x = row[i];
-  if (i + 1 < S && row[i + 1] < x) atomicOr(reinterpret_cast<int32_t*>(base + g.flag_off), 1);
-  int lo = 0, hi = S;  // first position with row[pos] >= x
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (row[mid] < x) lo = mid + 1; else hi = mid;
+  const bool in = i < S;
+  const int32_t x = in ? row[i] : 0;
+  const bool starts = in && (i == 0 || row[i - 1] != x);
+  const bool ends = in && (i == S - 1 || row[i + 1] != x);
+  const bool disorder = in && i + 1 < S && row[i + 1] < x;
+
+  __shared__ int s_start[kWarps], s_end[kWarps], s_tmin[kWarps], s_tmax[kWarps];
+  __shared__ int s_edge_lo, s_edge_hi;
+  // start of the run holding token i0 / end of the run holding token `last`
+  // (warp 0 / warp 1, 32-way searches)
+  if (warp == 0) {
+    const int32_t v = row[i0];
+    const int pos = warp_search(row, 0, i0, v, false, lane);  // first row[pos] >= v
+    if (lane == 0) s_edge_lo = pos;
+  } else if (warp == 1) {
+    const int32_t v = row[last];
+    const int pos = warp_search(row, last + 1, S, v, true, lane);  // first row[pos] > v
+    if (lane == 0) s_edge_hi = pos - 1;
   }
-  const int first = lo;
-  lo = i;
-  hi = S;  // first position with row[pos] > x, searching from i
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (row[mid] <= x) lo = mid + 1; else hi = mid;
+  // inclusive max-scan of run starts, inclusive suffix min-scan of run ends
+  int st = starts ? i : -1, en = ends ? i : INT32_MAX;
+  int32_t tmin = in ? x : INT32_MAX, tmax = in ? x : INT32_MIN;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, st, o);
+    const int d = __shfl_down_sync(0xffffffffu, en, o);
+    if (lane >= o) st = max(st, u);
+    if (lane + o < 32) en = min(en, d);
+    tmin = min(tmin, __shfl_xor_sync(0xffffffffu, tmin, o));
+    tmax = max(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
   }
-  int32_t* dlo = reinterpret_cast<int32_t*>(base + g.doc_off);
-  dlo[idx] = first;
-  dlo[(size_t)bm * S + idx] = lo - 1;
+  if (lane == 31) s_start[warp] = st;
+  if (lane == 0) {
+    s_end[warp] = en;
+    s_tmin[warp] = tmin;
+    s_tmax[warp] = tmax;
+  }
+  const int any_disorder = __syncthreads_or(disorder);
+  for (int w = 0; w < warp; ++w) st = max(st, s_start[w]);
+  for (int w = warp + 1; w < kWarps; ++w) en = min(en, s_end[w]);
+  if (in) {
+    int32_t* dlo = reinterpret_cast<int32_t*>(base + g.doc_off) + (size_t)b * S;
+    int32_t* dhi = reinterpret_cast<int32_t*>(base + g.doc_off) + ((size_t)g.bm + b) * S;
+    dlo[i] = st >= 0 ? st : s_edge_lo;
+    dhi[i] = en != INT32_MAX ? en : s_edge_hi;
+  }
+  constexpr int kTilesPerBlock = kDocPrepTokens / kTileN;
+  constexpr int kWarpsPerTile = kTileN / 32;
+  if (threadIdx.x < kTilesPerBlock) {
+    const int t = threadIdx.x;
+    if (i0 + t * kTileN < S) {
+      int32_t lo = INT32_MAX, hi = INT32_MIN;
+      for (int w = t * kWarpsPerTile; w < (t + 1) * kWarpsPerTile; ++w) {
+        lo = min(lo, s_tmin[w]);
+        hi = max(hi, s_tmax[w]);
+      }
+      const int kt = i0 / kTileN + t;
+      int32_t* tl = reinterpret_cast<int32_t*>(base + g.tile_off);
+      tl[(size_t)b * g.nK + kt] = lo;
+      tl[((size_t)g.bm + b) * g.nK + kt] = hi;
+    }
+  }
+  if (threadIdx.x == 0)
+    reinterpret_cast<int32_t*>(base + g.flag_off)[b * gridDim.x + blockIdx.x] = any_disorder;
 }
 
 // order[]: entries sorted by descending count (ties by entry index), so the
@@ -187,6 +277,14 @@ __global__ void __launch_bounds__(kBuildThreads) order_kernel(BlockMaskHeader* h
   const int32_t* cnt = reinterpret_cast<const int32_t*>(base + g.cnt_off);
 
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+  int disorder = 0;  // block 0: any document prep block saw ids out of order
+  if (blockIdx.x == 0) {
+    const int32_t* flags = reinterpret_cast<const int32_t*>(base + g.flag_off);
+    for (int j = threadIdx.x; j < g.n_flags; j += kBuildThreads) disorder |= flags[j];
+    disorder = __syncthreads_or(disorder);
+  }
   __shared__ int s_cnt[kBuildThreads];
   int mine = (e < n) ? cnt[e] : 0;
   int rank = 0;
@@ -230,11 +328,29 @@ __global__ void __launch_bounds__(kBuildThreads) order_kernel(BlockMaskHeader* h
     h.list_off = g.list_off;
     h.total_bytes = g.total;
     h.doc_off = g.doc_off;
-    h.docs_sorted =
-        (g.flag_off != 0) ? (*reinterpret_cast<const int32_t*>(base + g.flag_off) == 0) : 0;
+    h.docs_sorted = (g.flag_off != 0 && !disorder) ? 1 : 0;
     h.pad_ = 0;
     *hdr = h;
   }
+}
+
+// Every kernel of the build waits for its predecessor in the stream before
+// touching memory and is launched with programmatic stream serialization, so
+// its launch overlaps the tail of the kernel before it.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, int threads, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
 }
 
 }  // namespace
@@ -243,19 +359,20 @@ cudaError_t launch_build_block_mask(int B, int S_q, int S_k, const MaskParams& m
                                     int force_partial, void* dst, cudaStream_t stream) {
   BlockMaskGeom g = block_mask_geom(B, S_q, S_k, mp.flags);
   BlockMaskHeader* hdr = reinterpret_cast<BlockMaskHeader*>(dst);
-  classify_kernel<<<g.n_entries, kBuildThreads, 0, stream>>>(hdr, mp, g, force_partial);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
+  char* base = reinterpret_cast<char*>(dst);
+  cudaError_t err;
   if (g.flag_off != 0) {
-    const long long toks = (long long)g.bm * S_k;
-    doc_ranges_kernel<<<(unsigned)((toks + kBuildThreads - 1) / kBuildThreads), kBuildThreads, 0,
-                        stream>>>(mp.doc_ids, S_k, g.bm, reinterpret_cast<char*>(dst), g);
-    err = cudaGetLastError();
+    const dim3 grid((unsigned)((S_k + kDocPrepTokens - 1) / kDocPrepTokens), (unsigned)g.bm, 1);
+    err = launch_pdl(doc_prep_kernel, grid, kDocPrepTokens, stream,
+                     static_cast<const int32_t*>(mp.doc_ids), S_k, base, g);
     if (err != cudaSuccess) return err;
   }
-  int blocks = (g.n_entries + kBuildThreads - 1) / kBuildThreads;
-  order_kernel<<<blocks, kBuildThreads, 0, stream>>>(hdr, B, mp, g, force_partial);
-  return cudaGetLastError();
+  err = launch_pdl(classify_kernel, dim3((unsigned)g.n_entries), kClassifyThreads, stream, hdr, mp,
+                   g, force_partial);
+  if (err != cudaSuccess) return err;
+  const int blocks = (g.n_entries + kBuildThreads - 1) / kBuildThreads;
+  return launch_pdl(order_kernel, dim3((unsigned)blocks), kBuildThreads, stream, hdr, B, mp, g,
+                    force_partial);
 }
 
 }  // namespace attn

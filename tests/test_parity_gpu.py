@@ -147,6 +147,21 @@ def test_unsorted_document_ids(attn):
     run_and_compare(attn, q, k, v, 0.125, doc_ids=doc_ids, causal=True)
 
 
+def test_document_order_flag_across_blocks(attn):
+    # packed ids with one step back in the third 1024-token block: the ids
+    # are out of order, so the element-wise path must be taken
+    B, H, S, D = 1, 2, 3100, 64
+    ids = workloads.doc_ids_for(S, seed=12, lo=200, hi=900).clone()
+    ids[2500:] -= 1
+    ids[2500:] = torch.clamp(ids[2500:], min=0)
+    assert bool((ids[1:] < ids[:-1]).any())
+    doc_ids = ids[None].contiguous()
+    bm = attn.build_block_mask(B, H, S, S, device=DEV, doc_ids=doc_ids.to(DEV))
+    assert attn.decode_block_mask(bm)["docs_sorted"] == 0
+    q, k, v = rand_inputs(B, H, H, S, S, D, seed=9)
+    run_and_compare(attn, q, k, v, 0.125, doc_ids=doc_ids, causal=True)
+
+
 def test_explicit_alibi_slopes(attn):
     B, H, S, D = 1, 4, 300, 128
     q, k, v = rand_inputs(B, H, H, S, S, D, seed=9)
@@ -187,15 +202,32 @@ MASK_CASES = [
     (2, 900, 900, {"doc_ids": "packed"}),
     (2, 800, 800, {"prefix_len": [0, 333]}),
     (1, 520, 520, {"causal": True, "q_offset": -200}),
+    # documents longer than the 1024-token preparation blocks, ragged length
+    (2, 5000, 5000, {"doc_ids": "long", "causal": True}),
 ]
+
+
+def run_bounds(ids):
+    """First and last position of the run of equal values holding each token."""
+    ids = np.asarray(ids)
+    S = ids.shape[0]
+    lo = np.zeros(S, np.int64)
+    hi = np.zeros(S, np.int64)
+    for i in range(1, S):
+        lo[i] = lo[i - 1] if ids[i] == ids[i - 1] else i
+    hi[S - 1] = S - 1
+    for i in range(S - 2, -1, -1):
+        hi[i] = hi[i + 1] if ids[i] == ids[i + 1] else i
+    return lo, hi
 
 
 @pytest.mark.parametrize("case", range(len(MASK_CASES)))
 def test_block_mask_exact(attn, case):
     B, S_q, S_k, mods = MASK_CASES[case]
     mods = dict(mods)
-    if mods.get("doc_ids") == "packed":
-        ids = torch.stack([workloads.doc_ids_for(S_k, seed=10 + b, lo=64, hi=300)
+    if mods.get("doc_ids") in ("packed", "long"):
+        lo, hi = (64, 300) if mods["doc_ids"] == "packed" else (700, 3000)
+        ids = torch.stack([workloads.doc_ids_for(S_k, seed=10 + b, lo=lo, hi=hi)
                            for b in range(B)]).contiguous()
         mods["doc_ids"] = ids
     if "prefix_len" in mods:
@@ -205,6 +237,11 @@ def test_block_mask_exact(attn, case):
     got = attn.decode_block_mask(bm)
     # packed ids take the interval form of the document mask
     assert got["docs_sorted"] == (1 if "doc_ids" in mods else 0)
+    if "doc_ids" in mods:
+        for b in range(B):
+            lo, hi = run_bounds(mods["doc_ids"][b].numpy())
+            np.testing.assert_array_equal(got["doc_lo"][b], lo)
+            np.testing.assert_array_equal(got["doc_hi"][b], hi)
     cls = got["cls"]
     if cls.shape[0] == 1:  # batch-independent mask: stored once
         assert all(np.array_equal(want[0], w_) for w_ in want)
@@ -224,6 +261,36 @@ def test_block_mask_exact(attn, case):
     assert sorted(order.tolist()) == list(range(got["n_entries"]))
     c = got["cnt"][order]
     assert np.all(np.diff(c) <= 0)
+
+
+def random_mask_case(seed):
+    """A random combination of the interval masks over a small ragged problem."""
+    rng = np.random.default_rng(seed)
+    B = int(rng.integers(1, 3))
+    S_q, S_k = (int(x) for x in rng.integers(1, 800, size=2))
+    mods = {}
+    if rng.random() < 0.5:
+        mods["causal"] = True
+    if rng.random() < 0.4:
+        mods["window"] = 1 if rng.random() < 0.2 else int(rng.integers(1, 500))
+    if rng.random() < 0.4:
+        mods["q_offset"] = int(rng.integers(-900, 900))
+    if rng.random() < 0.3:
+        mods["prefix_len"] = [int(x) for x in rng.integers(0, 900, size=B)]
+    return B, S_q, S_k, mods
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_block_mask_exact_random(attn, seed):
+    B, S_q, S_k, mods = random_mask_case(seed)
+    if "prefix_len" in mods:
+        mods["prefix_len"] = torch.tensor(mods["prefix_len"], dtype=torch.int32)
+    want = expected_classes(B, S_q, S_k, mods)
+    bm = attn.build_block_mask(B, 1, S_q, S_k, device=DEV, **to_dev(mods))
+    cls = attn.decode_block_mask(bm)["cls"]
+    if cls.shape[0] == 1:
+        want = want[:1]
+    np.testing.assert_array_equal(cls, want)
 
 
 # ------------------------------------------------- invariants of the path ---
