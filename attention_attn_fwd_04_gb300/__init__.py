@@ -28,6 +28,7 @@ __all__ = [
     "BlockMask",
     "attn_fwd",
     "attn_fwd_into",
+    "attn_fwd_host",
     "build_block_mask",
     "block_mask_bytes",
     "block_mask_stats",
@@ -108,6 +109,9 @@ def _load() -> ctypes.CDLL:
     lib.attn_fwd.restype = I
     lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F,
                              ctypes.POINTER(ModDesc), P]
+    lib.attn_fwd_host.restype = I
+    lib.attn_fwd_host.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F,
+                                  ctypes.POINTER(ModDesc), P]
     lib.attn_block_mask_bytes.restype = ctypes.c_size_t
     lib.attn_block_mask_bytes.argtypes = [I, I, I, I, ctypes.POINTER(ModDesc)]
     lib.attn_build_block_mask.restype = I
@@ -321,6 +325,56 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, return_lse: b
     out = torch.empty((B, H, S_q, D), dtype=torch.bfloat16, device=q.device)
     lse = torch.empty((B, H, S_q), dtype=torch.float32, device=q.device) if return_lse else None
     attn_fwd_into(q, k, v, out, lse, stream=stream, **kw)
+    return (out, lse) if return_lse else out
+
+
+def attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *,
+                  out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                  return_lse: bool = True, scale: Optional[float] = None, device=None,
+                  stream: Optional[torch.cuda.Stream] = None, **mods):
+    """Attention forward on tensors in host memory (the library copies them
+    in and the results out).  ``q``, ``k``, ``v`` and the mask arrays
+    (``doc_ids``, ``prefix_len``, ``alibi_slopes``) are CPU tensors --
+    page-locked (``pin_memory()``) for full copy speed.  Returns CPU
+    ``(O, LSE)`` (or ``O``), written into ``out`` / ``lse`` when given.
+
+    Asynchronous: the call is ordered on ``stream`` (default: the current
+    stream of ``device``, default ``cuda``); synchronise it before reading
+    the results or changing the inputs.  Consecutive calls overlap their
+    copies with each other's compute."""
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, S, D]")
+    B, H, S_q, D = q.shape
+    Bk, H_kv, S_k, Dk = k.shape
+    if (Bk, Dk) != (B, D) or v.shape != k.shape:
+        raise ValueError("shape mismatch between q, k and v")
+    cpu = torch.device("cpu")
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty((B, H, S_q, D), dtype=torch.bfloat16, pin_memory=pin)
+    if lse is None and return_lse:
+        lse = torch.empty((B, H, S_q), dtype=torch.float32, pin_memory=pin)
+    for name, t in (("q", q), ("k", k), ("v", v), ("out", out)):
+        if t.device != cpu or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous bfloat16 CPU tensor" % name)
+    if tuple(out.shape) != (B, H, S_q, D):
+        raise ValueError("out must be [B, H, S_q, D]")
+    if lse is not None and (lse.device != cpu or lse.dtype != torch.float32
+                            or not lse.is_contiguous() or tuple(lse.shape) != (B, H, S_q)):
+        raise ValueError("lse must be a contiguous float32 [B, H, S_q] CPU tensor")
+    _check_mask_arrays(cpu, mods.get("doc_ids"), mods.get("prefix_len"), mods.get("alibi_slopes"))
+    if "block_mask" in mods:
+        raise ValueError("attn_fwd_host builds its own block mask")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    m, keep = _mod_desc(**mods)
+    dev = torch.device(device if device is not None else "cuda")
+    with torch.cuda.device(dev):
+        st = _lib.attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                _ptr(lse), B, H, H_kv, S_q, S_k, D, float(scale),
+                                ctypes.byref(m), _stream_ptr(stream, dev))
+    del keep
+    _check(st, "attn_fwd_host")
     return (out, lse) if return_lse else out
 
 

@@ -125,6 +125,89 @@ MaskParams mask_params(int S_q, int S_k, const attn_mod_desc* mod) {
   return mp;
 }
 
+// Checks on the tensors of one forward that do not depend on where they
+// live: present, head grouping, scale, head dim, sizes that index in 32
+// bits, outputs not overlapping inputs.
+attn_status check_tensors(const void* q, const void* k, const void* v, const void* out,
+                          const float* lse, int B, int H, int H_kv, int S_q, int S_k, int D,
+                          float scale) {
+  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return ATTN_ERR_INVALID_ARG;
+  if (H_kv <= 0 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!(isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
+  if ((size_t)B * H > (size_t)INT32_MAX || (size_t)B * H_kv * (size_t)S_k > (size_t)INT32_MAX * 128)
+    return ATTN_ERR_INVALID_ARG;
+  const size_t qb = (size_t)B * H * S_q * D * 2, kb = (size_t)B * H_kv * S_k * D * 2;
+  if (overlaps(out, qb, q, qb) || overlaps(out, qb, k, kb) || overlaps(out, qb, v, kb))
+    return ATTN_ERR_INVALID_ARG;
+  if (lse != nullptr) {
+    const size_t lb = (size_t)B * H * S_q * 4;
+    if (overlaps(lse, lb, q, qb) || overlaps(lse, lb, k, kb) || overlaps(lse, lb, v, kb) ||
+        overlaps(lse, lb, out, qb))
+      return ATTN_ERR_INVALID_ARG;
+  }
+  return ATTN_OK;
+}
+
+// Device tensors additionally need 16-byte (Q, K, V, O) and 4-byte (LSE)
+// alignment for the tensor maps and the vector stores.
+attn_status check_device_tensors(const void* q, const void* k, const void* v, const void* out,
+                                 const float* lse, int B, int H, int H_kv, int S_q, int S_k,
+                                 int D, float scale) {
+  attn_status st = check_tensors(q, k, v, out, lse, B, H, H_kv, S_q, S_k, D, scale);
+  if (st != ATTN_OK) return st;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+    return ATTN_ERR_INVALID_ARG;
+  if (lse != nullptr && !aligned(lse, 4)) return ATTN_ERR_INVALID_ARG;
+  return ATTN_OK;
+}
+
+// Enqueues one checked forward on s: the block-mask build into mask_buf
+// (skipped when bmask is given) and the forward kernel.
+attn_status enqueue_forward(const void* q, const void* k, const void* v, void* out, float* lse,
+                            int B, int H, int H_kv, int S_q, int S_k, int D, float scale,
+                            const attn_mod_desc* mod, const void* bmask, void* mask_buf,
+                            DeviceStatus* status, cudaStream_t s) {
+  const Options o = options_snapshot();
+  const MaskParams mp = mask_params(S_q, S_k, mod);
+  const BlockMaskGeom g = block_mask_geom(B, S_q, S_k, mp.flags);
+  if (bmask == nullptr) {
+    if (launch_build_block_mask(B, S_q, S_k, mp, o.force_partial != 0.0 ? 1 : 0, mask_buf, s) !=
+        cudaSuccess)
+      return ATTN_ERR_CUDA;
+    bmask = mask_buf;
+  }
+  FwdArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.lse = lse;
+  a.B = B;
+  a.H = H;
+  a.H_kv = H_kv;
+  a.S_q = S_q;
+  a.S_k = S_k;
+  a.D = D;
+  a.scale = scale;
+  a.mask = mp;
+  a.score_flags = mod ? mod->score_flags : 0u;
+  a.softcap = mod ? mod->softcap : 0.f;
+  a.alibi_slopes = (mod && (mod->score_flags & ATTN_SCORE_ALIBI)) ? mod->alibi_slopes : nullptr;
+  a.block_mask = bmask;
+  a.n_entries = g.n_entries;
+  a.bm = g.bm;
+  a.nP = g.nP;
+  a.status = status;
+  a.rescale_threshold = (float)o.rescale_threshold;
+  a.wait_budget_ms = o.wait_budget_ms;
+  a.num_ctas = (int)o.num_ctas;
+  a.poly_fraction = (float)o.poly_fraction;
+  a.debug_stall = o.debug_stall != 0.0 ? 1 : 0;
+  return launch_attn_fwd(a, s) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 }  // namespace
 
 // ---- scratch for attn_fwd_noalloc ----------------------------------------
@@ -157,6 +240,98 @@ attn_status noalloc_scratch(int dev, void** out) {
     g_noalloc_ptr[dev] = ptr;
   }
   *out = g_noalloc_ptr[dev];
+  return ATTN_OK;
+}
+
+// ---- pipeline for attn_fwd_host -------------------------------------------
+// Host-memory callers pay for the copies in and out.  Each device gets three
+// streams of the library's own -- host-to-device copies, compute,
+// device-to-host copies -- and two slots of device memory used by
+// alternate calls, so one call's input copy runs while the previous call
+// computes and the one before copies its results out.  Every hand-over is
+// an event: a slot is refilled only after its previous results have left.
+struct HostSlot {
+  void* buf = nullptr;
+  size_t bytes = 0;
+  cudaEvent_t done = nullptr;  // the slot's last output copy
+  bool used = false;
+};
+struct HostPipe {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t h2d = nullptr, comp = nullptr, d2h = nullptr;
+  // hand-overs; each wait is enqueued before the event is recorded again
+  cudaEvent_t user = nullptr, in = nullptr, comp_ev = nullptr;
+  HostSlot slot[2];
+  int next = 0;
+};
+constexpr int kHostChunks = 8;
+constexpr int kHostMaxDevices = 64;
+std::mutex g_host_mu;
+HostPipe g_host[kHostMaxDevices];
+
+attn_status host_pipe(int dev, HostPipe** out) {
+  if (dev < 0 || dev >= kHostMaxDevices) return ATTN_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_host_mu);
+  HostPipe& p = g_host[dev];
+  if (!p.ready) {
+    const unsigned fl = cudaStreamNonBlocking;
+    const unsigned ev = cudaEventDisableTiming;
+    if (cudaStreamCreateWithFlags(&p.h2d, fl) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&p.comp, fl) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&p.d2h, fl) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.user, ev) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.in, ev) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p.comp_ev, ev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+    for (HostSlot& sl : p.slot)
+      if (cudaEventCreateWithFlags(&sl.done, ev) != cudaSuccess) return ATTN_ERR_CUDA;
+    p.ready = true;
+  }
+  *out = &p;
+  return ATTN_OK;
+}
+
+// Byte offsets of one call's device copies inside a slot.
+struct HostLayout {
+  size_t q, k, v, o, lse, doc, prefix, slopes, mask, total;
+};
+HostLayout host_layout(int B, int H, int H_kv, int S_q, int S_k, int D, const attn_mod_desc* mod) {
+  HostLayout l;
+  const size_t qb = (size_t)B * H * S_q * D * 2, kb = (size_t)B * H_kv * S_k * D * 2;
+  size_t at = 0;
+  auto take = [&](size_t bytes) {
+    const size_t off = at;
+    at = align_up(at + bytes, 256);
+    return off;
+  };
+  l.q = take(qb);
+  l.k = take(kb);
+  l.v = take(kb);
+  l.o = take(qb);
+  l.lse = take((size_t)B * H * S_q * 4);
+  l.doc = take((size_t)B * S_k * 4);
+  l.prefix = take((size_t)B * 4);
+  l.slopes = take((size_t)H * 4);
+  l.mask = take(block_mask_geom(1, S_q, S_k, mod ? mod->mask_flags : 0u).total);  // one batch entry
+  l.total = at;
+  return l;
+}
+
+// Grows a slot; its previous call must have finished with the old memory.
+attn_status ensure_slot_capacity(HostSlot* sl, size_t bytes) {
+  if (sl->bytes >= bytes) return ATTN_OK;
+  if (sl->buf != nullptr) {
+    if (sl->used && cudaEventSynchronize(sl->done) != cudaSuccess) return ATTN_ERR_CUDA;
+    cudaFree(sl->buf);
+    sl->buf = nullptr;
+    sl->bytes = 0;
+  }
+  if (cudaMalloc(&sl->buf, bytes) != cudaSuccess) {
+    sl->buf = nullptr;
+    return ATTN_ERR_CUDA;
+  }
+  sl->bytes = bytes;
   return ATTN_OK;
 }
 }  // namespace
@@ -327,24 +502,8 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, flo
   // ---- host-side validation: nothing is enqueued on failure ------------
   attn_status st = check_problem(B, H, S_q, S_k, mod);
   if (st != ATTN_OK) return st;
-  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return ATTN_ERR_INVALID_ARG;
-  if (H_kv <= 0 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
-  if (!(isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
-    return ATTN_ERR_INVALID_ARG;
-  if (lse != nullptr && !aligned(lse, 4)) return ATTN_ERR_INVALID_ARG;
-  const size_t qb = (size_t)B * H * S_q * D * 2, kb = (size_t)B * H_kv * S_k * D * 2;
-  if ((size_t)B * H > (size_t)INT32_MAX || (size_t)B * H_kv * (size_t)S_k > (size_t)INT32_MAX * 128)
-    return ATTN_ERR_INVALID_ARG;
-  if (overlaps(out, qb, q, qb) || overlaps(out, qb, k, kb) || overlaps(out, qb, v, kb))
-    return ATTN_ERR_INVALID_ARG;
-  if (lse != nullptr) {
-    const size_t lb = (size_t)B * H * S_q * 4;
-    if (overlaps(lse, lb, q, qb) || overlaps(lse, lb, k, kb) || overlaps(lse, lb, v, kb) ||
-        overlaps(lse, lb, out, qb))
-      return ATTN_ERR_INVALID_ARG;
-  }
+  st = check_device_tensors(q, k, v, out, lse, B, H, H_kv, S_q, S_k, D, scale);
+  if (st != ATTN_OK) return st;
   const uint32_t mflags = mod ? mod->mask_flags : 0u;
   const BlockMaskGeom g = block_mask_geom(B, S_q, S_k, mflags);
   if (mod != nullptr && mod->block_mask != nullptr &&
@@ -358,48 +517,13 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, flo
   DeviceScratch* scr = nullptr;
   st = scratch_for(dev, &scr);
   if (st != ATTN_OK) return st;
-  const Options o = options_snapshot();
-  const MaskParams mp = mask_params(S_q, S_k, mod);
-
   const void* bmask = (mod != nullptr) ? mod->block_mask : nullptr;
   if (bmask == nullptr) {
     st = ensure_mask_capacity(scr, g.total);
     if (st != ATTN_OK) return st;
-    if (launch_build_block_mask(B, S_q, S_k, mp, o.force_partial != 0.0 ? 1 : 0, scr->mask, s) !=
-        cudaSuccess)
-      return ATTN_ERR_CUDA;
-    bmask = scr->mask;
   }
-
-  FwdArgs a;
-  memset(&a, 0, sizeof(a));
-  a.q = q;
-  a.k = k;
-  a.v = v;
-  a.out = out;
-  a.lse = lse;
-  a.B = B;
-  a.H = H;
-  a.H_kv = H_kv;
-  a.S_q = S_q;
-  a.S_k = S_k;
-  a.D = D;
-  a.scale = scale;
-  a.mask = mp;
-  a.score_flags = mod ? mod->score_flags : 0u;
-  a.softcap = mod ? mod->softcap : 0.f;
-  a.alibi_slopes = (mod && (mod->score_flags & ATTN_SCORE_ALIBI)) ? mod->alibi_slopes : nullptr;
-  a.block_mask = bmask;
-  a.n_entries = g.n_entries;
-  a.bm = g.bm;
-  a.nP = g.nP;
-  a.status = scr->status;
-  a.rescale_threshold = (float)o.rescale_threshold;
-  a.wait_budget_ms = o.wait_budget_ms;
-  a.num_ctas = (int)o.num_ctas;
-  a.poly_fraction = (float)o.poly_fraction;
-  a.debug_stall = o.debug_stall != 0.0 ? 1 : 0;
-  return launch_attn_fwd(a, s) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  return enqueue_forward(q, k, v, out, lse, B, H, H_kv, S_q, S_k, D, scale, mod, bmask, scr->mask,
+                         scr->status, s);
 }
 
 attn_status attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse,
@@ -408,24 +532,8 @@ attn_status attn_fwd_noalloc(const void* q, const void* k, const void* v, void* 
   // ---- host-side validation (same rules as attn_fwd) -----------------------
   attn_status st = check_problem(B, H, S_q, S_k, mod);
   if (st != ATTN_OK) return st;
-  if (q == nullptr || k == nullptr || v == nullptr || out == nullptr) return ATTN_ERR_INVALID_ARG;
-  if (H_kv <= 0 || H % H_kv != 0) return ATTN_ERR_INVALID_ARG;
-  if (!(isfinite(scale) && scale > 0.f)) return ATTN_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return ATTN_ERR_UNSUPPORTED;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
-    return ATTN_ERR_INVALID_ARG;
-  if (lse != nullptr && !aligned(lse, 4)) return ATTN_ERR_INVALID_ARG;
-  const size_t qb = (size_t)B * H * S_q * D * 2, kb = (size_t)B * H_kv * S_k * D * 2;
-  if ((size_t)B * H > (size_t)INT32_MAX || (size_t)B * H_kv * (size_t)S_k > (size_t)INT32_MAX * 128)
-    return ATTN_ERR_INVALID_ARG;
-  if (overlaps(out, qb, q, qb) || overlaps(out, qb, k, kb) || overlaps(out, qb, v, kb))
-    return ATTN_ERR_INVALID_ARG;
-  if (lse != nullptr) {
-    const size_t lb = (size_t)B * H * S_q * 4;
-    if (overlaps(lse, lb, q, qb) || overlaps(lse, lb, k, kb) || overlaps(lse, lb, v, kb) ||
-        overlaps(lse, lb, out, qb))
-      return ATTN_ERR_INVALID_ARG;
-  }
+  st = check_device_tensors(q, k, v, out, lse, B, H, H_kv, S_q, S_k, D, scale);
+  if (st != ATTN_OK) return st;
   // The block mask is always built into the fixed scratch array.
   if (mod != nullptr && mod->block_mask != nullptr) return ATTN_ERR_INVALID_ARG;
   const uint32_t mflags = mod ? mod->mask_flags : 0u;
@@ -443,41 +551,133 @@ attn_status attn_fwd_noalloc(const void* q, const void* k, const void* v, void* 
   void* bmask = static_cast<char*>(scratch) + kNoAllocStatusBytes;
   // The status word must start at zero; the block mask is rewritten whole.
   if (cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s) != cudaSuccess) return ATTN_ERR_CUDA;
-  const Options o = options_snapshot();
-  const MaskParams mp = mask_params(S_q, S_k, mod);
-  if (launch_build_block_mask(B, S_q, S_k, mp, o.force_partial != 0.0 ? 1 : 0, bmask, s) !=
-      cudaSuccess)
+  return enqueue_forward(q, k, v, out, lse, B, H, H_kv, S_q, S_k, D, scale, mod, nullptr, bmask,
+                         status, s);
+}
+
+attn_status attn_fwd_host(const void* q, const void* k, const void* v, void* out, float* lse,
+                          int B, int H, int H_kv, int S_q, int S_k, int D, float scale,
+                          const attn_mod_desc* mod, attn_stream_t stream) {
+  // ---- host-side validation: nothing is enqueued on failure --------------
+  attn_status st = check_problem(B, H, S_q, S_k, mod);
+  if (st != ATTN_OK) return st;
+  st = check_tensors(q, k, v, out, lse, B, H, H_kv, S_q, S_k, D, scale);
+  if (st != ATTN_OK) return st;
+  if (mod != nullptr && mod->block_mask != nullptr) return ATTN_ERR_INVALID_ARG;
+  const HostLayout lay = host_layout(B, H, H_kv, S_q, S_k, D, mod);
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  DeviceScratch* scr = nullptr;
+  st = scratch_for(dev, &scr);
+  if (st != ATTN_OK) return st;
+  HostPipe* pipe = nullptr;
+  st = host_pipe(dev, &pipe);
+  if (st != ATTN_OK) return st;
+  std::lock_guard<std::mutex> lk(pipe->mu);
+  HostSlot& slot = pipe->slot[pipe->next];
+  st = ensure_slot_capacity(&slot, lay.total);
+  if (st != ATTN_OK) return st;
+  pipe->next ^= 1;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(slot.buf);
+  auto ck = [](cudaError_t e) { return e == cudaSuccess; };
+  const uint32_t mflags = mod ? mod->mask_flags : 0u;
+  const uint32_t sflags = mod ? mod->score_flags : 0u;
+  const int group = H / H_kv;
+  const size_t q_head = (size_t)S_q * D * 2, k_head = (size_t)S_k * D * 2;
+  const size_t l_head = (size_t)S_q * 4;
+  // Inputs start after the caller's earlier work on `stream` and after this
+  // slot's previous call has copied its results out.
+  bool ok = ck(cudaEventRecord(pipe->user, s)) && ck(cudaStreamWaitEvent(pipe->h2d, pipe->user, 0));
+  if (ok && slot.used) ok = ck(cudaStreamWaitEvent(pipe->h2d, slot.done, 0));
+  if (ok && (mflags & ATTN_MASK_DOCUMENT))
+    ok = ck(cudaMemcpyAsync(base + lay.doc, mod->doc_ids, (size_t)B * S_k * 4,
+                            cudaMemcpyHostToDevice, pipe->h2d));
+  if (ok && (mflags & ATTN_MASK_PREFIX_LM))
+    ok = ck(cudaMemcpyAsync(base + lay.prefix, mod->prefix_len, (size_t)B * 4,
+                            cudaMemcpyHostToDevice, pipe->h2d));
+  const bool alibi = (sflags & ATTN_SCORE_ALIBI) != 0;
+  if (ok && alibi && mod->alibi_slopes != nullptr)
+    ok = ck(cudaMemcpyAsync(base + lay.slopes, mod->alibi_slopes, (size_t)H * 4,
+                            cudaMemcpyHostToDevice, pipe->h2d));
+  if (!ok) return ATTN_ERR_CUDA;
+  // Slices of heads run as separate forwards, so the default ALiBi slopes
+  // (which depend on the head's index among all H) are written out once.
+  float* dslopes = reinterpret_cast<float*>(base + lay.slopes);
+  if (alibi && mod->alibi_slopes == nullptr &&
+      launch_default_alibi_slopes(dslopes, H, pipe->comp) != cudaSuccess)
     return ATTN_ERR_CUDA;
 
-  FwdArgs a;
-  memset(&a, 0, sizeof(a));
-  a.q = q;
-  a.k = k;
-  a.v = v;
-  a.out = out;
-  a.lse = lse;
-  a.B = B;
-  a.H = H;
-  a.H_kv = H_kv;
-  a.S_q = S_q;
-  a.S_k = S_k;
-  a.D = D;
-  a.scale = scale;
-  a.mask = mp;
-  a.score_flags = mod ? mod->score_flags : 0u;
-  a.softcap = mod ? mod->softcap : 0.f;
-  a.alibi_slopes = (mod && (mod->score_flags & ATTN_SCORE_ALIBI)) ? mod->alibi_slopes : nullptr;
-  a.block_mask = bmask;
-  a.n_entries = g.n_entries;
-  a.bm = g.bm;
-  a.nP = g.nP;
-  a.status = status;
-  a.rescale_threshold = (float)o.rescale_threshold;
-  a.wait_budget_ms = o.wait_budget_ms;
-  a.num_ctas = (int)o.num_ctas;
-  a.poly_fraction = (float)o.poly_fraction;
-  a.debug_stall = o.debug_stall != 0.0 ? 1 : 0;
-  return launch_attn_fwd(a, s) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  // The call runs in chunks -- one batch entry and a run of K/V heads with
+  // their query heads each -- so chunk c's compute overlaps chunk c+1's input
+  // copy and chunk c-1's output copy.  The host link, not the tensor cores,
+  // bounds this path; about eight chunks hide nearly all of the compute.
+  const int units = B * H_kv;
+  const int per = (units + kHostChunks - 1) / kHostChunks;  // K/V heads per chunk
+  const bool mask_per_batch = (mflags & (ATTN_MASK_DOCUMENT | ATTN_MASK_PREFIX_LM)) != 0;
+  int mask_b = -1;  // batch entry whose block mask is in the slot
+  for (int b = 0; b < B && ok; ++b) {
+    for (int kv0 = 0; kv0 < H_kv && ok; kv0 += per) {
+      const int kv1 = kv0 + per < H_kv ? kv0 + per : H_kv;
+      const int nkv = kv1 - kv0, nh = nkv * group;
+      const size_t qh0 = (size_t)b * H + (size_t)kv0 * group;  // first query head (flat)
+      const size_t kh0 = (size_t)b * H_kv + (size_t)kv0;       // first K/V head (flat)
+      ok = ck(cudaMemcpyAsync(base + lay.q + qh0 * q_head, static_cast<const char*>(q) + qh0 * q_head,
+                              (size_t)nh * q_head, cudaMemcpyHostToDevice, pipe->h2d)) &&
+           ck(cudaMemcpyAsync(base + lay.k + kh0 * k_head, static_cast<const char*>(k) + kh0 * k_head,
+                              (size_t)nkv * k_head, cudaMemcpyHostToDevice, pipe->h2d)) &&
+           ck(cudaMemcpyAsync(base + lay.v + kh0 * k_head, static_cast<const char*>(v) + kh0 * k_head,
+                              (size_t)nkv * k_head, cudaMemcpyHostToDevice, pipe->h2d)) &&
+           ck(cudaEventRecord(pipe->in, pipe->h2d)) &&
+           ck(cudaStreamWaitEvent(pipe->comp, pipe->in, 0));
+      if (!ok) break;
+      // this chunk as a problem of its own: batch 1, its heads, batch b's
+      // mask arrays
+      attn_mod_desc cm;
+      memset(&cm, 0, sizeof(cm));
+      if (mod != nullptr) cm = *mod;
+      cm.version = ATTN_MOD_DESC_VERSION;
+      cm.block_mask = nullptr;
+      cm.block_mask_bytes = 0;
+      if (mflags & ATTN_MASK_DOCUMENT)
+        cm.doc_ids = reinterpret_cast<const int32_t*>(base + lay.doc) + (size_t)b * S_k;
+      if (mflags & ATTN_MASK_PREFIX_LM)
+        cm.prefix_len = reinterpret_cast<const int32_t*>(base + lay.prefix) + b;
+      if (alibi) cm.alibi_slopes = dslopes + (size_t)kv0 * group;
+      // one block mask per batch entry (or one for all when the mask does
+      // not depend on the batch); the stream orders each rebuild after the
+      // forwards that read the previous one
+      const int want_b = mask_per_batch ? b : 0;
+      if (mask_b != want_b) {
+        const Options o = options_snapshot();
+        if (launch_build_block_mask(1, S_q, S_k, mask_params(S_q, S_k, &cm),
+                                    o.force_partial != 0.0 ? 1 : 0, base + lay.mask,
+                                    pipe->comp) != cudaSuccess)
+          return ATTN_ERR_CUDA;
+        mask_b = want_b;
+      }
+      float* dl = lse != nullptr ? reinterpret_cast<float*>(base + lay.lse) + qh0 * S_q : nullptr;
+      st = enqueue_forward(base + lay.q + qh0 * q_head, base + lay.k + kh0 * k_head,
+                           base + lay.v + kh0 * k_head, base + lay.o + qh0 * q_head, dl, 1, nh,
+                           nkv, S_q, S_k, D, scale, &cm, base + lay.mask, nullptr, scr->status,
+                           pipe->comp);
+      if (st != ATTN_OK) return st;
+      ok = ck(cudaEventRecord(pipe->comp_ev, pipe->comp)) &&
+           ck(cudaStreamWaitEvent(pipe->d2h, pipe->comp_ev, 0)) &&
+           ck(cudaMemcpyAsync(static_cast<char*>(out) + qh0 * q_head, base + lay.o + qh0 * q_head,
+                              (size_t)nh * q_head, cudaMemcpyDeviceToHost, pipe->d2h));
+      if (ok && lse != nullptr)
+        ok = ck(cudaMemcpyAsync(lse + qh0 * S_q, dl, (size_t)nh * l_head, cudaMemcpyDeviceToHost,
+                                pipe->d2h));
+    }
+  }
+  // `stream` continues once every result is in host memory
+  if (ok) ok = ck(cudaEventRecord(slot.done, pipe->d2h));
+  if (ok) slot.used = true;
+  if (ok) ok = ck(cudaStreamWaitEvent(s, slot.done, 0));
+  return ok ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -912,6 +912,20 @@ cudaError_t launch_d(const KParams& kp, bool alibi, bool softcap, int grid, cuda
 
 }  // namespace
 
+namespace {
+// The same expression as the forward kernel's default slope, in the same
+// translation unit and with the same compiler flags.
+__global__ void default_alibi_slopes_kernel(float* dst, int H) {
+  const int h = blockIdx.x * blockDim.x + threadIdx.x;
+  if (h < H) dst[h] = exp2f(-8.0f * (float)(h + 1) / (float)H);
+}
+}  // namespace
+
+cudaError_t launch_default_alibi_slopes(float* dst, int H, cudaStream_t stream) {
+  default_alibi_slopes_kernel<<<(H + 127) / 128, 128, 0, stream>>>(dst, H);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
   KParams kp;
   memset(&kp, 0, sizeof(kp));

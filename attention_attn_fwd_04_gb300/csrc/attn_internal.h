@@ -144,4 +144,8 @@ struct FwdArgs {
 
 cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream);
 
+// dst[h] = the default ALiBi slope of head h of H, bit for bit the value the
+// forward kernel computes when it is given no slopes.
+cudaError_t launch_default_alibi_slopes(float* dst, int H, cudaStream_t stream);
+
 }  // namespace attn

@@ -248,6 +248,39 @@ attn_status attn_fwd_noalloc(const void *q, const void *k, const void *v,
                              int S_q, int S_k, int D, float scale,
                              const attn_mod_desc *mod, attn_stream_t stream);
 
+/*
+ * attn_fwd_host -- attn_fwd on tensors in host memory.  The pages define
+ * only the on-device computation; this entry point has no counterpart there.
+ * It is the same forward (same kernels, same results bit for bit) with the
+ * copies in and out made by the library:
+ *
+ *  q, k, v, out, lse   host memory, same layouts and sizes as attn_fwd; no
+ *                      alignment needed; page-locked memory (cudaHostAlloc,
+ *                      torch pin_memory) for full copy speed, pageable
+ *                      memory works but its copies are synchronous
+ *  mod                 as for attn_fwd, except that doc_ids, prefix_len and
+ *                      alibi_slopes are host memory too and block_mask must
+ *                      be NULL (else ATTN_ERR_INVALID_ARG)
+ *  stream              the call starts after the work already enqueued on
+ *                      `stream`, and work enqueued on `stream` afterwards
+ *                      starts once O and LSE are in host memory
+ *
+ * Asynchronous like cudaMemcpyAsync: the inputs must stay unchanged and the
+ * outputs unread until `stream` has passed the call (synchronise it).  The
+ * copies and the kernels run on three streams owned by the library (per
+ * device), alternating between two device buffers of the library, so the
+ * input copy of one call overlaps the compute of the previous one and the
+ * output copy of the one before.  Those buffers are allocated on first use,
+ * grown (after the calls that use them finish) when a larger problem
+ * arrives, and kept until the process exits.  Calls on one device are
+ * serialised by a lock.  Errors as for attn_fwd; device-side failures are
+ * read with attn_get_device_status(stream).
+ */
+attn_status attn_fwd_host(const void *q, const void *k, const void *v,
+                          void *out, float *lse, int B, int H, int H_kv,
+                          int S_q, int S_k, int D, float scale,
+                          const attn_mod_desc *mod, attn_stream_t stream);
+
 /* Tuning options.  Process-wide; set them before enqueuing work. */
 typedef enum attn_option {
     /* Rescale O only when the running row max grows by more than this many

@@ -91,6 +91,28 @@ def test_host_validation_rejects_bad_arguments(attn):
     assert _call(attn, **ok, mod=m) == INVALID                      # prefix_len NULL
 
 
+def test_host_entry_point_validation(attn):
+    # attn_fwd_host checks its arguments before any CUDA call
+    lib = attn.lib()
+    buf = [ctypes.create_string_buffer(1 << 16) for _ in range(5)]
+    q, k, v, out, lse = (ctypes.addressof(b) for b in buf)
+    INVALID, UNSUP = 1, 2
+
+    def call(q=q, k=k, v=v, out=out, lse=lse, D=64, H=2, H_kv=2, mod=None):
+        return lib.attn_fwd_host(q, k, v, out, lse, 1, H, H_kv, 64, 64, D, 0.125,
+                                 ctypes.byref(mod) if mod is not None else None, None)
+
+    assert call(q=None) == INVALID
+    assert call(out=None) == INVALID
+    assert call(D=80) == UNSUP
+    assert call(H=3, H_kv=2) == INVALID
+    assert call(out=q) == INVALID                                   # out aliases q
+    m = attn.ModDesc()
+    m.version = 1
+    m.block_mask = k                                                # not accepted here
+    assert call(mod=m) == INVALID
+
+
 def test_block_mask_bytes_is_host_only(attn):
     lib = attn.lib()
     m = attn.ModDesc()
