@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for the attention forward -- TEST INFRASTRUCTURE ONLY.
+"""fp64 CPU oracle for the attention forward and backward -- TEST
+INFRASTRUCTURE ONLY.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
 leg may import this package.  The CUDA library never imports, links or calls
@@ -75,6 +76,20 @@ def _load():
         P, ctypes.c_int64,                         # rows n
         P, P, P,                                   # out lse probs
     ]
+    for name in ("oracle_attn_bwd_rows", "oracle_attn_bwd_keys"):
+        fn = getattr(lib, name)
+        fn.restype = ctypes.c_int
+        fn.argtypes = [
+            P, P, P, P,                                # q k v dout
+            ctypes.c_int, ctypes.c_int, ctypes.c_int,  # B H H_kv
+            ctypes.c_int, ctypes.c_int, ctypes.c_int,  # S_q S_k D
+            ctypes.c_double,                           # scale
+            ctypes.c_uint32, ctypes.c_uint32,          # mask / score flags
+            ctypes.c_int, ctypes.c_int,                # window q_offset
+            P, P, P,                                   # doc_ids prefix_len slopes
+            ctypes.c_double,                           # softcap
+            P, ctypes.c_int64,                         # rows / keys, n
+        ] + ([P] if name.endswith("rows") else [P, P])
     lib.oracle_num_threads.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     _lib = lib
@@ -178,6 +193,87 @@ def attn_rows(q, k, v, *, scale: float, rows: Optional[Sequence[int]] = None,
     if want_probs:
         return out, lse, probs
     return out, lse
+
+
+def _mod_args(B, H, S_k, causal, window, doc_ids, prefix_len, alibi, alibi_slopes,
+              softcap):
+    mask = 0
+    if causal:
+        mask |= MASK_CAUSAL
+    if window and window > 0:
+        mask |= MASK_WINDOW
+    if doc_ids is not None:
+        mask |= MASK_DOCUMENT
+    if prefix_len is not None:
+        mask |= MASK_PREFIX_LM
+    score = 0
+    if alibi or alibi_slopes is not None:
+        score |= SCORE_ALIBI
+    if softcap and softcap > 0:
+        score |= SCORE_SOFTCAP
+    docs = _i32(doc_ids)
+    if docs is not None:
+        docs = np.ascontiguousarray(np.broadcast_to(docs.reshape(-1, S_k), (B, S_k)))
+    pref = _i32(prefix_len)
+    slopes = None
+    if alibi_slopes is not None:
+        slopes = np.ascontiguousarray(np.asarray(alibi_slopes, dtype=np.float64))
+        assert slopes.shape == (H,)
+    cap32 = float(np.float32(softcap)) if softcap else 0.0
+    return mask, score, docs, pref, slopes, cap32
+
+
+def attn_bwd_rows(q, k, v, dout, *, scale: float, rows: Optional[Sequence[int]] = None,
+                  causal: bool = False, window: int = 0, doc_ids=None, prefix_len=None,
+                  alibi: bool = False, alibi_slopes: Optional[Sequence[float]] = None,
+                  softcap: float = 0.0, q_offset: int = 0):
+    """dQ of the requested query rows (flattened (b*H + h)*S_q + i; all when
+    None) for upstream gradient ``dout`` [B,H,S_q,D] (bf16), in float64:
+    an array [n, D]."""
+    lib = _load()
+    qb, kb, vb, gb = _bits(q), _bits(k), _bits(v), _bits(dout)
+    B, H, S_q, D = qb.shape
+    _, H_kv, S_k, _ = kb.shape
+    assert gb.shape == qb.shape and vb.shape == kb.shape
+    rows_a = (np.arange(B * H * S_q, dtype=np.int64) if rows is None
+              else np.ascontiguousarray(np.asarray(rows, dtype=np.int64)))
+    mask, score, docs, pref, slopes, cap32 = _mod_args(
+        B, H, S_k, causal, window, doc_ids, prefix_len, alibi, alibi_slopes, softcap)
+    dq = np.empty((rows_a.shape[0], D), dtype=np.float64)
+    rc = lib.oracle_attn_bwd_rows(
+        _ptr(qb), _ptr(kb), _ptr(vb), _ptr(gb), B, H, H_kv, S_q, S_k, D,
+        float(np.float32(scale)), mask, score, int(window or 0), int(q_offset), _ptr(docs),
+        _ptr(pref), _ptr(slopes), cap32, _ptr(rows_a), rows_a.shape[0], _ptr(dq))
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd_rows rejected its arguments")
+    return dq
+
+
+def attn_bwd_keys(q, k, v, dout, *, scale: float, keys: Optional[Sequence[int]] = None,
+                  causal: bool = False, window: int = 0, doc_ids=None, prefix_len=None,
+                  alibi: bool = False, alibi_slopes: Optional[Sequence[float]] = None,
+                  softcap: float = 0.0, q_offset: int = 0):
+    """dK and dV of the requested key positions (flattened
+    (b*H_kv + hk)*S_k + j; all when None), summed over the query heads that
+    share each K/V head, in float64: two arrays [n, D]."""
+    lib = _load()
+    qb, kb, vb, gb = _bits(q), _bits(k), _bits(v), _bits(dout)
+    B, H, S_q, D = qb.shape
+    _, H_kv, S_k, _ = kb.shape
+    assert gb.shape == qb.shape and vb.shape == kb.shape
+    keys_a = (np.arange(B * H_kv * S_k, dtype=np.int64) if keys is None
+              else np.ascontiguousarray(np.asarray(keys, dtype=np.int64)))
+    mask, score, docs, pref, slopes, cap32 = _mod_args(
+        B, H, S_k, causal, window, doc_ids, prefix_len, alibi, alibi_slopes, softcap)
+    dk = np.empty((keys_a.shape[0], D), dtype=np.float64)
+    dv = np.empty((keys_a.shape[0], D), dtype=np.float64)
+    rc = lib.oracle_attn_bwd_keys(
+        _ptr(qb), _ptr(kb), _ptr(vb), _ptr(gb), B, H, H_kv, S_q, S_k, D,
+        float(np.float32(scale)), mask, score, int(window or 0), int(q_offset), _ptr(docs),
+        _ptr(pref), _ptr(slopes), cap32, _ptr(keys_a), keys_a.shape[0], _ptr(dk), _ptr(dv))
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd_keys rejected its arguments")
+    return dk, dv
 
 
 def attn_workload_rows(w, inputs, rows=None, want_probs: bool = False):

@@ -1,5 +1,6 @@
 /*
- * attn_oracle.c -- fp64 CPU oracle for the masked / modified attention forward.
+ * attn_oracle.c -- fp64 CPU oracle for the masked / modified attention forward
+ * and its backward (gradients of Q, K, V).
  *
  * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
  * benchmark's CPU-baseline leg may call this code.  The CUDA library never
@@ -215,5 +216,326 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
         free(vis);
         free(qrow);
     }
+    return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Backward: gradients of the attention forward with respect to Q, K and V,
+ * given the gradient dO of the output, from the same plain definition.
+ *
+ * Source: the forward's definition above and calculus.  The pages name the
+ * backward pass as the step after the forward ("FlashAttention-4
+ * explained", section "FlashAttention-4: Built for Blackwell") but print no
+ * formula, so the gradient is written out from the chain rule:
+ *
+ *   x_ij  = scale * q_i . k_j                      (scaled score)
+ *   s_ij  = mod(x_ij)  (+ ALiBi bias, then cap * tanh(./cap))
+ *   p_ij  = exp(s_ij - LSE_i) on visible keys, 0 elsewhere
+ *   O_i   = sum_j p_ij v_j
+ *   dV_j  = sum_i p_ij dO_i                        (over every query head of
+ *   dP_ij = dO_i . v_j                              the K/V head's group)
+ *   dS_ij = p_ij (dP_ij - sum_j' p_ij' dP_ij')      (softmax Jacobian)
+ *         = p_ij (dP_ij - dO_i . O_i)
+ *   dX_ij = dS_ij * ds/dx,  ds/dx = 1, or 1 - (s_ij/cap)^2 with the soft cap
+ *   dQ_i  = scale * sum_j dX_ij k_j
+ *   dK_j  = scale * sum_i dX_ij q_i                (summed over the group)
+ *
+ * Rows with no visible key contribute nothing (p = 0 everywhere).
+ * ------------------------------------------------------------------------ */
+
+/* The forward of one query row: scores after the mods s[], visibility vis[],
+ * probabilities p[], the output row o[] and the natural-log LSE (-inf and
+ * all-zero p/o when no key is visible).  Returns 0, or -1 when no key is
+ * visible. */
+static int row_forward(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                       int b, int h, int64_t i, int H, int H_kv, int S_q, int S_k,
+                       int D, double scale, uint32_t mask_flags,
+                       uint32_t score_flags, int window, int q_offset,
+                       const int32_t *doc_ids, const int32_t *prefix_len,
+                       const double *alibi_slopes, double softcap, double *qrow,
+                       double *s, unsigned char *vis, double *p, double *o,
+                       double *lse)
+{
+    const int hk = h / (H / H_kv);
+    const uint16_t *qp = q + (((int64_t)b * H + h) * S_q + i) * D;
+    const uint16_t *kb = k + ((int64_t)b * H_kv + hk) * (int64_t)S_k * D;
+    const uint16_t *vb = v + ((int64_t)b * H_kv + hk) * (int64_t)S_k * D;
+    for (int d = 0; d < D; ++d)
+        qrow[d] = bf16_to_double(qp[d]);
+    double slope = 0.0;
+    if (score_flags & OR_SCORE_ALIBI)
+        slope = alibi_slopes ? alibi_slopes[h] : pow(2.0, -8.0 * (double)(h + 1) / (double)H);
+    const double qpos = (double)(i + q_offset);
+    double M = -INFINITY;
+    for (int64_t j = 0; j < S_k; ++j) {
+        const uint16_t *kp = kb + j * D;
+        double dot = 0.0;
+        for (int d = 0; d < D; ++d)
+            dot += qrow[d] * bf16_to_double(kp[d]);
+        double sj = scale * dot;
+        if (score_flags & OR_SCORE_ALIBI)
+            sj += -slope * (qpos - (double)j);
+        if (score_flags & OR_SCORE_SOFTCAP)
+            sj = softcap * tanh(sj / softcap);
+        s[j] = sj;
+        vis[j] = (unsigned char)visible(i, j, b, S_k, mask_flags, window, q_offset,
+                                        doc_ids, prefix_len);
+        if (vis[j] && sj > M)
+            M = sj;
+    }
+    for (int d = 0; d < D; ++d)
+        o[d] = 0.0;
+    if (M == -INFINITY) {
+        memset(p, 0, sizeof(double) * (size_t)S_k);
+        *lse = -INFINITY;
+        return -1;
+    }
+    double Z = 0.0;
+    for (int64_t j = 0; j < S_k; ++j)
+        if (vis[j])
+            Z += exp(s[j] - M);
+    for (int64_t j = 0; j < S_k; ++j) {
+        p[j] = vis[j] ? exp(s[j] - M) / Z : 0.0;
+        if (p[j] != 0.0) {
+            const uint16_t *vp = vb + j * D;
+            for (int d = 0; d < D; ++d)
+                o[d] += p[j] * bf16_to_double(vp[d]);
+        }
+    }
+    *lse = M + log(Z);
+    return 0;
+}
+
+/* d s / d x of the score modification at modified score s. */
+static double mod_slope(double s, uint32_t score_flags, double softcap)
+{
+    if (score_flags & OR_SCORE_SOFTCAP) {
+        double t = s / softcap;
+        return 1.0 - t * t;
+    }
+    return 1.0;
+}
+
+static int check_dims(int B, int H, int H_kv, int S_q, int S_k, int D, uint32_t mask_flags,
+                      uint32_t score_flags, const int32_t *doc_ids,
+                      const int32_t *prefix_len, double softcap)
+{
+    if (B <= 0 || H <= 0 || H_kv <= 0 || S_q <= 0 || S_k <= 0 || D <= 0)
+        return -1;
+    if (H % H_kv != 0)
+        return -1;
+    if ((mask_flags & OR_MASK_DOCUMENT) && (doc_ids == NULL || S_q != S_k))
+        return -1;
+    if ((mask_flags & OR_MASK_PREFIX_LM) && prefix_len == NULL)
+        return -1;
+    if ((score_flags & OR_SCORE_SOFTCAP) && !(softcap > 0.0))
+        return -1;
+    return 0;
+}
+
+/*
+ * oracle_attn_bwd_rows: dQ of a list of query rows.
+ *
+ *  q, k, v, arguments as oracle_attn_rows; dout bf16 bits [B][H][S_q][D]
+ *  rows   flattened (b*H + h)*S_q + i
+ *  dq     [n_rows][D] doubles
+ */
+int oracle_attn_bwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         const uint16_t *dout, int B, int H, int H_kv, int S_q, int S_k,
+                         int D, double scale, uint32_t mask_flags, uint32_t score_flags,
+                         int window, int q_offset, const int32_t *doc_ids,
+                         const int32_t *prefix_len, const double *alibi_slopes,
+                         double softcap, const int64_t *rows, int64_t n_rows, double *dq)
+{
+    if (check_dims(B, H, H_kv, S_q, S_k, D, mask_flags, score_flags, doc_ids, prefix_len,
+                   softcap))
+        return -1;
+    const int group = H / H_kv;
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)S_k);
+        double *p = (double *)malloc(sizeof(double) * (size_t)S_k);
+        unsigned char *vis = (unsigned char *)malloc((size_t)S_k);
+        double *qrow = (double *)malloc(sizeof(double) * (size_t)D);
+        double *o = (double *)malloc(sizeof(double) * (size_t)D);
+        double *g = (double *)malloc(sizeof(double) * (size_t)D);
+        if (!s || !p || !vis || !qrow || !o || !g) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t r = 0; r < n_rows; ++r) {
+                const int64_t row = rows[r];
+                if (row < 0 || row >= (int64_t)B * H * S_q) {
+#pragma omp atomic write
+                    bad = 1;
+                    continue;
+                }
+                const int64_t i = row % S_q;
+                const int h = (int)((row / S_q) % H);
+                const int b = (int)(row / ((int64_t)S_q * H));
+                const int hk = h / group;
+                double *dqr = dq + r * D;
+                for (int d = 0; d < D; ++d)
+                    dqr[d] = 0.0;
+                double lse;
+                if (row_forward(q, k, v, b, h, i, H, H_kv, S_q, S_k, D, scale, mask_flags,
+                                score_flags, window, q_offset, doc_ids, prefix_len,
+                                alibi_slopes, softcap, qrow, s, vis, p, o, &lse) != 0)
+                    continue;
+                const uint16_t *dop = dout + (((int64_t)b * H + h) * S_q + i) * D;
+                const uint16_t *kb = k + ((int64_t)b * H_kv + hk) * (int64_t)S_k * D;
+                const uint16_t *vb = v + ((int64_t)b * H_kv + hk) * (int64_t)S_k * D;
+                double delta = 0.0;
+                for (int d = 0; d < D; ++d) {
+                    g[d] = bf16_to_double(dop[d]);
+                    delta += g[d] * o[d];
+                }
+                for (int64_t j = 0; j < S_k; ++j) {
+                    if (p[j] == 0.0)
+                        continue;
+                    const uint16_t *vp = vb + j * D;
+                    double dp = 0.0;
+                    for (int d = 0; d < D; ++d)
+                        dp += g[d] * bf16_to_double(vp[d]);
+                    const double dx = p[j] * (dp - delta) * mod_slope(s[j], score_flags, softcap);
+                    const uint16_t *kp = kb + j * D;
+                    for (int d = 0; d < D; ++d)
+                        dqr[d] += scale * dx * bf16_to_double(kp[d]);
+                }
+            }
+        }
+        free(s);
+        free(p);
+        free(vis);
+        free(qrow);
+        free(o);
+        free(g);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * oracle_attn_bwd_keys: dK and dV of a list of key positions.
+ *
+ *  keys   flattened (b*H_kv + hk)*S_k + j
+ *  dk, dv [n_keys][D] doubles, summed over the H/H_kv query heads of the
+ *         K/V head
+ *
+ * Needs every query row of the K/V head's group: their LSE and
+ * dO_i . O_i are computed once per (b, hk) that appears in keys.
+ */
+int oracle_attn_bwd_keys(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         const uint16_t *dout, int B, int H, int H_kv, int S_q, int S_k,
+                         int D, double scale, uint32_t mask_flags, uint32_t score_flags,
+                         int window, int q_offset, const int32_t *doc_ids,
+                         const int32_t *prefix_len, const double *alibi_slopes,
+                         double softcap, const int64_t *keys, int64_t n_keys, double *dk,
+                         double *dv)
+{
+    if (check_dims(B, H, H_kv, S_q, S_k, D, mask_flags, score_flags, doc_ids, prefix_len,
+                   softcap))
+        return -1;
+    const int group = H / H_kv;
+    for (int64_t r = 0; r < n_keys; ++r)
+        if (keys[r] < 0 || keys[r] >= (int64_t)B * H_kv * S_k)
+            return -1;
+    const int64_t n_rows = (int64_t)group * S_q;  /* query rows of one K/V head */
+    double *lse = (double *)malloc(sizeof(double) * (size_t)n_rows);
+    double *delta = (double *)malloc(sizeof(double) * (size_t)n_rows);
+    if (!lse || !delta) {
+        free(lse);
+        free(delta);
+        return -1;
+    }
+    int bad = 0;
+    for (int64_t bh = 0; bh < (int64_t)B * H_kv; ++bh) {
+        int any = 0;
+        for (int64_t r = 0; r < n_keys; ++r)
+            if (keys[r] / S_k == bh)
+                any = 1;
+        if (!any)
+            continue;
+        const int b = (int)(bh / H_kv), hk = (int)(bh % H_kv);
+        /* every query row of the group: LSE and dO . O */
+#pragma omp parallel
+        {
+            double *s = (double *)malloc(sizeof(double) * (size_t)S_k);
+            double *p = (double *)malloc(sizeof(double) * (size_t)S_k);
+            unsigned char *vis = (unsigned char *)malloc((size_t)S_k);
+            double *qrow = (double *)malloc(sizeof(double) * (size_t)D);
+            double *o = (double *)malloc(sizeof(double) * (size_t)D);
+            if (!s || !p || !vis || !qrow || !o) {
+#pragma omp atomic write
+                bad = 1;
+            } else {
+#pragma omp for schedule(dynamic, 4)
+                for (int64_t rr = 0; rr < n_rows; ++rr) {
+                    const int h = hk * group + (int)(rr / S_q);
+                    const int64_t i = rr % S_q;
+                    double l;
+                    row_forward(q, k, v, b, h, i, H, H_kv, S_q, S_k, D, scale, mask_flags,
+                                score_flags, window, q_offset, doc_ids, prefix_len,
+                                alibi_slopes, softcap, qrow, s, vis, p, o, &l);
+                    const uint16_t *dop = dout + (((int64_t)b * H + h) * S_q + i) * D;
+                    double dd = 0.0;
+                    for (int d = 0; d < D; ++d)
+                        dd += bf16_to_double(dop[d]) * o[d];
+                    lse[rr] = l;
+                    delta[rr] = dd;
+                }
+            }
+            free(s);
+            free(p);
+            free(vis);
+            free(qrow);
+            free(o);
+        }
+        /* each requested key of this head: sum over the group's rows */
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t r = 0; r < n_keys; ++r) {
+            if (keys[r] / S_k != bh)
+                continue;
+            const int64_t j = keys[r] % S_k;
+            const uint16_t *kp = k + ((int64_t)bh * S_k + j) * D;
+            const uint16_t *vp = v + ((int64_t)bh * S_k + j) * D;
+            double *dkr = dk + r * D, *dvr = dv + r * D;
+            for (int d = 0; d < D; ++d)
+                dkr[d] = dvr[d] = 0.0;
+            for (int64_t rr = 0; rr < n_rows; ++rr) {
+                if (lse[rr] == -INFINITY)
+                    continue;
+                const int h = hk * group + (int)(rr / S_q);
+                const int64_t i = rr % S_q;
+                if (!visible(i, j, b, S_k, mask_flags, window, q_offset, doc_ids, prefix_len))
+                    continue;
+                const uint16_t *qp = q + (((int64_t)b * H + h) * S_q + i) * D;
+                const uint16_t *dop = dout + (((int64_t)b * H + h) * S_q + i) * D;
+                double dot = 0.0, dp = 0.0;
+                for (int d = 0; d < D; ++d) {
+                    dot += bf16_to_double(qp[d]) * bf16_to_double(kp[d]);
+                    dp += bf16_to_double(dop[d]) * bf16_to_double(vp[d]);
+                }
+                double sj = scale * dot;
+                if (score_flags & OR_SCORE_ALIBI) {
+                    const double slope = alibi_slopes
+                                             ? alibi_slopes[h]
+                                             : pow(2.0, -8.0 * (double)(h + 1) / (double)H);
+                    sj += -slope * ((double)(i + q_offset) - (double)j);
+                }
+                if (score_flags & OR_SCORE_SOFTCAP)
+                    sj = softcap * tanh(sj / softcap);
+                const double pj = exp(sj - lse[rr]);
+                const double dx = pj * (dp - delta[rr]) * mod_slope(sj, score_flags, softcap);
+                for (int d = 0; d < D; ++d) {
+                    dvr[d] += pj * bf16_to_double(dop[d]);
+                    dkr[d] += scale * dx * bf16_to_double(qp[d]);
+                }
+            }
+        }
+    }
+    free(lse);
+    free(delta);
     return bad ? -1 : 0;
 }
