@@ -29,6 +29,7 @@ __all__ = [
     "attn_fwd",
     "attn_fwd_into",
     "attn_fwd_host",
+    "attn_bwd",
     "build_block_mask",
     "block_mask_bytes",
     "block_mask_stats",
@@ -108,6 +109,9 @@ def _load() -> ctypes.CDLL:
     P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     lib.attn_fwd.restype = I
     lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F,
+                             ctypes.POINTER(ModDesc), P]
+    lib.attn_bwd.restype = I
+    lib.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F,
                              ctypes.POINTER(ModDesc), P]
     lib.attn_fwd_host.restype = I
     lib.attn_fwd_host.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F,
@@ -326,6 +330,44 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, return_lse: b
     lse = torch.empty((B, H, S_q), dtype=torch.float32, device=q.device) if return_lse else None
     attn_fwd_into(q, k, v, out, lse, stream=stream, **kw)
     return (out, lse) if return_lse else out
+
+
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor,
+             lse: torch.Tensor, dout: torch.Tensor, *, scale: Optional[float] = None,
+             stream: Optional[torch.cuda.Stream] = None, **mods):
+    """Gradients of :func:`attn_fwd`: returns ``(dQ, dK, dV)`` (bf16, shapes
+    of q, k, v) for the upstream gradient ``dout`` of ``out``.  ``out`` and
+    ``lse`` are the forward's results for the same inputs, scale and mods
+    (keywords as for :func:`attn_fwd`, without ``block_mask``)."""
+    B, H, S_q, D = q.shape
+    _, H_kv, S_k, _ = k.shape
+    dev = q.device
+    for name, t, shape, dt in (("q", q, (B, H, S_q, D), torch.bfloat16),
+                               ("k", k, (B, H_kv, S_k, D), torch.bfloat16),
+                               ("v", v, (B, H_kv, S_k, D), torch.bfloat16),
+                               ("out", out, (B, H, S_q, D), torch.bfloat16),
+                               ("lse", lse, (B, H, S_q), torch.float32),
+                               ("dout", dout, (B, H, S_q, D), torch.bfloat16)):
+        if (t.device != dev or t.dtype != dt or not t.is_contiguous()
+                or tuple(t.shape) != shape):
+            raise ValueError("%s must be a contiguous %s %s tensor on %s" % (name, dt, shape, dev))
+    _check_mask_arrays(dev, mods.get("doc_ids"), mods.get("prefix_len"), mods.get("alibi_slopes"))
+    if "block_mask" in mods:
+        raise ValueError("attn_bwd builds its own block masks")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    m, keep = _mod_desc(**mods)
+    with torch.cuda.device(dev):
+        st = _lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                           lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                           dv.data_ptr(), B, H, H_kv, S_q, S_k, D, float(scale),
+                           ctypes.byref(m), _stream_ptr(stream, dev))
+    del keep
+    _check(st, "attn_bwd")
+    return dq, dk, dv
 
 
 def attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *,

@@ -82,6 +82,37 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
+// Per-device scratch of attn_bwd: its own block masks (forward and
+// transposed) and the row statistics, grown on demand like the forward's.
+struct BwdScratch {
+  void* buf = nullptr;
+  size_t bytes = 0;
+};
+std::mutex g_bwd_mu;
+std::vector<BwdScratch> g_bwd;
+
+attn_status bwd_scratch(int dev, size_t bytes, void** out) {
+  std::lock_guard<std::mutex> lk(g_bwd_mu);
+  if ((int)g_bwd.size() <= dev) g_bwd.resize(dev + 1);
+  BwdScratch& s = g_bwd[dev];
+  if (s.bytes < bytes) {
+    if (s.buf != nullptr) {
+      if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+      cudaFree(s.buf);
+      s.buf = nullptr;
+      s.bytes = 0;
+    }
+    const size_t cap = align_up(bytes, 1u << 20);
+    if (cudaMalloc(&s.buf, cap) != cudaSuccess) {
+      s.buf = nullptr;
+      return ATTN_ERR_CUDA;
+    }
+    s.bytes = cap;
+  }
+  *out = s.buf;
+  return ATTN_OK;
+}
+
 // Shape and mod checks shared by every entry point.
 attn_status check_problem(int B, int H, int S_q, int S_k, const attn_mod_desc* mod) {
   if (B <= 0 || H <= 0 || S_q <= 0 || S_k <= 0) return ATTN_ERR_INVALID_ARG;
@@ -678,6 +709,87 @@ attn_status attn_fwd_host(const void* q, const void* k, const void* v, void* out
   if (ok) slot.used = true;
   if (ok) ok = ck(cudaStreamWaitEvent(s, slot.done, 0));
   return ok ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                     const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                     int H, int H_kv, int S_q, int S_k, int D, float scale,
+                     const attn_mod_desc* mod, attn_stream_t stream) {
+  // ---- host-side validation: nothing is enqueued on failure --------------
+  attn_status st = check_problem(B, H, S_q, S_k, mod);
+  if (st != ATTN_OK) return st;
+  st = check_device_tensors(q, k, v, out, lse, B, H, H_kv, S_q, S_k, D, scale);
+  if (st != ATTN_OK) return st;
+  if (lse == nullptr || dout == nullptr || dq == nullptr || dk == nullptr || dv == nullptr)
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned(dout, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16))
+    return ATTN_ERR_INVALID_ARG;
+  if (mod != nullptr && mod->block_mask != nullptr) return ATTN_ERR_INVALID_ARG;
+  const size_t qb = (size_t)B * H * S_q * D * 2, kb = (size_t)B * H_kv * S_k * D * 2;
+  const size_t lb = (size_t)B * H * S_q * 4;
+  const void* ins[6] = {q, k, v, out, lse, dout};
+  const size_t in_b[6] = {qb, kb, kb, qb, lb, qb};
+  void* outs[3] = {dq, dk, dv};
+  const size_t out_b[3] = {qb, kb, kb};
+  for (int o = 0; o < 3; ++o) {
+    for (int i = 0; i < 6; ++i)
+      if (overlaps(outs[o], out_b[o], ins[i], in_b[i])) return ATTN_ERR_INVALID_ARG;
+    for (int o2 = 0; o2 < o; ++o2)
+      if (overlaps(outs[o], out_b[o], outs[o2], out_b[o2])) return ATTN_ERR_INVALID_ARG;
+  }
+
+  // ---- device work -------------------------------------------------------
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  DeviceScratch* scr = nullptr;
+  st = scratch_for(dev, &scr);
+  if (st != ATTN_OK) return st;
+  const uint32_t mflags = mod ? mod->mask_flags : 0u;
+  const BlockMaskGeom g = block_mask_geom(B, S_q, S_k, mflags);
+  const BlockMaskTGeom gt = block_mask_t_geom(B, S_q, S_k, mflags);
+  const size_t off_t = align_up(g.total, 256);
+  const size_t off_r = align_up(off_t + gt.total, 256);
+  const size_t total = off_r + bwd_rowstat_bytes(B, H, S_q);
+  void* buf = nullptr;
+  st = bwd_scratch(dev, total, &buf);
+  if (st != ATTN_OK) return st;
+  char* base = static_cast<char*>(buf);
+  const Options o = options_snapshot();
+  const MaskParams mp = mask_params(S_q, S_k, mod);
+  const int fp = o.force_partial != 0.0 ? 1 : 0;
+  if (launch_build_block_mask(B, S_q, S_k, mp, fp, base, s) != cudaSuccess ||
+      launch_build_block_mask_t(B, S_q, S_k, mp, fp, base, base + off_t, s) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  BwdArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.lse = lse;
+  a.dout = dout;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.B = B;
+  a.H = H;
+  a.H_kv = H_kv;
+  a.S_q = S_q;
+  a.S_k = S_k;
+  a.D = D;
+  a.scale = scale;
+  a.mask = mp;
+  a.score_flags = mod ? mod->score_flags : 0u;
+  a.softcap = mod ? mod->softcap : 0.f;
+  a.alibi_slopes = (mod && (mod->score_flags & ATTN_SCORE_ALIBI)) ? mod->alibi_slopes : nullptr;
+  a.block_mask = base;
+  a.block_mask_t = base + off_t;
+  a.rowstat = reinterpret_cast<float*>(base + off_r);
+  a.status = scr->status;
+  a.wait_budget_ms = o.wait_budget_ms;
+  a.force_partial = fp;
+  return launch_attn_bwd(a, s) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -1,0 +1,1079 @@
+// attn_bwd_sm103.cu -- attention backward for GB300 (sm_103a): dQ, dK, dV.
+//
+// The gradients of the forward (softmax attention with the same masks and
+// score mods), by the chain rule:
+//   P  = exp(S' - LSE)            S' the modified score, LSE from the forward
+//   dP = dO V^T
+//   dS = P * (dP - rowsum(dO * O)) * dS'/dS
+//   dQ = scale * dS K,   dK = scale * dS^T Q,   dV = P^T dO
+// ("FlashAttention-4 explained", section "FlashAttention-4: Built for
+// Blackwell", names the backward as the step after the forward; the
+// recomputation of P from the saved LSE instead of storing it is the same
+// principle as "Enter Tri Dao and FlashAttention": the score matrix never
+// goes to HBM.)
+//
+// Three kernels:
+//   bwd_prep_kernel   per query row: LSE in log2 units and dO . O, padded to
+//                     whole 128-row tiles (padding rows get +inf / 0, so
+//                     they contribute P = 0 without a mask)
+//   bwd_dq_kernel     one 128-row query tile per work item: for each key tile
+//                     of its block-mask list, S = Q K^T and dP = dO V^T into
+//                     Tensor Memory, dS by the elementwise warpgroup (one
+//                     thread per query row), dQ += dS K accumulated in Tensor
+//                     Memory
+//   bwd_dkdv_kernel   one 128-key tile per work item (K/V head, all query
+//                     heads of its group): S^T = K Q^T and dP^T = V dO^T, then
+//                     P^T and dS^T by the elementwise warpgroup (one thread
+//                     per key), dV += P^T dO and dK += dS^T Q accumulated in
+//                     Tensor Memory (GQA sums over the group in place)
+// Neither kernel uses atomics: every output row is written once by the work
+// item that owns it, so results are deterministic.
+//
+// Warp roles (256 threads): warps 0-3 elementwise (one TMEM lane quarter
+// each), warp 4 TMA loads, warp 5 allocates Tensor Memory and issues the
+// MMAs, warps 6-7 only join the teardown.  Every wait is bounded like the
+// forward's: on expiry the kernel records ATTN_ERR_TIMEOUT and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "attn_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace attn {
+
+namespace {
+
+constexpr int kBThreads = 256;
+constexpr int kBLoadWarp = 4;
+constexpr int kBMmaWarp = 5;
+constexpr uint32_t kBTmemCols = 512;
+constexpr float kBLog2e = 1.4426950408889634f;
+
+enum BSite : int {
+  kBSiteHeader = 101,
+  kBSiteLoad = 110,
+  kBSiteMma = 120,
+  kBSiteElem = 130,
+  kBSiteDrain = 140,
+};
+
+template <int D>
+struct BCfg {
+  static constexpr int kHalfBytes = kTileM * 64 * 2;  // 128 rows x 64 bf16, 128-byte swizzle
+  static constexpr int kHalves = D / 64;
+  static constexpr int kTileBytes = kHalves * kHalfBytes;
+  // bwd_dq_kernel: Q, dO, then two stages of (K, V)
+  static constexpr int kDqQ = 0;
+  static constexpr int kDqDo = kTileBytes;
+  static constexpr int kDqKV = 2 * kTileBytes;
+  static constexpr int kDqBar = kDqKV + 2 * 2 * kTileBytes;
+  // bwd_dkdv_kernel: K, V, then two stages of (Q, dO, LSE2[128], Delta[128])
+  static constexpr int kKvK = 0;
+  static constexpr int kKvV = kTileBytes;
+  static constexpr int kKvStage0 = 2 * kTileBytes;
+  static constexpr int kKvStageBytes = 2 * kTileBytes + 1024;
+  static constexpr int kKvBar = kKvStage0 + 2 * kKvStageBytes;
+  static constexpr int kNumBars = 16;
+  static constexpr int kSmemDq = kDqBar + 8 * kNumBars + 16;
+  static constexpr int kSmemKv = kKvBar + 8 * kNumBars + 16;
+  static constexpr int kSmemAllocDq = kSmemDq + 1024;
+  static constexpr int kSmemAllocKv = kSmemKv + 1024;
+};
+
+struct BParams {
+  CUtensorMap tmap_q;
+  CUtensorMap tmap_k;
+  CUtensorMap tmap_v;
+  CUtensorMap tmap_do;
+  __nv_bfloat16* dq;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
+  const float* lse2;   // [B*H][nQ*128]
+  const float* delta;  // [B*H][nQ*128]
+  int B, H, H_kv, S_q, S_k, group, nQ, nK, nP, bm;
+  float scale, scale_log2, softcap;
+  uint32_t mask_flags;
+  int window, q_offset;
+  const int32_t* doc_ids;
+  const int32_t* prefix_len;
+  const int32_t* doc_lo;
+  const int32_t* doc_hi;
+  const float* alibi_slopes;
+  const BlockMaskHeader* hdr;
+  const int32_t* cnt;      // forward block mask: per query-tile pair
+  const uint32_t* list;
+  const int32_t* cnt_t;    // transposed: per key tile
+  const uint32_t* list_t;
+  int n_items;
+  DeviceStatus* status;
+  uint64_t budget_ns;
+};
+
+struct BCtl {
+  volatile int* abort;
+  uint32_t abort_smem;
+  DeviceStatus* status;
+  uint64_t budget_ns;
+};
+
+__device__ __noinline__ void breport(const BCtl& c, int code, int site, int detail) {
+  if (atomicCAS(&c.status->code, 0, code) == 0) {
+    c.status->where = site;
+    c.status->block = blockIdx.x;
+    c.status->detail = detail;
+  }
+  *c.abort = 1;
+}
+
+// Bounded mbarrier wait (see the forward kernel's): false on timeout or when
+// another role has aborted.
+__device__ __forceinline__ bool bwait(uint32_t bar, uint32_t parity, const BCtl& c, int site) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = 0;
+  for (uint32_t spin = 1;; ++spin) {
+    if (ptx::mbar_try_wait_hint(bar, parity, 20000)) return true;
+    if ((spin & 15) == 0) {
+      if (ptx::ld_volatile_shared(c.abort_smem)) return false;
+      const uint64_t now = ptx::globaltimer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > c.budget_ns) {
+        breport(c, ATTN_ERR_TIMEOUT, site, (int)parity);
+        return false;
+      }
+    }
+  }
+}
+
+template <int D>
+struct BDesc {
+  static constexpr uint64_t kKMajor = ptx::smem_desc_sw128(0, 16, 1024);
+  static constexpr uint64_t kMNMajor = ptx::smem_desc_sw128(0, BCfg<D>::kHalfBytes, 1024);
+};
+
+// C = A B^T over the head dimension with both operands K-major 128 x D
+// tiles in shared memory (8 or 4 MMAs, K = 16 each).  Warp-wide.
+template <int D>
+__device__ __forceinline__ void mma_nt(uint32_t tmem_c, uint64_t a_desc, uint64_t b_desc) {
+  constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTileM, kTileN, false);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    const uint64_t off = (uint64_t)(((kk / 4) * BCfg<D>::kHalfBytes + (kk % 4) * 32) >> 4);
+    ptx::mma_ss_elect(tmem_c, a_desc + off, b_desc + off, idesc, kk > 0 ? 1u : 0u);
+  }
+}
+
+// C (+)= A B with A 128 x 128 bf16 packed in Tensor Memory (the 64 packed
+// columns at tmem_a) and B a 128 x D tile in shared memory read MN-major.
+template <int D>
+__device__ __forceinline__ void mma_tn(uint32_t tmem_c, uint32_t tmem_a, uint64_t b_desc,
+                                       bool accumulate) {
+  constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTileM, D, true);
+#pragma unroll
+  for (int kk = 0; kk < kTileN / 16; ++kk)
+    ptx::mma_ts_elect(tmem_c, tmem_a + (uint32_t)(kk * 8), b_desc + (uint64_t)((kk * 2048) >> 4),
+                      idesc, (accumulate || kk > 0) ? 1u : 0u);
+}
+
+// After an abort, let a loader's copies in flight land before the CTA
+// exits: wait (bounded) for the last phase issued on each of n_stages
+// barriers that saw `issued` loads in total (round-robin).
+__device__ __forceinline__ void drain_loads(uint32_t bar0, int n_stages, uint32_t issued,
+                                            uint64_t budget_ns) {
+  const uint32_t first = issued > (uint32_t)n_stages ? issued - n_stages : 0;
+  for (uint32_t c = first; c < issued; ++c) {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (!ptx::mbar_try_wait(bar0 + 8u * (c % n_stages), (c / n_stages) & 1) &&
+           ptx::globaltimer_ns() - t0 < budget_ns) {
+    }
+  }
+}
+
+// Static snake schedule over the items (as the forward's).
+__device__ __forceinline__ int bitem_of(int r) {
+  const int G = gridDim.x, c = blockIdx.x;
+  return r * G + ((r & 1) ? (G - 1 - c) : c);
+}
+
+// The score transform in log2 units, as in the forward kernel.
+struct ScoreMod {
+  float sc, slope2, capl2;
+};
+template <bool ALIBI, bool SOFTCAP>
+__device__ __forceinline__ float score_t(float s, float bias_pos, const ScoreMod& m) {
+  float x = s * m.sc;
+  if constexpr (ALIBI) x = fmaf(m.slope2, bias_pos, x);
+  if constexpr (SOFTCAP) {
+    const float e = ptx::ex2_approx(x);
+    x = m.capl2 * (1.0f - 2.0f * ptx::rcp_approx(e + 1.0f));
+  }
+  return x;
+}
+template <bool ALIBI, bool SOFTCAP>
+__device__ __forceinline__ ScoreMod make_mod(const BParams& p, int h) {
+  ScoreMod m;
+  m.sc = SOFTCAP ? p.scale * (2.0f * kBLog2e / p.softcap) : p.scale_log2;
+  m.capl2 = p.softcap * kBLog2e;
+  m.slope2 = 0.f;
+  if constexpr (ALIBI) {
+    const float mh =
+        p.alibi_slopes ? p.alibi_slopes[h] : exp2f(-8.0f * (float)(h + 1) / (float)p.H);
+    m.slope2 = SOFTCAP ? mh * (2.0f * kBLog2e / p.softcap) : mh * kBLog2e;
+  }
+  return m;
+}
+
+// Visible key interval of query row i (forward orientation).
+__device__ __forceinline__ void row_keys(const BParams& p, int b, int i, bool docs_sorted,
+                                         int& lo, int& hi) {
+  const int qpos = i + p.q_offset;
+  lo = 0;
+  hi = p.S_k - 1;
+  if (p.mask_flags & ATTN_MASK_CAUSAL) hi = min(hi, qpos);
+  if (p.mask_flags & ATTN_MASK_WINDOW) {
+    lo = max(lo, qpos - p.window + 1);
+    hi = min(hi, qpos);
+  }
+  if (p.mask_flags & ATTN_MASK_PREFIX_LM) hi = min(hi, max(qpos, p.prefix_len[b] - 1));
+  if ((p.mask_flags & ATTN_MASK_DOCUMENT) && docs_sorted && i < p.S_q) {
+    const size_t di = (size_t)b * p.S_k + (size_t)i;
+    lo = max(lo, p.doc_lo[di]);
+    hi = min(hi, p.doc_hi[di]);
+  }
+}
+
+// Query rows that see key j (transposed orientation): the interval
+// [ilo, ihi] of query indices, from the same mask rules.
+__device__ __forceinline__ void key_rows(const BParams& p, int b, int j, bool docs_sorted,
+                                         int& ilo, int& ihi) {
+  long long lo = 0, hi = (long long)p.S_q - 1;
+  const long long first = (long long)j - p.q_offset;  // query index whose qpos == j
+  if (p.mask_flags & ATTN_MASK_CAUSAL) lo = max(lo, first);
+  if (p.mask_flags & ATTN_MASK_WINDOW) {
+    lo = max(lo, first);
+    hi = min(hi, first + p.window - 1);
+  }
+  if ((p.mask_flags & ATTN_MASK_PREFIX_LM) && !(j < p.prefix_len[b])) lo = max(lo, first);
+  if ((p.mask_flags & ATTN_MASK_DOCUMENT) && docs_sorted && j < p.S_k) {
+    const size_t di = (size_t)b * p.S_k + (size_t)j;
+    lo = max(lo, (long long)p.doc_lo[di]);
+    hi = min(hi, (long long)p.doc_hi[di]);
+  }
+  ilo = (int)max(lo, -1ll);
+  ihi = (int)min(hi, (long long)p.S_q);
+}
+
+// ---------------------------------------------------------------- prep ----
+// lse2[r] = LSE * log2(e) (+inf where the row has no visible key or r is
+// padding); delta[r] = dO_r . O_r (0 for padding).  One warp per row.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* out,
+                                                       const __nv_bfloat16* dout,
+                                                       const float* lse, float* lse2,
+                                                       float* delta, int BH, int S_q, int nQ) {
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+  const long long rows = (long long)BH * nQ * kTileM;
+  const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  const long long bh = r / ((long long)nQ * kTileM);
+  const int i = (int)(r % ((long long)nQ * kTileM));
+  float acc = 0.f;
+  if (i < S_q) {
+    const size_t base = ((size_t)bh * S_q + (size_t)i) * D;
+    for (int d = lane * 2; d < D; d += 64) {
+      const __nv_bfloat162 o2 = *reinterpret_cast<const __nv_bfloat162*>(out + base + d);
+      const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(dout + base + d);
+      acc = fmaf(__bfloat162float(o2.x), __bfloat162float(g2.x), acc);
+      acc = fmaf(__bfloat162float(o2.y), __bfloat162float(g2.y), acc);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) {
+    float l2 = INFINITY;
+    if (i < S_q) {
+      const float l = lse[(size_t)bh * S_q + (size_t)i];
+      if (l != -INFINITY) l2 = l * kBLog2e;
+    }
+    lse2[r] = l2;
+    delta[r] = acc;
+  }
+}
+
+// ------------------------------------------------------------------ dQ ----
+template <int D, bool ALIBI, bool SOFTCAP>
+__global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_constant__ BParams p) {
+  using C = BCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_addr(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  ptx::griddep_wait();
+  const int docs_sorted = p.hdr->docs_sorted;
+
+  auto bar = [&](int i) { return sbase + (uint32_t)(C::kDqBar + 8 * i); };
+  enum { QF = 0, QE = 1, KVF = 2, KVE = 4, SF = 6, DSF = 7, DQF = 8, DQE = 9, DRAIN = 10 };
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kDqBar + 8 * C::kNumBars);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kDqBar + 8 * C::kNumBars + 4);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(QF), 1);
+    ptx::mbar_init(bar(QE), 1);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(bar(KVF + s), 1);
+      ptx::mbar_init(bar(KVE + s), 1);
+    }
+    ptx::mbar_init(bar(SF), 1);
+    ptx::mbar_init(bar(DSF), 4);
+    ptx::mbar_init(bar(DQF), 1);
+    ptx::mbar_init(bar(DQE), 4);
+    ptx::mbar_init(bar(DRAIN), 1);
+    *s_abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kBMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_addr(s_tmem), kBTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const BCtl ctl{s_abort, sbase + (uint32_t)(C::kDqBar + 8 * C::kNumBars + 4), p.status,
+                 p.budget_ns};
+
+  // Item w -> (b, h, query tile); its key tiles are the forward mask's list
+  // of the tile's pair, skipping the entries EMPTY for this tile.
+  struct It {
+    int b, h, qt, t, n;
+    const uint32_t* lst;
+  };
+  auto item = [&](int w) {
+    It it;
+    it.qt = w % p.nQ;
+    const int bh = w / p.nQ;
+    it.b = bh / p.H;
+    it.h = bh % p.H;
+    it.t = it.qt & 1;
+    const int e = (p.bm == 1 ? 0 : it.b) * p.nP + (it.qt >> 1);
+    it.n = p.cnt[e];
+    it.lst = p.list + (size_t)e * p.nK;
+    return it;
+  };
+  auto nonempty = [&](const It& it) {
+    int m = 0;
+    for (int j = 0; j < it.n; ++j) m += entry_cls(it.lst[j], it.t) != kEmpty;
+    return m;
+  };
+
+  if (warp == kBLoadWarp) {
+    if (lane == 0) {
+      ptx::prefetch_tmap(&p.tmap_q);
+      ptx::prefetch_tmap(&p.tmap_do);
+      ptx::prefetch_tmap(&p.tmap_k);
+      ptx::prefetch_tmap(&p.tmap_v);
+      const uint64_t pol = ptx::policy_evict_last();
+      uint32_t kv_cnt = 0, q_issued = 0;
+      int act = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int w = bitem_of(r);
+        if (w >= p.n_items) break;
+        const It it = item(w);
+        if (nonempty(it) == 0) continue;
+        if (act > 0) ok = bwait(bar(QE), (act - 1) & 1, ctl, kBSiteLoad);
+        if (!ok) break;
+        ptx::mbar_arrive_expect_tx(bar(QF), 2 * C::kTileBytes);
+        q_issued = act + 1;
+        for (int hx = 0; hx < C::kHalves; ++hx) {
+          ptx::tma_load_3d(sbase + C::kDqQ + hx * C::kHalfBytes, &p.tmap_q, bar(QF), hx * 64,
+                           it.qt * kTileM, it.b * p.H + it.h, pol);
+          ptx::tma_load_3d(sbase + C::kDqDo + hx * C::kHalfBytes, &p.tmap_do, bar(QF), hx * 64,
+                           it.qt * kTileM, it.b * p.H + it.h, pol);
+        }
+        const int kvz = it.b * p.H_kv + it.h / p.group;
+        for (int j = 0; j < it.n && ok; ++j) {
+          if (entry_cls(it.lst[j], it.t) == kEmpty) continue;
+          const int st = (int)(kv_cnt & 1);
+          if (kv_cnt >= 2) ok = bwait(bar(KVE + st), ((kv_cnt >> 1) - 1) & 1, ctl, kBSiteLoad);
+          if (!ok) break;
+          const int row0 = (int)entry_tile(it.lst[j]) * kTileN;
+          const uint32_t kdst = sbase + C::kDqKV + st * 2 * C::kTileBytes;
+          ptx::mbar_arrive_expect_tx(bar(KVF + st), 2 * C::kTileBytes);
+          for (int hx = 0; hx < C::kHalves; ++hx) {
+            ptx::tma_load_3d(kdst + hx * C::kHalfBytes, &p.tmap_k, bar(KVF + st), hx * 64, row0,
+                             kvz, pol);
+            ptx::tma_load_3d(kdst + C::kTileBytes + hx * C::kHalfBytes, &p.tmap_v, bar(KVF + st),
+                             hx * 64, row0, kvz, pol);
+          }
+          ++kv_cnt;
+        }
+        ++act;
+      }
+      if (!ok) {
+        drain_loads(bar(QF), 1, q_issued, p.budget_ns);
+        drain_loads(bar(KVF), 2, kv_cnt, p.budget_ns);
+      }
+    }
+  } else if (warp == kBMmaWarp) {
+    const uint32_t tS = tmem, tP = tmem + 128u, tQ = tmem + 256u;
+    const uint64_t q_desc = BDesc<D>::kKMajor + ((sbase + C::kDqQ) >> 4);
+    const uint64_t do_desc = BDesc<D>::kKMajor + ((sbase + C::kDqDo) >> 4);
+    auto waitw = [&](uint32_t b, uint32_t par) {
+      return __all_sync(0xffffffffu, bwait(b, par, ctl, kBSiteMma));
+    };
+    uint32_t kv_cnt = 0, ds_cnt = 0;
+    int act = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int w = bitem_of(r);
+      if (w >= p.n_items) break;
+      const It it = item(w);
+      if (nonempty(it) == 0) continue;
+      ok = waitw(bar(QF), act & 1);
+      if (ok && act > 0) ok = waitw(bar(DQE), (act - 1) & 1);
+      if (!ok) break;
+      int u = 0;
+      for (int j = 0; j < it.n && ok; ++j) {
+        if (entry_cls(it.lst[j], it.t) == kEmpty) continue;
+        const int st = (int)(kv_cnt & 1);
+        ok = waitw(bar(KVF + st), (kv_cnt >> 1) & 1);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint32_t kaddr = sbase + C::kDqKV + st * 2 * C::kTileBytes;
+        const uint64_t k_kmaj = BDesc<D>::kKMajor + (kaddr >> 4);
+        const uint64_t v_kmaj = BDesc<D>::kKMajor + ((kaddr + C::kTileBytes) >> 4);
+        const uint64_t k_mn = BDesc<D>::kMNMajor + (kaddr >> 4);
+        mma_nt<D>(tS, q_desc, k_kmaj);    // S = Q K^T
+        mma_nt<D>(tP, do_desc, v_kmaj);   // dP = dO V^T
+        ptx::mma_commit_elect(bar(SF));
+        ok = waitw(bar(DSF), ds_cnt & 1);
+        if (!ok) break;
+        ++ds_cnt;
+        ptx::tc_fence_after();
+        mma_tn<D>(tQ, tS, k_mn, u > 0);   // dQ += dS K
+        ptx::mma_commit_elect(bar(KVE + st));
+        ++kv_cnt;
+        ++u;
+      }
+      if (!ok) break;
+      ptx::mma_commit_elect(bar(DQF));
+      ptx::mma_commit_elect(bar(QE));
+      ++act;
+    }
+    // every MMA done before Tensor Memory is freed
+    __syncwarp();
+    ptx::mma_commit_elect(bar(DRAIN));
+    const uint64_t t0 = ptx::globaltimer_ns();
+    bool drained = true;
+    while (!ptx::mbar_try_wait(bar(DRAIN), 0)) {
+      if (ptx::globaltimer_ns() - t0 > p.budget_ns) {
+        drained = false;
+        break;
+      }
+    }
+    if (!__all_sync(0xffffffffu, drained) && lane == 0) breport(ctl, ATTN_ERR_TIMEOUT, kBSiteDrain, 0);
+  } else if (warp < 4) {
+    // ===================== elementwise: one thread per query row =========
+    const int row = warp * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t tS = lane_base, tP = lane_base + 128u, tQ = lane_base + 256u;
+    uint32_t s_cnt = 0;
+    int act = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int w = bitem_of(r);
+      if (w >= p.n_items) break;
+      const It it = item(w);
+      const int i = it.qt * kTileM + row;
+      const bool valid = i < p.S_q;
+      const size_t bh = (size_t)it.b * p.H + it.h;
+      __nv_bfloat16* dqrow = p.dq + (bh * p.S_q + (size_t)i) * D;
+      if (nonempty(it) == 0) {
+        if (valid) {
+          const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(dqrow)[c] = z;
+        }
+        continue;
+      }
+      const size_t si = bh * (size_t)p.nQ * kTileM + (size_t)it.qt * kTileM + row;
+      const float lse2 = p.lse2[si];
+      const float dlt = p.delta[si];
+      int lo, hi;
+      row_keys(p, it.b, i, docs_sorted != 0, lo, hi);
+      const bool has_doc = (p.mask_flags & ATTN_MASK_DOCUMENT) != 0 && !docs_sorted;
+      const int* doc_b = has_doc ? p.doc_ids + (size_t)it.b * p.S_k : nullptr;
+      const int doc_i = (has_doc && valid) ? doc_b[i] : 0;
+      const ScoreMod md = make_mod<ALIBI, SOFTCAP>(p, it.h);
+      const int qpos = i + p.q_offset;
+      for (int j = 0; j < it.n && ok; ++j) {
+        const uint32_t cls = entry_cls(it.lst[j], it.t);
+        if (cls == kEmpty) continue;
+        const int j0 = (int)entry_tile(it.lst[j]) * kTileN;
+        {
+          const bool got = bwait(bar(SF), s_cnt & 1, ctl, kBSiteElem);
+          ok = __all_sync(0xffffffffu, got);
+          if (!ok) break;
+        }
+        ++s_cnt;
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t ra[32], rb[32], pa[32], pb[32];
+          ptx::tmem_ld32(tS + (uint32_t)(64 * hh), ra);
+          ptx::tmem_ld32(tS + (uint32_t)(64 * hh + 32), rb);
+          ptx::tmem_ld32(tP + (uint32_t)(64 * hh), pa);
+          ptx::tmem_ld32(tP + (uint32_t)(64 * hh + 32), pb);
+          ptx::tmem_wait_ld();
+          uint32_t pk[32];
+#pragma unroll
+          for (int c2 = 0; c2 < 32; ++c2) {
+            float ds2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int c = 2 * c2 + e;  // column within this half
+              const float s = __uint_as_float(c < 32 ? ra[c] : rb[c - 32]);
+              const float dp = __uint_as_float(c < 32 ? pa[c] : pb[c - 32]);
+              const int jj = j0 + 64 * hh + c;
+              const float tv = score_t<ALIBI, SOFTCAP>(s, (float)(jj - qpos), md);
+              bool vis = true;
+              if (cls == kPartial) {
+                vis = (jj >= lo) & (jj <= hi);
+                if (has_doc) vis = vis && jj < p.S_k && doc_b[jj] == doc_i;
+              }
+              const float pr = vis ? ptx::ex2_approx(tv - lse2) : 0.f;
+              float ds = pr * (dp - dlt);
+              if constexpr (SOFTCAP) {
+                const float u = tv / md.capl2;
+                ds *= 1.0f - u * u;
+              }
+              ds2[e] = ds;
+            }
+            pk[c2] = ptx::pack_bf16x2(ds2[0], ds2[1]);
+          }
+          ptx::tmem_st32(tS + (uint32_t)(32 * hh), pk);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(DSF));
+      }
+      if (!ok) break;
+      {
+        const bool got = bwait(bar(DQF), act & 1, ctl, kBSiteElem);
+        ok = __all_sync(0xffffffffu, got);
+        if (!ok) break;
+      }
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int c4 = 0; c4 < D / 32; ++c4) {
+        uint32_t o[32];
+        ptx::tmem_ld32(tQ + (uint32_t)(c4 * 32), o);
+        ptx::tmem_wait_ld();
+        if (valid) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            pk[c] = ptx::pack_bf16x2(__uint_as_float(o[2 * c]) * p.scale,
+                                     __uint_as_float(o[2 * c + 1]) * p.scale);
+          uint4* dst = reinterpret_cast<uint4*>(dqrow + c4 * 32);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(DQE));
+      ++act;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kBMmaWarp) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kBTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- dK dV ---
+template <int D, bool ALIBI, bool SOFTCAP>
+__global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_constant__ BParams p) {
+  using C = BCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_addr(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  ptx::griddep_wait();
+  const int docs_sorted = p.hdr->docs_sorted;
+
+  auto bar = [&](int i) { return sbase + (uint32_t)(C::kKvBar + 8 * i); };
+  enum { KF = 0, KE = 1, QF = 2, QE = 4, SF = 6, PF = 7, AF = 8, AE = 9, DRAIN = 10 };
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kKvBar + 8 * C::kNumBars);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kKvBar + 8 * C::kNumBars + 4);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar(KF), 1);
+    ptx::mbar_init(bar(KE), 1);
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(bar(QF + s), 1);
+      ptx::mbar_init(bar(QE + s), 1);
+    }
+    ptx::mbar_init(bar(SF), 1);
+    ptx::mbar_init(bar(PF), 4);
+    ptx::mbar_init(bar(AF), 1);
+    ptx::mbar_init(bar(AE), 4);
+    ptx::mbar_init(bar(DRAIN), 1);
+    *s_abort = 0;
+    ptx::fence_mbar_init();
+  }
+  if (warp == kBMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_addr(s_tmem), kBTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const BCtl ctl{s_abort, sbase + (uint32_t)(C::kKvBar + 8 * C::kNumBars + 4), p.status,
+                 p.budget_ns};
+
+  // Item w -> (b, K/V head, key tile); its work units are (query head of the
+  // group, query tile of the transposed list).
+  struct It {
+    int b, hk, kt, n;
+    const uint32_t* lst;
+  };
+  auto item = [&](int w) {
+    It it;
+    it.kt = w % p.nK;
+    const int bh = w / p.nK;
+    it.b = bh / p.H_kv;
+    it.hk = bh % p.H_kv;
+    const int e = (p.bm == 1 ? 0 : it.b) * p.nK + it.kt;
+    it.n = p.cnt_t[e];
+    it.lst = p.list_t + (size_t)e * p.nQ;
+    return it;
+  };
+  auto stage_addr = [&](int st) { return sbase + (uint32_t)(C::kKvStage0 + st * C::kKvStageBytes); };
+
+  if (warp == kBLoadWarp) {
+    if (lane == 0) {
+      ptx::prefetch_tmap(&p.tmap_q);
+      ptx::prefetch_tmap(&p.tmap_do);
+      ptx::prefetch_tmap(&p.tmap_k);
+      ptx::prefetch_tmap(&p.tmap_v);
+      const uint64_t pol = ptx::policy_evict_last();
+      uint32_t q_cnt = 0, k_issued = 0;
+      int act = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int w = bitem_of(r);
+        if (w >= p.n_items) break;
+        const It it = item(w);
+        if (it.n == 0) continue;
+        if (act > 0) ok = bwait(bar(KE), (act - 1) & 1, ctl, kBSiteLoad);
+        if (!ok) break;
+        const int kvz = it.b * p.H_kv + it.hk;
+        ptx::mbar_arrive_expect_tx(bar(KF), 2 * C::kTileBytes);
+        k_issued = act + 1;
+        for (int hx = 0; hx < C::kHalves; ++hx) {
+          ptx::tma_load_3d(sbase + C::kKvK + hx * C::kHalfBytes, &p.tmap_k, bar(KF), hx * 64,
+                           it.kt * kTileN, kvz, pol);
+          ptx::tma_load_3d(sbase + C::kKvV + hx * C::kHalfBytes, &p.tmap_v, bar(KF), hx * 64,
+                           it.kt * kTileN, kvz, pol);
+        }
+        for (int g = 0; g < p.group && ok; ++g) {
+          const int h = it.hk * p.group + g;
+          const size_t bh = (size_t)it.b * p.H + h;
+          for (int u = 0; u < it.n && ok; ++u) {
+            const int qt = (int)entry_tile(it.lst[u]);
+            const int st = (int)(q_cnt & 1);
+            if (q_cnt >= 2) ok = bwait(bar(QE + st), ((q_cnt >> 1) - 1) & 1, ctl, kBSiteLoad);
+            if (!ok) break;
+            const uint32_t dst = stage_addr(st);
+            ptx::mbar_arrive_expect_tx(bar(QF + st), 2 * C::kTileBytes + 2 * kTileM * 4);
+            for (int hx = 0; hx < C::kHalves; ++hx) {
+              ptx::tma_load_3d(dst + hx * C::kHalfBytes, &p.tmap_q, bar(QF + st), hx * 64,
+                               qt * kTileM, (int)bh, pol);
+              ptx::tma_load_3d(dst + C::kTileBytes + hx * C::kHalfBytes, &p.tmap_do, bar(QF + st),
+                               hx * 64, qt * kTileM, (int)bh, pol);
+            }
+            const size_t so = bh * (size_t)p.nQ * kTileM + (size_t)qt * kTileM;
+            ptx::bulk_load(dst + 2 * C::kTileBytes, p.lse2 + so, kTileM * 4, bar(QF + st));
+            ptx::bulk_load(dst + 2 * C::kTileBytes + kTileM * 4, p.delta + so, kTileM * 4,
+                           bar(QF + st));
+            ++q_cnt;
+          }
+        }
+        ++act;
+      }
+      if (!ok) {
+        drain_loads(bar(KF), 1, k_issued, p.budget_ns);
+        drain_loads(bar(QF), 2, q_cnt, p.budget_ns);
+      }
+    }
+  } else if (warp == kBMmaWarp) {
+    const uint32_t tST = tmem, tDPT = tmem + 128u, tDV = tmem + 256u, tDK = tmem + 256u + D;
+    const uint64_t k_kmaj = BDesc<D>::kKMajor + ((sbase + C::kKvK) >> 4);
+    const uint64_t v_kmaj = BDesc<D>::kKMajor + ((sbase + C::kKvV) >> 4);
+    auto waitw = [&](uint32_t b, uint32_t par) {
+      return __all_sync(0xffffffffu, bwait(b, par, ctl, kBSiteMma));
+    };
+    uint32_t q_cnt = 0, p_cnt = 0;
+    int act = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int w = bitem_of(r);
+      if (w >= p.n_items) break;
+      const It it = item(w);
+      if (it.n == 0) continue;
+      ok = waitw(bar(KF), act & 1);
+      if (ok && act > 0) ok = waitw(bar(AE), (act - 1) & 1);
+      if (!ok) break;
+      const int units = p.group * it.n;
+      for (int u = 0; u < units && ok; ++u) {
+        const int st = (int)(q_cnt & 1);
+        ok = waitw(bar(QF + st), (q_cnt >> 1) & 1);
+        if (!ok) break;
+        ptx::tc_fence_after();
+        const uint32_t qaddr = stage_addr(st);
+        const uint64_t q_kmaj = BDesc<D>::kKMajor + (qaddr >> 4);
+        const uint64_t do_kmaj = BDesc<D>::kKMajor + ((qaddr + C::kTileBytes) >> 4);
+        const uint64_t q_mn = BDesc<D>::kMNMajor + (qaddr >> 4);
+        const uint64_t do_mn = BDesc<D>::kMNMajor + ((qaddr + C::kTileBytes) >> 4);
+        mma_nt<D>(tST, k_kmaj, q_kmaj);    // S^T = K Q^T
+        mma_nt<D>(tDPT, v_kmaj, do_kmaj);  // dP^T = V dO^T
+        ptx::mma_commit_elect(bar(SF));
+        ok = waitw(bar(PF), p_cnt & 1);
+        if (!ok) break;
+        ++p_cnt;
+        ptx::tc_fence_after();
+        mma_tn<D>(tDV, tST, do_mn, u > 0);   // dV += P^T dO
+        mma_tn<D>(tDK, tDPT, q_mn, u > 0);   // dK += dS^T Q
+        ptx::mma_commit_elect(bar(QE + st));
+        ++q_cnt;
+      }
+      if (!ok) break;
+      ptx::mma_commit_elect(bar(AF));
+      ptx::mma_commit_elect(bar(KE));
+      ++act;
+    }
+    __syncwarp();
+    ptx::mma_commit_elect(bar(DRAIN));
+    const uint64_t t0 = ptx::globaltimer_ns();
+    bool drained = true;
+    while (!ptx::mbar_try_wait(bar(DRAIN), 0)) {
+      if (ptx::globaltimer_ns() - t0 > p.budget_ns) {
+        drained = false;
+        break;
+      }
+    }
+    if (!__all_sync(0xffffffffu, drained) && lane == 0) breport(ctl, ATTN_ERR_TIMEOUT, kBSiteDrain, 0);
+  } else if (warp < 4) {
+    // ===================== elementwise: one thread per key ================
+    const int row = warp * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t tST = lane_base, tDPT = lane_base + 128u, tDV = lane_base + 256u,
+                   tDK = lane_base + 256u + D;
+    uint32_t q_cnt = 0;
+    int act = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int w = bitem_of(r);
+      if (w >= p.n_items) break;
+      const It it = item(w);
+      const int j = it.kt * kTileN + row;  // this thread's key
+      const bool valid = j < p.S_k;
+      const size_t kvh = (size_t)it.b * p.H_kv + it.hk;
+      __nv_bfloat16* dkrow = p.dk + (kvh * p.S_k + (size_t)j) * D;
+      __nv_bfloat16* dvrow = p.dv + (kvh * p.S_k + (size_t)j) * D;
+      if (it.n == 0) {
+        if (valid) {
+          const uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c) {
+            reinterpret_cast<uint4*>(dkrow)[c] = z;
+            reinterpret_cast<uint4*>(dvrow)[c] = z;
+          }
+        }
+        continue;
+      }
+      int ilo, ihi;
+      key_rows(p, it.b, j, docs_sorted != 0, ilo, ihi);
+      const bool has_doc = (p.mask_flags & ATTN_MASK_DOCUMENT) != 0 && !docs_sorted;
+      const int* doc_b = has_doc ? p.doc_ids + (size_t)it.b * p.S_k : nullptr;
+      const int doc_j = (has_doc && valid) ? doc_b[j] : 0;
+      for (int g = 0; g < p.group && ok; ++g) {
+        const int h = it.hk * p.group + g;
+        const ScoreMod md = make_mod<ALIBI, SOFTCAP>(p, h);
+        for (int u = 0; u < it.n && ok; ++u) {
+          const uint32_t cls = entry_cls(it.lst[u], 0);
+          const int i0 = (int)entry_tile(it.lst[u]) * kTileM;
+          const int st = (int)(q_cnt & 1);
+          {
+            const bool got = bwait(bar(SF), q_cnt & 1, ctl, kBSiteElem);
+            ok = __all_sync(0xffffffffu, got);
+            if (!ok) break;
+          }
+          ptx::tc_fence_after();
+          const float* s_lse2 = reinterpret_cast<const float*>(smem + C::kKvStage0 +
+                                                               st * C::kKvStageBytes +
+                                                               2 * C::kTileBytes);
+          const float* s_delta = s_lse2 + kTileM;
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t ra[32], rb[32], pa[32], pb[32];
+            ptx::tmem_ld32(tST + (uint32_t)(64 * hh), ra);
+            ptx::tmem_ld32(tST + (uint32_t)(64 * hh + 32), rb);
+            ptx::tmem_ld32(tDPT + (uint32_t)(64 * hh), pa);
+            ptx::tmem_ld32(tDPT + (uint32_t)(64 * hh + 32), pb);
+            ptx::tmem_wait_ld();
+            uint32_t pp[32], pd[32];
+#pragma unroll
+            for (int c2 = 0; c2 < 32; ++c2) {
+              float pr2[2], ds2[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int c = 2 * c2 + e;  // query column within this half
+                const int qi = i0 + 64 * hh + c;
+                const float s = __uint_as_float(c < 32 ? ra[c] : rb[c - 32]);
+                const float dp = __uint_as_float(c < 32 ? pa[c] : pb[c - 32]);
+                const float tv = score_t<ALIBI, SOFTCAP>(s, (float)(j - (qi + p.q_offset)), md);
+                bool vis = valid;
+                if (cls == kPartial) {
+                  vis = vis && (qi >= ilo) & (qi <= ihi);
+                  if (has_doc) vis = vis && qi < p.S_q && doc_b[qi] == doc_j;
+                }
+                const float pr = vis ? ptx::ex2_approx(tv - s_lse2[64 * hh + c]) : 0.f;
+                float ds = pr * (dp - s_delta[64 * hh + c]);
+                if constexpr (SOFTCAP) {
+                  const float uu = tv / md.capl2;
+                  ds *= 1.0f - uu * uu;
+                }
+                pr2[e] = pr;
+                ds2[e] = ds;
+              }
+              pp[c2] = ptx::pack_bf16x2(pr2[0], pr2[1]);
+              pd[c2] = ptx::pack_bf16x2(ds2[0], ds2[1]);
+            }
+            ptx::tmem_st32(tST + (uint32_t)(32 * hh), pp);
+            ptx::tmem_st32(tDPT + (uint32_t)(32 * hh), pd);
+          }
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bar(PF));
+          ++q_cnt;
+        }
+      }
+      if (!ok) break;
+      {
+        const bool got = bwait(bar(AF), act & 1, ctl, kBSiteElem);
+        ok = __all_sync(0xffffffffu, got);
+        if (!ok) break;
+      }
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int c4 = 0; c4 < D / 32; ++c4) {
+        uint32_t ov[32], ok32[32];
+        ptx::tmem_ld32(tDV + (uint32_t)(c4 * 32), ov);
+        ptx::tmem_ld32(tDK + (uint32_t)(c4 * 32), ok32);
+        ptx::tmem_wait_ld();
+        if (valid) {
+          uint32_t pv[16], pkk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            pv[c] = ptx::pack_bf16x2(__uint_as_float(ov[2 * c]), __uint_as_float(ov[2 * c + 1]));
+            pkk[c] = ptx::pack_bf16x2(__uint_as_float(ok32[2 * c]) * p.scale,
+                                      __uint_as_float(ok32[2 * c + 1]) * p.scale);
+          }
+          uint4* dv4 = reinterpret_cast<uint4*>(dvrow + c4 * 32);
+          uint4* dk4 = reinterpret_cast<uint4*>(dkrow + c4 * 32);
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            dv4[c] = make_uint4(pv[4 * c], pv[4 * c + 1], pv[4 * c + 2], pv[4 * c + 3]);
+            dk4[c] = make_uint4(pkk[4 * c], pkk[4 * c + 1], pkk[4 * c + 2], pkk[4 * c + 3]);
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(AE));
+      ++act;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kBMmaWarp) {
+    __syncwarp();
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kBTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- host ----
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn bget_encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// [outer][S][D] bf16 as 3-D (D, S, outer); box 64 x 128 x 1, 128-byte
+// swizzle; rows beyond S read as zero.
+bool bmake_map(CUtensorMap* map, const void* ptr, int D, int S, int outer) {
+  EncodeTiledFn enc = bget_encode_tiled();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)outer};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * (cuuint64_t)D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)kTileM, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <typename K>
+cudaError_t launch_ex(K kern, int grid, int smem, cudaStream_t stream, const BParams& bp) {
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kBThreads, 1, 1);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, bp);
+}
+
+template <int D, bool ALIBI, bool SOFTCAP>
+cudaError_t launch_bwd_variant(BParams bp, int sms, cudaStream_t s) {
+  using C = BCfg<D>;
+  bp.n_items = bp.B * bp.H * bp.nQ;
+  const int g1 = bp.n_items < sms ? bp.n_items : sms;
+  cudaError_t err =
+      launch_ex(bwd_dq_kernel<D, ALIBI, SOFTCAP>, g1 > 0 ? g1 : 1, C::kSmemAllocDq, s, bp);
+  if (err != cudaSuccess) return err;
+  bp.n_items = bp.B * bp.H_kv * bp.nK;
+  const int g2 = bp.n_items < sms ? bp.n_items : sms;
+  return launch_ex(bwd_dkdv_kernel<D, ALIBI, SOFTCAP>, g2 > 0 ? g2 : 1, C::kSmemAllocKv, s, bp);
+}
+
+template <int D>
+cudaError_t launch_bwd_d(const BParams& bp, bool alibi, bool softcap, int sms, cudaStream_t s) {
+  if (alibi && softcap) return launch_bwd_variant<D, true, true>(bp, sms, s);
+  if (alibi) return launch_bwd_variant<D, true, false>(bp, sms, s);
+  if (softcap) return launch_bwd_variant<D, false, true>(bp, sms, s);
+  return launch_bwd_variant<D, false, false>(bp, sms, s);
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
+  BParams bp;
+  memset(&bp, 0, sizeof(bp));
+  if (!bmake_map(&bp.tmap_q, a.q, a.D, a.S_q, a.B * a.H) ||
+      !bmake_map(&bp.tmap_do, a.dout, a.D, a.S_q, a.B * a.H) ||
+      !bmake_map(&bp.tmap_k, a.k, a.D, a.S_k, a.B * a.H_kv) ||
+      !bmake_map(&bp.tmap_v, a.v, a.D, a.S_k, a.B * a.H_kv))
+    return cudaErrorInvalidValue;
+  const BlockMaskGeom g = block_mask_geom(a.B, a.S_q, a.S_k, a.mask.flags);
+  const BlockMaskTGeom gt = block_mask_t_geom(a.B, a.S_q, a.S_k, a.mask.flags);
+  bp.dq = reinterpret_cast<__nv_bfloat16*>(a.dq);
+  bp.dk = reinterpret_cast<__nv_bfloat16*>(a.dk);
+  bp.dv = reinterpret_cast<__nv_bfloat16*>(a.dv);
+  const size_t padded = (size_t)a.B * a.H * (size_t)g.nQ * kTileM;
+  bp.lse2 = a.rowstat;
+  bp.delta = a.rowstat + padded;
+  bp.B = a.B;
+  bp.H = a.H;
+  bp.H_kv = a.H_kv;
+  bp.S_q = a.S_q;
+  bp.S_k = a.S_k;
+  bp.group = a.H / a.H_kv;
+  bp.nQ = g.nQ;
+  bp.nK = g.nK;
+  bp.nP = g.nP;
+  bp.bm = g.bm;
+  bp.scale = a.scale;
+  bp.scale_log2 = a.scale * kBLog2e;
+  bp.softcap = (a.score_flags & ATTN_SCORE_SOFTCAP) ? a.softcap : 0.f;
+  bp.mask_flags = a.mask.flags;
+  bp.window = a.mask.window;
+  bp.q_offset = a.mask.q_offset;
+  bp.doc_ids = a.mask.doc_ids;
+  bp.prefix_len = a.mask.prefix_len;
+  bp.alibi_slopes = a.alibi_slopes;
+  const char* base = reinterpret_cast<const char*>(a.block_mask);
+  bp.hdr = reinterpret_cast<const BlockMaskHeader*>(base);
+  bp.cnt = reinterpret_cast<const int32_t*>(base + g.cnt_off);
+  bp.list = reinterpret_cast<const uint32_t*>(base + g.list_off);
+  if (g.doc_off != 0) {
+    bp.doc_lo = reinterpret_cast<const int32_t*>(base + g.doc_off);
+    bp.doc_hi = bp.doc_lo + (size_t)g.bm * a.S_k;
+  }
+  const char* tb = reinterpret_cast<const char*>(a.block_mask_t);
+  bp.cnt_t = reinterpret_cast<const int32_t*>(tb);
+  bp.list_t = reinterpret_cast<const uint32_t*>(tb + gt.list_off);
+  bp.status = a.status;
+  const double ms = a.wait_budget_ms > 0 ? a.wait_budget_ms : 2000.0;
+  bp.budget_ns = (uint64_t)(ms * 1e6);
+
+  // row statistics, then the two gradient kernels
+  const int BH = a.B * a.H;
+  const long long rows = (long long)padded;
+  const unsigned blocks = (unsigned)((rows + 7) / 8);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const __nv_bfloat16* o = reinterpret_cast<const __nv_bfloat16*>(a.out);
+  const __nv_bfloat16* dout = reinterpret_cast<const __nv_bfloat16*>(a.dout);
+  cudaError_t err = (a.D == 64)
+                        ? cudaLaunchKernelEx(&cfg, bwd_prep_kernel<64>, o, dout, a.lse, a.rowstat,
+                                             a.rowstat + padded, BH, a.S_q, g.nQ)
+                        : cudaLaunchKernelEx(&cfg, bwd_prep_kernel<128>, o, dout, a.lse,
+                                             a.rowstat, a.rowstat + padded, BH, a.S_q, g.nQ);
+  if (err != cudaSuccess) return err;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return cudaErrorUnknown;
+  const bool alibi = (a.score_flags & ATTN_SCORE_ALIBI) != 0;
+  const bool softcap = (a.score_flags & ATTN_SCORE_SOFTCAP) != 0;
+  if (a.D == 64) return launch_bwd_d<64>(bp, alibi, softcap, sms, stream);
+  return launch_bwd_d<128>(bp, alibi, softcap, sms, stream);
+}
+
+}  // namespace attn

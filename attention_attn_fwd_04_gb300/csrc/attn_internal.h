@@ -96,6 +96,25 @@ inline BlockMaskGeom block_mask_geom(int B, int S_q, int S_k, uint32_t mask_flag
   return g;
 }
 
+// Transposed block mask for the key-side backward: for every (mask batch,
+// key tile) the non-empty query tiles in ascending order, each entry the
+// query tile index in bits 0..23 and its class in bits 24..25.
+// Layout: int32 cnt[bm * nK], then uint32 list[bm * nK][nQ].
+struct BlockMaskTGeom {
+  int nQ, nK, bm, n_entries;
+  size_t list_off, total;
+};
+inline BlockMaskTGeom block_mask_t_geom(int B, int S_q, int S_k, uint32_t mask_flags) {
+  BlockMaskTGeom g;
+  g.nQ = (S_q + kTileM - 1) / kTileM;
+  g.nK = (S_k + kTileN - 1) / kTileN;
+  g.bm = (mask_flags & (ATTN_MASK_DOCUMENT | ATTN_MASK_PREFIX_LM)) ? B : 1;
+  g.n_entries = g.bm * g.nK;
+  g.list_off = align_up(sizeof(int32_t) * (size_t)g.n_entries, 16);
+  g.total = align_up(g.list_off + sizeof(uint32_t) * (size_t)g.n_entries * (size_t)g.nQ, 16);
+  return g;
+}
+
 // Mask parameters as the kernels see them.
 struct MaskParams {
   uint32_t flags;
@@ -117,6 +136,12 @@ struct DeviceStatus {
 // Launchers (defined in the .cu files, called by the host API).
 cudaError_t launch_build_block_mask(int B, int S_q, int S_k, const MaskParams& mp,
                                     int force_partial, void* dst, cudaStream_t stream);
+
+// Builds the transposed block mask into dst_t from the block mask fwd_mask
+// already built (on the same stream) for the same problem.
+cudaError_t launch_build_block_mask_t(int B, int S_q, int S_k, const MaskParams& mp,
+                                      int force_partial, const void* fwd_mask, void* dst_t,
+                                      cudaStream_t stream);
 
 struct FwdArgs {
   const void* q;
@@ -143,6 +168,39 @@ struct FwdArgs {
 };
 
 cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream);
+
+// Backward: dQ, dK, dV from Q, K, V, O, LSE and dO (all device pointers).
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* out;
+  const float* lse;
+  const void* dout;
+  void* dq;
+  void* dk;
+  void* dv;
+  int B, H, H_kv, S_q, S_k, D;
+  float scale;
+  MaskParams mask;
+  uint32_t score_flags;
+  float softcap;
+  const float* alibi_slopes;
+  const void* block_mask;    // forward block mask, built for this call
+  const void* block_mask_t;  // transposed block mask, built for this call
+  float* rowstat;            // scratch: [2][B*H][nQ*128] (LSE in log2 units, dO . O)
+  DeviceStatus* status;
+  double wait_budget_ms;
+  int force_partial;
+};
+
+// Bytes of the row-statistics scratch of a backward.
+inline size_t bwd_rowstat_bytes(int B, int H, int S_q) {
+  const size_t nQ = (size_t)((S_q + kTileM - 1) / kTileM);
+  return 2 * sizeof(float) * (size_t)B * (size_t)H * nQ * kTileM;
+}
+
+cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream);
 
 // dst[h] = the default ALiBi slope of head h of H, bit for bit the value the
 // forward kernel computes when it is given no slopes.

@@ -164,6 +164,60 @@ __global__ void __launch_bounds__(kClassifyThreads) classify_kernel(BlockMaskHea
   if (threadIdx.x == 0) cnt[e] = total;
 }
 
+// One block per (mask batch, key tile) of the transposed mask: the query
+// tiles that see some key of the tile, ascending, with their classes (the
+// same classifier as the forward's mask, so the two always agree).
+__global__ void __launch_bounds__(kClassifyThreads) classify_t_kernel(char* dst_t,
+                                                                       const char* fwd_mask,
+                                                                       MaskParams mp,
+                                                                       BlockMaskGeom g,
+                                                                       BlockMaskTGeom gt,
+                                                                       int force_partial) {
+  constexpr int kWarps = kClassifyThreads / 32;
+  const int e = blockIdx.x;
+  const int bb = e / gt.nK, kt = e % gt.nK;
+  int32_t* cnt = reinterpret_cast<int32_t*>(dst_t);
+  uint32_t* list = reinterpret_cast<uint32_t*>(dst_t + gt.list_off) + (size_t)e * gt.nQ;
+  ptx::griddep_wait();
+  ptx::griddep_launch_dependents();
+  __shared__ int s_warp_cnt[kWarps];
+  const bool docs = (mp.flags & ATTN_MASK_DOCUMENT) != 0;
+  const int32_t* t_lo =
+      docs ? reinterpret_cast<const int32_t*>(fwd_mask + g.tile_off) + (size_t)bb * g.nK : nullptr;
+  const int32_t* t_hi = docs ? t_lo + (size_t)g.bm * g.nK : nullptr;
+  const long long pl = (mp.flags & ATTN_MASK_PREFIX_LM) ? mp.prefix_len[bb] : 0;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c0 = kt * kTileN;
+  const Range dk = docs ? Range{t_lo[kt], t_hi[kt]} : Range{0, 0};
+  int total = 0;
+  for (int chunk = 0; chunk < gt.nQ; chunk += kClassifyThreads) {
+    const int qt = chunk + threadIdx.x;
+    uint32_t entry = 0;
+    bool keep = false;
+    if (qt < gt.nQ) {
+      const int r0 = qt * kTileM, r1 = min(r0 + kTileM - 1, mp.S_q - 1);
+      const Range dq = docs ? Range{t_lo[qt], t_hi[qt]} : Range{0, 0};
+      uint32_t c = classify_tile(r0, r1, c0, pl, mp, dq, dk);
+      if (force_partial && c == kFull) c = kPartial;
+      keep = c != kEmpty;
+      entry = (uint32_t)qt | (c << 24);
+    }
+    const unsigned ball = __ballot_sync(0xffffffffu, keep);
+    if (lane == 0) s_warp_cnt[warp] = __popc(ball);
+    __syncthreads();
+    int before = 0, chunk_total = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      if (w < warp) before += s_warp_cnt[w];
+      chunk_total += s_warp_cnt[w];
+    }
+    before += __popc(ball & ((1u << lane) - 1u));
+    if (keep) list[total + before] = entry;
+    total += chunk_total;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) cnt[e] = total;
+}
+
 // First position pos in [lo, hi) with row[pos] > v (strict) or row[pos] >= v,
 // for ids that are non-decreasing on [lo, hi); hi when there is none.  The
 // warp probes 32 evenly spaced positions per step, so a step shrinks the
@@ -372,6 +426,16 @@ cudaError_t launch_build_block_mask(int B, int S_q, int S_k, const MaskParams& m
   if (err != cudaSuccess) return err;
   const int blocks = (g.n_entries + kBuildThreads - 1) / kBuildThreads;
   return launch_pdl(order_kernel, dim3((unsigned)blocks), kBuildThreads, stream, hdr, B, mp, g,
+                    force_partial);
+}
+
+cudaError_t launch_build_block_mask_t(int B, int S_q, int S_k, const MaskParams& mp,
+                                      int force_partial, const void* fwd_mask, void* dst_t,
+                                      cudaStream_t stream) {
+  const BlockMaskGeom g = block_mask_geom(B, S_q, S_k, mp.flags);
+  const BlockMaskTGeom gt = block_mask_t_geom(B, S_q, S_k, mp.flags);
+  return launch_pdl(classify_t_kernel, dim3((unsigned)gt.n_entries), kClassifyThreads, stream,
+                    static_cast<char*>(dst_t), static_cast<const char*>(fwd_mask), mp, g, gt,
                     force_partial);
 }
 

@@ -281,6 +281,38 @@ attn_status attn_fwd_host(const void *q, const void *k, const void *v,
                           int S_q, int S_k, int D, float scale,
                           const attn_mod_desc *mod, attn_stream_t stream);
 
+/*
+ * attn_bwd -- gradients of attn_fwd: dQ, dK and dV for a given dO.
+ *
+ * Defined by the forward's definition and the chain rule; "FlashAttention-4
+ * explained", section "FlashAttention-4: Built for Blackwell", names the
+ * backward pass as the step after the forward and prints no formula:
+ *   P = softmax of the modified, masked scores (recomputed from the forward's
+ *   LSE), dP = dO V^T, dS = P * (dP - rowsum(dO * O)) * (derivative of the
+ *   score mod), dQ = scale * dS K, dK = scale * dS^T Q, dV = P^T dO; dK and dV
+ *   of a K/V head sum over the query heads that share it.
+ *
+ *  q, k, v, out, lse   the forward's inputs and outputs (out and lse exactly
+ *                      as attn_fwd wrote them for these q, k, v, scale, mod)
+ *  dout                device, bf16 [B][H][S_q][D], the gradient of out
+ *  dq                  device, bf16 [B][H][S_q][D]
+ *  dk, dv              device, bf16 [B][H_kv][S_k][D]
+ *  others              as attn_fwd; mod->block_mask must be NULL (the masks
+ *                      are rebuilt, forward and transposed, into a
+ *                      library-owned per-device buffer)
+ *
+ * All tensors 16-byte aligned (lse 4-byte), outputs overlapping nothing.
+ * Deterministic: no atomics, every output row is written once.  Errors as
+ * for attn_fwd; device-side failures are read with attn_get_device_status.
+ * Calls that share the library's buffer must not run concurrently on
+ * different streams of one device.
+ */
+attn_status attn_bwd(const void *q, const void *k, const void *v,
+                     const void *out, const float *lse, const void *dout,
+                     void *dq, void *dk, void *dv, int B, int H, int H_kv,
+                     int S_q, int S_k, int D, float scale,
+                     const attn_mod_desc *mod, attn_stream_t stream);
+
 /* Tuning options.  Process-wide; set them before enqueuing work. */
 typedef enum attn_option {
     /* Rescale O only when the running row max grows by more than this many

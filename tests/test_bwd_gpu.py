@@ -1,0 +1,125 @@
+"""Backward (attn_bwd) against the fp64 oracle's gradients.
+
+dQ, dK and dV are compared element by element with the oracle on every row
+and key of small problems that span several tiles, ragged tails, every mask
+and score mod, GQA and both head dimensions; and on sampled rows and keys at
+a larger size.  Tolerance (derived in the design notes from the bf16 rounding
+of P and dS fed to the tensor cores and of the stored gradients):
+|delta| <= 1e-2 * max|ref| + 2^-7 * |ref| per tensor.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+DEV = torch.device("cuda:0")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def attn():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    import attention_attn_fwd_04_gb300 as a
+    return a
+
+
+def inputs(B, H, Hkv, Sq, Sk, D, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((B, H, Sq, D), generator=g).to(torch.bfloat16)
+    k = torch.randn((B, Hkv, Sk, D), generator=g).to(torch.bfloat16)
+    v = torch.randn((B, Hkv, Sk, D), generator=g).to(torch.bfloat16)
+    do = torch.randn((B, H, Sq, D), generator=g).to(torch.bfloat16)
+    return q, k, v, do
+
+
+def check(name, got, ref):
+    got = got.float().cpu().numpy().astype(np.float64).reshape(ref.shape)
+    err = np.abs(got - ref)
+    bound = 1e-2 * np.abs(ref).max() + 2.0 ** -7 * np.abs(ref)
+    worst = np.argmax(err - bound)
+    assert np.all(err <= bound), "%s: max err %.3g (ref max %.3g), worst at %s: got %.5g ref %.5g" % (
+        name, err.max(), np.abs(ref).max(), np.unravel_index(worst, ref.shape),
+        got.flat[worst], ref.flat[worst])
+
+
+def run_case(attn, B, H, Hkv, S, D, mods, seed):
+    q, k, v, do = inputs(B, H, Hkv, S, S, D, seed)
+    scale = 1.0 / math.sqrt(D)
+    dmods = {n: (t.to(DEV) if isinstance(t, torch.Tensor) else t) for n, t in mods.items()}
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    o, lse = attn.attn_fwd(qd, kd, vd, scale=scale, **dmods)
+    dq, dk, dv = attn.attn_bwd(qd, kd, vd, o, lse, dod, scale=scale, **dmods)
+    torch.cuda.synchronize()
+    assert attn.get_device_status(device=DEV) == 0
+    omods = dict(mods)
+    if "window" in omods and omods["window"] is None:
+        del omods["window"]
+    ref_dq = oracle.attn_bwd_rows(q, k, v, do, scale=scale, **omods)
+    ref_dk, ref_dv = oracle.attn_bwd_keys(q, k, v, do, scale=scale, **omods)
+    check("dQ", dq, ref_dq)
+    check("dK", dk, ref_dk)
+    check("dV", dv, ref_dv)
+
+
+def packed_docs(B, S, seed):
+    return torch.stack([workloads.doc_ids_for(S, seed=seed + b, lo=40, hi=300)
+                        for b in range(B)]).contiguous()
+
+
+CASES = [
+    (1, 2, 2, 256, 128, {}),
+    (1, 2, 2, 300, 64, {"causal": True}),
+    (2, 4, 2, 384, 128, {"causal": True}),                       # GQA 2:1
+    (1, 4, 1, 260, 64, {}),                                     # GQA 4:1, ragged
+    (1, 2, 2, 640, 128, {"window": 200, "causal": True, "softcap": 30.0}),
+    (1, 2, 2, 520, 64, {"alibi": True, "softcap": 5.0}),
+    (1, 4, 4, 600, 128, {"causal": True, "alibi": True}),
+    (2, 2, 2, 700, 128, {"doc_ids": "packed", "causal": True}),
+    (1, 2, 2, 400, 64, {"doc_ids": "unsorted"}),
+    (2, 2, 2, 500, 128, {"prefix_len": [0, 200]}),
+    (1, 2, 2, 384, 128, {"causal": True, "q_offset": -100}),    # rows with no key
+]
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_backward_small(attn, case):
+    B, H, Hkv, S, D, mods = CASES[case]
+    mods = dict(mods)
+    if mods.get("doc_ids") == "packed":
+        mods["doc_ids"] = packed_docs(B, S, seed=20)
+    elif mods.get("doc_ids") == "unsorted":
+        g = torch.Generator().manual_seed(21)
+        mods["doc_ids"] = torch.randint(0, 3, (B, S), generator=g).to(torch.int32)
+    if "prefix_len" in mods:
+        mods["prefix_len"] = torch.tensor(mods["prefix_len"], dtype=torch.int32)
+    run_case(attn, B, H, Hkv, S, D, mods, seed=300 + case)
+
+
+def test_backward_explicit_slopes(attn):
+    mods = {"causal": True, "alibi_slopes": torch.tensor([0.5, 0.03125], dtype=torch.float32)}
+    run_case(attn, 1, 2, 2, 300, 128, mods, seed=400)
+
+
+def test_backward_sampled_at_size(attn):
+    # causal GQA at S = 2048: sampled rows and keys (all tiles of the schedule run)
+    B, H, Hkv, S, D = 1, 8, 2, 2048, 128
+    q, k, v, do = inputs(B, H, Hkv, S, S, D, seed=500)
+    scale = 1.0 / math.sqrt(D)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    o, lse = attn.attn_fwd(qd, kd, vd, scale=scale, causal=True)
+    dq, dk, dv = attn.attn_bwd(qd, kd, vd, o, lse, dod, scale=scale, causal=True)
+    torch.cuda.synchronize()
+    g = torch.Generator().manual_seed(501)
+    rows = torch.randperm(B * H * S, generator=g)[:256].numpy()
+    keys = torch.randperm(B * Hkv * S, generator=g)[:64].numpy()
+    keys = keys[keys // S < 1]  # one K/V head keeps the oracle's row pass short
+    ref_dq = oracle.attn_bwd_rows(q, k, v, do, scale=scale, rows=rows, causal=True)
+    ref_dk, ref_dv = oracle.attn_bwd_keys(q, k, v, do, scale=scale, keys=keys, causal=True)
+    check("dQ", dq.reshape(-1, D)[torch.from_numpy(rows)], ref_dq)
+    check("dK", dk.reshape(-1, D)[torch.from_numpy(keys)], ref_dk)
+    check("dV", dv.reshape(-1, D)[torch.from_numpy(keys)], ref_dv)
