@@ -11,7 +11,8 @@ forward kernel, through the C ABI, on inputs already resident in HBM.
 Metric: useful TFLOPS = 4 * D * (visible (query, key) pairs) / time, so the
 two GEMMs are counted only on unmasked pairs; softmax work is not counted.
 The headline workload is dense B=4 H=16 S=4096 D=128; the other named
-workloads are reported per mask type under "per_workload".
+workloads are reported per mask type under "per_workload", each with the
+backward's time (attn_bwd) and its TFLOPS at 2.5x the forward's FLOPs.
 
 One JSON line is printed by rank 0.  With N > 1 (torchrun, one process per
 GPU) every rank runs an independent replica of the workload ("scaling":
@@ -256,6 +257,30 @@ def time_workload(attn, w, inp, dev, steps, warmup):
     return total_ms / steps, statistics.mean(kern_ms), statistics.median(kern_ms)
 
 
+def time_backward(attn, w, inp, dev, steps, warmup):
+    """Device time of one attn_bwd call (block masks, row statistics, dQ and
+    dK/dV kernels) on resident inputs, after the forward produced O and LSE."""
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    kw = mods_of(w, inp, dev)
+    o, lse = attn.attn_fwd(q, k, v, scale=w.scale, **kw)
+    g = torch.Generator(device=dev).manual_seed(7)
+    do = torch.randn(o.shape, device=dev, generator=g).to(torch.bfloat16)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        attn.attn_bwd(q, k, v, o, lse, do, scale=w.scale, stream=stream, **kw)
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        attn.attn_bwd(q, k, v, o, lse, do, scale=w.scale, stream=stream, **kw)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    st = attn.get_device_status(device=dev)
+    if st != 0:
+        raise RuntimeError("device status %s" % attn.status_string(st))
+    return start.elapsed_time(end) / steps
+
+
 def time_e2e(attn, w, inp, dev, steps, warmup):
     """Same metric through the public host-memory entry point
     (attn_fwd_host): every step copies Q, K, V (+ mask arrays) in from
@@ -421,9 +446,12 @@ def main():
     per = {}
     if not args.no_per_workload:
         for name, wx in workloads.WORKLOADS.items():
+            bsteps = min(max(3, args.steps // 100), 20)
             if name == w.name:
                 per[name] = {"tflops": value / world, "kernel_tflops": achieved,
                              "ms_per_step": ms_step, "frac": achieved / peak}
+                bms = time_backward(attn, w, inp, dev, bsteps, 3)
+                per[name].update(bwd_ms=bms, bwd_tflops=2.5 * flops / (bms * 1e-3) / 1e12)
                 continue
             ix = workloads.generate(wx)
             px = visible_pairs(wx, ix.get("doc_ids"), ix.get("prefix_len"))
@@ -434,6 +462,10 @@ def main():
                          "ms_per_step": msx, "kernel_ms": kx,
                          "frac": fx / (kx * 1e-3) / 1e12 / peak,
                          "hbm_gbs": algorithmic_bytes(wx) / (kx * 1e-3) / 1e9}
+            # backward: 2.5x the forward's useful FLOPs (dQ, dK, dV and the
+            # recomputed S and dP over the visible pairs, the usual count)
+            bms = time_backward(attn, wx, ix, dev, bsteps, 3)
+            per[name].update(bwd_ms=bms, bwd_tflops=2.5 * fx / (bms * 1e-3) / 1e12)
             del ix
 
     cpu = None
