@@ -530,26 +530,42 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
           ptx::tmem_ld32(tP + (uint32_t)(64 * hh), pa);
           ptx::tmem_ld32(tP + (uint32_t)(64 * hh + 32), pb);
           ptx::tmem_wait_ld();
+          // modified scores of this half, then the mask in a loop of its own
+          // (a branch per element would split the unrolled loop and
+          // serialise the exponentials), then P and dS branch-free
+          const int jh = j0 + 64 * hh;  // first key of this half
+          float tv[64];
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            tv[c] = score_t<ALIBI, SOFTCAP>(__uint_as_float(c < 32 ? ra[c] : rb[c - 32]),
+                                            (float)(jh + c - qpos), md);
+          if (cls == kPartial) {
+            const int clo = lo - jh, chi = hi - jh;
+            if (has_doc) {
+#pragma unroll
+              for (int c = 0; c < 64; ++c) {
+                const int jj = jh + c;
+                const bool vis = (c >= clo) & (c <= chi) & (jj < p.S_k) &&
+                                 doc_b[jj < p.S_k ? jj : 0] == doc_i;
+                tv[c] = vis ? tv[c] : -INFINITY;
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < 64; ++c) tv[c] = ((c >= clo) & (c <= chi)) ? tv[c] : -INFINITY;
+            }
+          }
           uint32_t pk[32];
 #pragma unroll
           for (int c2 = 0; c2 < 32; ++c2) {
             float ds2[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const int c = 2 * c2 + e;  // column within this half
-              const float s = __uint_as_float(c < 32 ? ra[c] : rb[c - 32]);
+              const int c = 2 * c2 + e;
               const float dp = __uint_as_float(c < 32 ? pa[c] : pb[c - 32]);
-              const int jj = j0 + 64 * hh + c;
-              const float tv = score_t<ALIBI, SOFTCAP>(s, (float)(jj - qpos), md);
-              bool vis = true;
-              if (cls == kPartial) {
-                vis = (jj >= lo) & (jj <= hi);
-                if (has_doc) vis = vis && jj < p.S_k && doc_b[jj] == doc_i;
-              }
-              const float pr = vis ? ptx::ex2_approx(tv - lse2) : 0.f;
+              const float pr = ptx::ex2_approx(tv[c] - lse2);
               float ds = pr * (dp - dlt);
-              if constexpr (SOFTCAP) {
-                const float u = tv / md.capl2;
+              if constexpr (SOFTCAP) {  // masked: t = -inf, clamped so the factor is 0
+                const float u = fmaxf(tv[c], -md.capl2) / md.capl2;
                 ds *= 1.0f - u * u;
               }
               ds2[e] = ds;
@@ -836,26 +852,42 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
             ptx::tmem_ld32(tDPT + (uint32_t)(64 * hh), pa);
             ptx::tmem_ld32(tDPT + (uint32_t)(64 * hh + 32), pb);
             ptx::tmem_wait_ld();
+            // scores, then the mask in its own loop, then P and dS
+            // branch-free (as in the dQ kernel)
+            const int ih = i0 + 64 * hh;  // first query of this half
+            float tv[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              tv[c] = score_t<ALIBI, SOFTCAP>(__uint_as_float(c < 32 ? ra[c] : rb[c - 32]),
+                                              (float)(j - (ih + c + p.q_offset)), md);
+            if (!valid || cls == kPartial) {
+              const int clo = ilo - ih, chi = ihi - ih;
+              if (has_doc) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                  const int qi = ih + c;
+                  const bool vis = valid & (c >= clo) & (c <= chi) & (qi < p.S_q) &&
+                                   doc_b[qi < p.S_q ? qi : 0] == doc_j;
+                  tv[c] = vis ? tv[c] : -INFINITY;
+                }
+              } else {
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                  tv[c] = (valid & (c >= clo) & (c <= chi)) ? tv[c] : -INFINITY;
+              }
+            }
             uint32_t pp[32], pd[32];
 #pragma unroll
             for (int c2 = 0; c2 < 32; ++c2) {
               float pr2[2], ds2[2];
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
-                const int c = 2 * c2 + e;  // query column within this half
-                const int qi = i0 + 64 * hh + c;
-                const float s = __uint_as_float(c < 32 ? ra[c] : rb[c - 32]);
+                const int c = 2 * c2 + e;
                 const float dp = __uint_as_float(c < 32 ? pa[c] : pb[c - 32]);
-                const float tv = score_t<ALIBI, SOFTCAP>(s, (float)(j - (qi + p.q_offset)), md);
-                bool vis = valid;
-                if (cls == kPartial) {
-                  vis = vis && (qi >= ilo) & (qi <= ihi);
-                  if (has_doc) vis = vis && qi < p.S_q && doc_b[qi] == doc_j;
-                }
-                const float pr = vis ? ptx::ex2_approx(tv - s_lse2[64 * hh + c]) : 0.f;
+                const float pr = ptx::ex2_approx(tv[c] - s_lse2[64 * hh + c]);
                 float ds = pr * (dp - s_delta[64 * hh + c]);
                 if constexpr (SOFTCAP) {
-                  const float uu = tv / md.capl2;
+                  const float uu = fmaxf(tv[c], -md.capl2) / md.capl2;
                   ds *= 1.0f - uu * uu;
                 }
                 pr2[e] = pr;
