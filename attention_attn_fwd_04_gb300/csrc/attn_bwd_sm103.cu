@@ -317,7 +317,8 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
   const int docs_sorted = p.hdr->docs_sorted;
 
   auto bar = [&](int i) { return sbase + (uint32_t)(C::kDqBar + 8 * i); };
-  enum { QF = 0, QE = 1, KVF = 2, KVE = 4, SF = 6, DSF = 7, DQF = 8, DQE = 9, DRAIN = 10 };
+  enum { QF = 0, QE = 1, KVF = 2, KVE = 4, SF = 6, DSF = 7, DQF = 8, DQE = 9, DRAIN = 10,
+         DPF = 11, SCON = 12 };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kDqBar + 8 * C::kNumBars);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kDqBar + 8 * C::kNumBars + 4);
   if (threadIdx.x == 0) {
@@ -331,6 +332,8 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
     ptx::mbar_init(bar(DSF), 4);
     ptx::mbar_init(bar(DQF), 1);
     ptx::mbar_init(bar(DQE), 4);
+    ptx::mbar_init(bar(DPF), 1);
+    ptx::mbar_init(bar(SCON), 4);
     ptx::mbar_init(bar(DRAIN), 1);
     *s_abort = 0;
     ptx::fence_mbar_init();
@@ -426,7 +429,7 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
     auto waitw = [&](uint32_t b, uint32_t par) {
       return __all_sync(0xffffffffu, bwait(b, par, ctl, kBSiteMma));
     };
-    uint32_t kv_cnt = 0, ds_cnt = 0;
+    uint32_t kv_cnt = 0, ds_cnt = 0, scon_cnt = 0;
     int act = 0;
     bool ok = true;
     for (int r = 0; ok; ++r) {
@@ -437,29 +440,46 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
       ok = waitw(bar(QF), act & 1);
       if (ok && act > 0) ok = waitw(bar(DQE), (act - 1) & 1);
       if (!ok) break;
-      int u = 0;
-      for (int j = 0; j < it.n && ok; ++j) {
-        if (entry_cls(it.lst[j], it.t) == kEmpty) continue;
-        const int st = (int)(kv_cnt & 1);
-        ok = waitw(bar(KVF + st), (kv_cnt >> 1) & 1);
+      // Software pipeline over the item's key tiles u: S(u+1) is issued as
+      // soon as the elementwise warps have read S(u), so their next tile is
+      // ready while dQ(u) and dP(u+1) run.  dS(u) is written over dP(u)'s
+      // columns, which dP(u+1) overwrites only after dQ(u) read them.
+      const int m = nonempty(it);
+      const uint32_t kv0 = kv_cnt;
+      auto kaddr = [&](int u) { return sbase + C::kDqKV + ((kv0 + u) & 1) * 2 * C::kTileBytes; };
+      auto kv_ready = [&](int u) {
+        return waitw(bar(KVF + ((kv0 + u) & 1)), ((kv0 + u) >> 1) & 1);
+      };
+      ok = kv_ready(0);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      mma_nt<D>(tS, q_desc, BDesc<D>::kKMajor + (kaddr(0) >> 4));  // S = Q K^T
+      ptx::mma_commit_elect(bar(SF));
+      mma_nt<D>(tP, do_desc, BDesc<D>::kKMajor + ((kaddr(0) + C::kTileBytes) >> 4));  // dP
+      ptx::mma_commit_elect(bar(DPF));
+      for (int u = 0; u < m && ok; ++u) {
+        ok = waitw(bar(SCON), scon_cnt & 1);
         if (!ok) break;
-        ptx::tc_fence_after();
-        const uint32_t kaddr = sbase + C::kDqKV + st * 2 * C::kTileBytes;
-        const uint64_t k_kmaj = BDesc<D>::kKMajor + (kaddr >> 4);
-        const uint64_t v_kmaj = BDesc<D>::kKMajor + ((kaddr + C::kTileBytes) >> 4);
-        const uint64_t k_mn = BDesc<D>::kMNMajor + (kaddr >> 4);
-        mma_nt<D>(tS, q_desc, k_kmaj);    // S = Q K^T
-        mma_nt<D>(tP, do_desc, v_kmaj);   // dP = dO V^T
-        ptx::mma_commit_elect(bar(SF));
+        ++scon_cnt;
+        if (u + 1 < m) {
+          ok = kv_ready(u + 1);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          mma_nt<D>(tS, q_desc, BDesc<D>::kKMajor + (kaddr(u + 1) >> 4));
+          ptx::mma_commit_elect(bar(SF));
+        }
         ok = waitw(bar(DSF), ds_cnt & 1);
         if (!ok) break;
         ++ds_cnt;
         ptx::tc_fence_after();
-        mma_tn<D>(tQ, tS, k_mn, u > 0);   // dQ += dS K
-        ptx::mma_commit_elect(bar(KVE + st));
-        ++kv_cnt;
-        ++u;
+        mma_tn<D>(tQ, tP, BDesc<D>::kMNMajor + (kaddr(u) >> 4), u > 0);  // dQ += dS K
+        ptx::mma_commit_elect(bar(KVE + ((kv0 + u) & 1)));
+        if (u + 1 < m) {
+          mma_nt<D>(tP, do_desc, BDesc<D>::kKMajor + ((kaddr(u + 1) + C::kTileBytes) >> 4));
+          ptx::mma_commit_elect(bar(DPF));
+        }
       }
+      kv_cnt = kv0 + (uint32_t)m;
       if (!ok) break;
       ptx::mma_commit_elect(bar(DQF));
       ptx::mma_commit_elect(bar(QE));
@@ -522,57 +542,75 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
         }
         ++s_cnt;
         ptx::tc_fence_after();
+        // S of the whole tile into registers, then release it for S(u+1)
+        // modified scores, 64 columns per load (fewer live registers); the
+        // mask then runs in a loop of its own (a branch per element would
+        // split the unrolled loop and serialise the exponentials)
+        float tv[kTileN];
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          uint32_t ra[32], rb[32], pa[32], pb[32];
+          uint32_t ra[32], rb[32];
           ptx::tmem_ld32(tS + (uint32_t)(64 * hh), ra);
           ptx::tmem_ld32(tS + (uint32_t)(64 * hh + 32), rb);
-          ptx::tmem_ld32(tP + (uint32_t)(64 * hh), pa);
-          ptx::tmem_ld32(tP + (uint32_t)(64 * hh + 32), pb);
           ptx::tmem_wait_ld();
-          // modified scores of this half, then the mask in a loop of its own
-          // (a branch per element would split the unrolled loop and
-          // serialise the exponentials), then P and dS branch-free
-          const int jh = j0 + 64 * hh;  // first key of this half
-          float tv[64];
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            tv[c] = score_t<ALIBI, SOFTCAP>(__uint_as_float(c < 32 ? ra[c] : rb[c - 32]),
-                                            (float)(jh + c - qpos), md);
-          if (cls == kPartial) {
-            const int clo = lo - jh, chi = hi - jh;
-            if (has_doc) {
-#pragma unroll
-              for (int c = 0; c < 64; ++c) {
-                const int jj = jh + c;
-                const bool vis = (c >= clo) & (c <= chi) & (jj < p.S_k) &&
-                                 doc_b[jj < p.S_k ? jj : 0] == doc_i;
-                tv[c] = vis ? tv[c] : -INFINITY;
-              }
-            } else {
-#pragma unroll
-              for (int c = 0; c < 64; ++c) tv[c] = ((c >= clo) & (c <= chi)) ? tv[c] : -INFINITY;
-            }
+          if (hh == 1) {  // all of S is in registers: release it for S(u+1)
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(SCON));
           }
-          uint32_t pk[32];
 #pragma unroll
-          for (int c2 = 0; c2 < 32; ++c2) {
-            float ds2[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int c = 2 * c2 + e;
-              const float dp = __uint_as_float(c < 32 ? pa[c] : pb[c - 32]);
-              const float pr = ptx::ex2_approx(tv[c] - lse2);
-              float ds = pr * (dp - dlt);
-              if constexpr (SOFTCAP) {  // masked: t = -inf, clamped so the factor is 0
-                const float u = fmaxf(tv[c], -md.capl2) / md.capl2;
-                ds *= 1.0f - u * u;
-              }
-              ds2[e] = ds;
-            }
-            pk[c2] = ptx::pack_bf16x2(ds2[0], ds2[1]);
+          for (int c = 0; c < 32; ++c) {
+            const int c0 = 64 * hh + c;
+            tv[c0] = score_t<ALIBI, SOFTCAP>(__uint_as_float(ra[c]), (float)(j0 + c0 - qpos), md);
+            tv[c0 + 32] =
+                score_t<ALIBI, SOFTCAP>(__uint_as_float(rb[c]), (float)(j0 + c0 + 32 - qpos), md);
           }
-          ptx::tmem_st32(tS + (uint32_t)(32 * hh), pk);
+        }
+        if (cls == kPartial) {
+          const int clo = lo - j0, chi = hi - j0;
+          if (has_doc) {
+#pragma unroll
+            for (int c = 0; c < kTileN; ++c) {
+              const int jj = j0 + c;
+              const bool vis = (c >= clo) & (c <= chi) & (jj < p.S_k) &&
+                               doc_b[jj < p.S_k ? jj : 0] == doc_i;
+              tv[c] = vis ? tv[c] : -INFINITY;
+            }
+          } else {
+#pragma unroll
+            for (int c = 0; c < kTileN; ++c) tv[c] = ((c >= clo) & (c <= chi)) ? tv[c] : -INFINITY;
+          }
+        }
+        // P (times the soft cap's derivative), in place, while dP computes
+#pragma unroll
+        for (int c = 0; c < kTileN; ++c) {
+          float pr = ptx::ex2_approx(tv[c] - lse2);
+          if constexpr (SOFTCAP) {  // masked: t = -inf, clamped so the factor is 0
+            const float uu = fmaxf(tv[c], -md.capl2) / md.capl2;
+            pr *= 1.0f - uu * uu;
+          }
+          tv[c] = pr;
+        }
+        {
+          const bool got = bwait(bar(DPF), (s_cnt & 1) ^ 1, ctl, kBSiteElem);
+          ok = __all_sync(0xffffffffu, got);
+          if (!ok) break;
+        }
+        ptx::tc_fence_after();
+        // dS = P (dP - Delta), 32 columns at a time, packed over dP's columns
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4) {
+          uint32_t dp[32];
+          ptx::tmem_ld32(tP + (uint32_t)(32 * k4), dp);
+          ptx::tmem_wait_ld();
+          uint32_t pk[16];
+#pragma unroll
+          for (int c2 = 0; c2 < 16; ++c2) {
+            const int c = 32 * k4 + 2 * c2;
+            pk[c2] = ptx::pack_bf16x2(tv[c] * (__uint_as_float(dp[2 * c2]) - dlt),
+                                      tv[c + 1] * (__uint_as_float(dp[2 * c2 + 1]) - dlt));
+          }
+          ptx::tmem_st16(tP + (uint32_t)(16 * k4), pk);
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
@@ -632,7 +670,8 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
   const int docs_sorted = p.hdr->docs_sorted;
 
   auto bar = [&](int i) { return sbase + (uint32_t)(C::kKvBar + 8 * i); };
-  enum { KF = 0, KE = 1, QF = 2, QE = 4, SF = 6, PF = 7, AF = 8, AE = 9, DRAIN = 10 };
+  enum { KF = 0, KE = 1, QF = 2, QE = 4, SF = 6, PF = 7, AF = 8, AE = 9, DRAIN = 10, DPF = 11,
+         DSF = 12 };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kKvBar + 8 * C::kNumBars);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kKvBar + 8 * C::kNumBars + 4);
   if (threadIdx.x == 0) {
@@ -646,6 +685,8 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
     ptx::mbar_init(bar(PF), 4);
     ptx::mbar_init(bar(AF), 1);
     ptx::mbar_init(bar(AE), 4);
+    ptx::mbar_init(bar(DPF), 1);
+    ptx::mbar_init(bar(DSF), 4);
     ptx::mbar_init(bar(DRAIN), 1);
     *s_abort = 0;
     ptx::fence_mbar_init();
@@ -743,7 +784,7 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
     auto waitw = [&](uint32_t b, uint32_t par) {
       return __all_sync(0xffffffffu, bwait(b, par, ctl, kBSiteMma));
     };
-    uint32_t q_cnt = 0, p_cnt = 0;
+    uint32_t q_cnt = 0, p_cnt = 0, ds_cnt = 0;
     int act = 0;
     bool ok = true;
     for (int r = 0; ok; ++r) {
@@ -754,29 +795,48 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
       ok = waitw(bar(KF), act & 1);
       if (ok && act > 0) ok = waitw(bar(AE), (act - 1) & 1);
       if (!ok) break;
+      // Software pipeline over the item's units u: dV(u) starts as soon as
+      // P^T(u) is written, S^T(u+1) follows it (P^T(u) has been read), and
+      // dK(u) waits for dS^T(u), so the elementwise warps' next tile is
+      // computed while dK(u) and dP^T(u+1) run.
       const int units = p.group * it.n;
+      const uint32_t q0 = q_cnt;
+      auto qaddr = [&](int u) { return stage_addr((int)((q0 + (uint32_t)u) & 1)); };
+      auto q_ready = [&](int u) {
+        return waitw(bar(QF + (int)((q0 + (uint32_t)u) & 1)), ((q0 + (uint32_t)u) >> 1) & 1);
+      };
+      ok = q_ready(0);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      mma_nt<D>(tST, k_kmaj, BDesc<D>::kKMajor + (qaddr(0) >> 4));  // S^T = K Q^T
+      ptx::mma_commit_elect(bar(SF));
+      mma_nt<D>(tDPT, v_kmaj, BDesc<D>::kKMajor + ((qaddr(0) + C::kTileBytes) >> 4));  // dP^T
+      ptx::mma_commit_elect(bar(DPF));
       for (int u = 0; u < units && ok; ++u) {
-        const int st = (int)(q_cnt & 1);
-        ok = waitw(bar(QF + st), (q_cnt >> 1) & 1);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        const uint32_t qaddr = stage_addr(st);
-        const uint64_t q_kmaj = BDesc<D>::kKMajor + (qaddr >> 4);
-        const uint64_t do_kmaj = BDesc<D>::kKMajor + ((qaddr + C::kTileBytes) >> 4);
-        const uint64_t q_mn = BDesc<D>::kMNMajor + (qaddr >> 4);
-        const uint64_t do_mn = BDesc<D>::kMNMajor + ((qaddr + C::kTileBytes) >> 4);
-        mma_nt<D>(tST, k_kmaj, q_kmaj);    // S^T = K Q^T
-        mma_nt<D>(tDPT, v_kmaj, do_kmaj);  // dP^T = V dO^T
-        ptx::mma_commit_elect(bar(SF));
         ok = waitw(bar(PF), p_cnt & 1);
         if (!ok) break;
         ++p_cnt;
         ptx::tc_fence_after();
-        mma_tn<D>(tDV, tST, do_mn, u > 0);   // dV += P^T dO
-        mma_tn<D>(tDK, tDPT, q_mn, u > 0);   // dK += dS^T Q
-        ptx::mma_commit_elect(bar(QE + st));
-        ++q_cnt;
+        mma_tn<D>(tDV, tST, BDesc<D>::kMNMajor + ((qaddr(u) + C::kTileBytes) >> 4), u > 0);  // dV
+        if (u + 1 < units) {
+          ok = q_ready(u + 1);
+          if (!ok) break;
+          ptx::tc_fence_after();
+          mma_nt<D>(tST, k_kmaj, BDesc<D>::kKMajor + (qaddr(u + 1) >> 4));
+          ptx::mma_commit_elect(bar(SF));
+        }
+        ok = waitw(bar(DSF), ds_cnt & 1);
+        if (!ok) break;
+        ++ds_cnt;
+        ptx::tc_fence_after();
+        mma_tn<D>(tDK, tDPT, BDesc<D>::kMNMajor + (qaddr(u) >> 4), u > 0);  // dK += dS^T Q
+        ptx::mma_commit_elect(bar(QE + (int)((q0 + (uint32_t)u) & 1)));
+        if (u + 1 < units) {
+          mma_nt<D>(tDPT, v_kmaj, BDesc<D>::kKMajor + ((qaddr(u + 1) + C::kTileBytes) >> 4));
+          ptx::mma_commit_elect(bar(DPF));
+        }
       }
+      q_cnt = q0 + (uint32_t)units;
       if (!ok) break;
       ptx::mma_commit_elect(bar(AF));
       ptx::mma_commit_elect(bar(KE));
@@ -844,65 +904,91 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
                                                                st * C::kKvStageBytes +
                                                                2 * C::kTileBytes);
           const float* s_delta = s_lse2 + kTileM;
+          // S^T of the whole tile (this key against 128 queries) into registers
+          float tv[kTileM];
+          const float jb = (float)(j - (i0 + p.q_offset));  // bias position of column 0
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
-            uint32_t ra[32], rb[32], pa[32], pb[32];
+            uint32_t ra[32], rb[32];
             ptx::tmem_ld32(tST + (uint32_t)(64 * hh), ra);
             ptx::tmem_ld32(tST + (uint32_t)(64 * hh + 32), rb);
-            ptx::tmem_ld32(tDPT + (uint32_t)(64 * hh), pa);
-            ptx::tmem_ld32(tDPT + (uint32_t)(64 * hh + 32), pb);
             ptx::tmem_wait_ld();
-            // scores, then the mask in its own loop, then P and dS
-            // branch-free (as in the dQ kernel)
-            const int ih = i0 + 64 * hh;  // first query of this half
-            float tv[64];
 #pragma unroll
-            for (int c = 0; c < 64; ++c)
-              tv[c] = score_t<ALIBI, SOFTCAP>(__uint_as_float(c < 32 ? ra[c] : rb[c - 32]),
-                                              (float)(j - (ih + c + p.q_offset)), md);
-            if (!valid || cls == kPartial) {
-              const int clo = ilo - ih, chi = ihi - ih;
-              if (has_doc) {
-#pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                  const int qi = ih + c;
-                  const bool vis = valid & (c >= clo) & (c <= chi) & (qi < p.S_q) &&
-                                   doc_b[qi < p.S_q ? qi : 0] == doc_j;
-                  tv[c] = vis ? tv[c] : -INFINITY;
-                }
-              } else {
-#pragma unroll
-                for (int c = 0; c < 64; ++c)
-                  tv[c] = (valid & (c >= clo) & (c <= chi)) ? tv[c] : -INFINITY;
-              }
+            for (int c = 0; c < 32; ++c) {
+              const int c0 = 64 * hh + c;
+              tv[c0] = score_t<ALIBI, SOFTCAP>(__uint_as_float(ra[c]), jb - (float)c0, md);
+              tv[c0 + 32] = score_t<ALIBI, SOFTCAP>(__uint_as_float(rb[c]), jb - (float)(c0 + 32), md);
             }
-            uint32_t pp[32], pd[32];
+          }
+          // the mask in a loop of its own (rows beyond S_k see nothing)
+          if (!valid || cls == kPartial) {
+            const int clo = ilo - i0, chi = ihi - i0;
+            if (has_doc) {
+#pragma unroll
+              for (int c = 0; c < kTileM; ++c) {
+                const int qi = i0 + c;
+                const bool vis = valid & (c >= clo) & (c <= chi) & (qi < p.S_q) &&
+                                 doc_b[qi < p.S_q ? qi : 0] == doc_j;
+                tv[c] = vis ? tv[c] : -INFINITY;
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < kTileM; ++c)
+                tv[c] = (valid & (c >= clo) & (c <= chi)) ? tv[c] : -INFINITY;
+            }
+          }
+          // P^T, packed over S^T's first 64 columns for dV; kept (times the
+          // soft cap's derivative) in place for dS^T
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t pp[32];
 #pragma unroll
             for (int c2 = 0; c2 < 32; ++c2) {
-              float pr2[2], ds2[2];
+              float pr[2];
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
-                const int c = 2 * c2 + e;
-                const float dp = __uint_as_float(c < 32 ? pa[c] : pb[c - 32]);
-                const float pr = ptx::ex2_approx(tv[c] - s_lse2[64 * hh + c]);
-                float ds = pr * (dp - s_delta[64 * hh + c]);
+                const int c = 64 * hh + 2 * c2 + e;
+                pr[e] = ptx::ex2_approx(tv[c] - s_lse2[c]);
+                float dm = 1.0f;
                 if constexpr (SOFTCAP) {
                   const float uu = fmaxf(tv[c], -md.capl2) / md.capl2;
-                  ds *= 1.0f - uu * uu;
+                  dm = 1.0f - uu * uu;
                 }
-                pr2[e] = pr;
-                ds2[e] = ds;
+                tv[c] = pr[e] * dm;
               }
-              pp[c2] = ptx::pack_bf16x2(pr2[0], pr2[1]);
-              pd[c2] = ptx::pack_bf16x2(ds2[0], ds2[1]);
+              pp[c2] = ptx::pack_bf16x2(pr[0], pr[1]);
             }
             ptx::tmem_st32(tST + (uint32_t)(32 * hh), pp);
-            ptx::tmem_st32(tDPT + (uint32_t)(32 * hh), pd);
           }
           ptx::tmem_wait_st();
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive(bar(PF));
+          {
+            const bool got = bwait(bar(DPF), q_cnt & 1, ctl, kBSiteElem);
+            ok = __all_sync(0xffffffffu, got);
+            if (!ok) break;
+          }
+          ptx::tc_fence_after();
+          // dS^T = P^T (dP^T - Delta), 32 columns at a time, packed over dP^T's
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            uint32_t dp[32];
+            ptx::tmem_ld32(tDPT + (uint32_t)(32 * k4), dp);
+            ptx::tmem_wait_ld();
+            uint32_t pk[16];
+#pragma unroll
+            for (int c2 = 0; c2 < 16; ++c2) {
+              const int c = 32 * k4 + 2 * c2;
+              pk[c2] = ptx::pack_bf16x2(tv[c] * (__uint_as_float(dp[2 * c2]) - s_delta[c]),
+                                        tv[c + 1] * (__uint_as_float(dp[2 * c2 + 1]) - s_delta[c + 1]));
+            }
+            ptx::tmem_st16(tDPT + (uint32_t)(16 * k4), pk);
+          }
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bar(DSF));
           ++q_cnt;
         }
       }
