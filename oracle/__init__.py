@@ -34,8 +34,21 @@ MASK_CAUSAL = 1
 MASK_WINDOW = 2
 MASK_DOCUMENT = 4
 MASK_PREFIX_LM = 8
+MASK_BLOCKS = 16
 SCORE_ALIBI = 1
 SCORE_SOFTCAP = 2
+SCORE_RELBIAS = 4
+BLOCK = 128  # edge of a block-map tile
+
+
+class _Mods(ctypes.Structure):
+    """Mirror of the C ``or_mods``."""
+    _fields_ = [("mask_flags", ctypes.c_uint32), ("score_flags", ctypes.c_uint32),
+                ("window", ctypes.c_int), ("q_offset", ctypes.c_int),
+                ("doc_ids", ctypes.c_void_p), ("prefix_len", ctypes.c_void_p),
+                ("alibi_slopes", ctypes.c_void_p), ("softcap", ctypes.c_double),
+                ("blocks", ctypes.c_void_p), ("blocks_batched", ctypes.c_int),
+                ("rel_bias", ctypes.c_void_p), ("rel_max", ctypes.c_int)]
 
 
 def build(force: bool = False) -> str:
@@ -63,16 +76,13 @@ def _load():
     build()
     lib = ctypes.CDLL(_LIB_PATH)
     P = ctypes.c_void_p
+    M = ctypes.POINTER(_Mods)
     lib.oracle_attn_rows.restype = ctypes.c_int
     lib.oracle_attn_rows.argtypes = [
         P, P, P,                                   # q k v
         ctypes.c_int, ctypes.c_int, ctypes.c_int,  # B H H_kv
         ctypes.c_int, ctypes.c_int, ctypes.c_int,  # S_q S_k D
-        ctypes.c_double,                           # scale
-        ctypes.c_uint32, ctypes.c_uint32,          # mask / score flags
-        ctypes.c_int, ctypes.c_int,                # window q_offset
-        P, P, P,                                   # doc prefix slopes
-        ctypes.c_double,                           # softcap
+        ctypes.c_double, M,                        # scale, mods
         P, ctypes.c_int64,                         # rows n
         P, P, P,                                   # out lse probs
     ]
@@ -83,11 +93,7 @@ def _load():
             P, P, P, P,                                # q k v dout
             ctypes.c_int, ctypes.c_int, ctypes.c_int,  # B H H_kv
             ctypes.c_int, ctypes.c_int, ctypes.c_int,  # S_q S_k D
-            ctypes.c_double,                           # scale
-            ctypes.c_uint32, ctypes.c_uint32,          # mask / score flags
-            ctypes.c_int, ctypes.c_int,                # window q_offset
-            P, P, P,                                   # doc_ids prefix_len slopes
-            ctypes.c_double,                           # softcap
+            ctypes.c_double, M,                        # scale, mods
             P, ctypes.c_int64,                         # rows / keys, n
         ] + ([P] if name.endswith("rows") else [P, P])
     lib.oracle_num_threads.restype = ctypes.c_int
@@ -131,18 +137,74 @@ def _ptr(a: Optional[np.ndarray]):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
+def _mods(B, H, S_q, S_k, causal=False, window=0, doc_ids=None, prefix_len=None,
+          alibi=False, alibi_slopes=None, softcap=0.0, q_offset=0, rel_bias=None,
+          blocks=None):
+    """The C mods struct and the arrays it points to (keep them alive)."""
+    m = _Mods()
+    keep = []
+    if causal:
+        m.mask_flags |= MASK_CAUSAL
+    if window and window > 0:
+        m.mask_flags |= MASK_WINDOW
+        m.window = int(window)
+    m.q_offset = int(q_offset)
+    if doc_ids is not None:
+        m.mask_flags |= MASK_DOCUMENT
+        docs = np.ascontiguousarray(np.broadcast_to(_i32(doc_ids).reshape(-1, S_k), (B, S_k)))
+        keep.append(docs)
+        m.doc_ids = docs.ctypes.data
+    if prefix_len is not None:
+        m.mask_flags |= MASK_PREFIX_LM
+        pref = _i32(prefix_len)
+        keep.append(pref)
+        m.prefix_len = pref.ctypes.data
+    if blocks is not None:
+        blk = np.ascontiguousarray(np.asarray(
+            blocks.cpu().numpy() if hasattr(blocks, "cpu") else blocks, dtype=np.uint8))
+        nq, nk = -(-S_q // BLOCK), -(-S_k // BLOCK)
+        blk = blk.reshape(-1, nq, nk)
+        assert blk.shape[0] in (1, B)
+        m.mask_flags |= MASK_BLOCKS
+        m.blocks_batched = 1 if (blk.shape[0] == B and B > 1) else 0
+        keep.append(blk)
+        m.blocks = blk.ctypes.data
+    if alibi or alibi_slopes is not None:
+        m.score_flags |= SCORE_ALIBI
+        if alibi_slopes is not None:
+            sl = np.ascontiguousarray(np.asarray(
+                alibi_slopes.cpu().numpy() if hasattr(alibi_slopes, "cpu") else alibi_slopes,
+                dtype=np.float64))
+            assert sl.shape == (H,)
+            keep.append(sl)
+            m.alibi_slopes = sl.ctypes.data
+    if rel_bias is not None:
+        rb = np.ascontiguousarray(np.asarray(
+            rel_bias.cpu().numpy() if hasattr(rel_bias, "cpu") else rel_bias, dtype=np.float64))
+        assert rb.ndim == 2 and rb.shape[0] == H and rb.shape[1] % 2 == 1
+        m.score_flags |= SCORE_RELBIAS
+        m.rel_max = (rb.shape[1] - 1) // 2
+        keep.append(rb)
+        m.rel_bias = rb.ctypes.data
+    if softcap and softcap > 0:
+        m.score_flags |= SCORE_SOFTCAP
+        m.softcap = float(np.float32(softcap))
+    return m, keep
+
+
 def attn_rows(q, k, v, *, scale: float, rows: Optional[Sequence[int]] = None,
-              causal: bool = False, window: int = 0, doc_ids=None,
-              prefix_len=None, alibi: bool = False,
-              alibi_slopes: Optional[Sequence[float]] = None,
-              softcap: float = 0.0, q_offset: int = 0,
-              want_probs: bool = False):
+              want_probs: bool = False, **mods):
     """Attention forward of the requested rows, in float64.
 
     ``q`` [B,H,S_q,D] and ``k``/``v`` [B,H_kv,S_k,D] are bf16 torch tensors
     (or uint16 numpy arrays of bf16 bits).  ``scale`` and ``softcap`` are used
-    as the float32 values a GPU kernel would receive.  ``rows`` are flattened
-    (b*H + h)*S_q + i indices (all rows when None).
+    as the float32 values a GPU kernel would receive (the bias-table entries
+    as the float32 values given).  ``rows`` are flattened (b*H + h)*S_q + i
+    indices (all rows when None).  Mods: ``causal``, ``window``, ``doc_ids``
+    [B,S_k], ``prefix_len`` [B], ``alibi`` / ``alibi_slopes`` [H],
+    ``softcap``, ``q_offset``, ``rel_bias`` [H, 2R+1] (score += rel_bias[h,
+    clamp(kpos - qpos, -R, R) + R]), ``blocks`` [B or 1, ceil(S_q/128),
+    ceil(S_k/128)] (0 hides the tile).
 
     Returns ``(O, LSE)`` as float64 arrays of shapes [n, D] and [n] (and the
     [n, S_k] probability matrix when ``want_probs``).
@@ -157,37 +219,14 @@ def attn_rows(q, k, v, *, scale: float, rows: Optional[Sequence[int]] = None,
     else:
         rows_a = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
     n = rows_a.shape[0]
-    mask = 0
-    if causal:
-        mask |= MASK_CAUSAL
-    if window and window > 0:
-        mask |= MASK_WINDOW
-    if doc_ids is not None:
-        mask |= MASK_DOCUMENT
-    if prefix_len is not None:
-        mask |= MASK_PREFIX_LM
-    score = 0
-    if alibi or alibi_slopes is not None:
-        score |= SCORE_ALIBI
-    if softcap and softcap > 0:
-        score |= SCORE_SOFTCAP
-    docs = _i32(doc_ids)
-    if docs is not None:
-        docs = np.ascontiguousarray(np.broadcast_to(docs.reshape(-1, S_k), (B, S_k)))
-    pref = _i32(prefix_len)
-    slopes = None
-    if alibi_slopes is not None:
-        slopes = np.ascontiguousarray(np.asarray(alibi_slopes, dtype=np.float64))
-        assert slopes.shape == (H,)
+    m, keep = _mods(B, H, S_q, S_k, **mods)
     out = np.empty((n, D), dtype=np.float64)
     lse = np.empty((n,), dtype=np.float64)
     probs = np.empty((n, S_k), dtype=np.float64) if want_probs else None
-    scale32 = float(np.float32(scale))
-    cap32 = float(np.float32(softcap)) if softcap else 0.0
     rc = lib.oracle_attn_rows(
-        _ptr(qb), _ptr(kb), _ptr(vb), B, H, H_kv, S_q, S_k, D, scale32,
-        mask, score, int(window or 0), int(q_offset), _ptr(docs), _ptr(pref),
-        _ptr(slopes), cap32, _ptr(rows_a), n, _ptr(out), _ptr(lse), _ptr(probs))
+        _ptr(qb), _ptr(kb), _ptr(vb), B, H, H_kv, S_q, S_k, D, float(np.float32(scale)),
+        ctypes.byref(m), _ptr(rows_a), n, _ptr(out), _ptr(lse), _ptr(probs))
+    del keep
     if rc != 0:
         raise ValueError("oracle_attn_rows rejected its arguments")
     if want_probs:
@@ -195,41 +234,11 @@ def attn_rows(q, k, v, *, scale: float, rows: Optional[Sequence[int]] = None,
     return out, lse
 
 
-def _mod_args(B, H, S_k, causal, window, doc_ids, prefix_len, alibi, alibi_slopes,
-              softcap):
-    mask = 0
-    if causal:
-        mask |= MASK_CAUSAL
-    if window and window > 0:
-        mask |= MASK_WINDOW
-    if doc_ids is not None:
-        mask |= MASK_DOCUMENT
-    if prefix_len is not None:
-        mask |= MASK_PREFIX_LM
-    score = 0
-    if alibi or alibi_slopes is not None:
-        score |= SCORE_ALIBI
-    if softcap and softcap > 0:
-        score |= SCORE_SOFTCAP
-    docs = _i32(doc_ids)
-    if docs is not None:
-        docs = np.ascontiguousarray(np.broadcast_to(docs.reshape(-1, S_k), (B, S_k)))
-    pref = _i32(prefix_len)
-    slopes = None
-    if alibi_slopes is not None:
-        slopes = np.ascontiguousarray(np.asarray(alibi_slopes, dtype=np.float64))
-        assert slopes.shape == (H,)
-    cap32 = float(np.float32(softcap)) if softcap else 0.0
-    return mask, score, docs, pref, slopes, cap32
-
-
 def attn_bwd_rows(q, k, v, dout, *, scale: float, rows: Optional[Sequence[int]] = None,
-                  causal: bool = False, window: int = 0, doc_ids=None, prefix_len=None,
-                  alibi: bool = False, alibi_slopes: Optional[Sequence[float]] = None,
-                  softcap: float = 0.0, q_offset: int = 0):
+                  **mods):
     """dQ of the requested query rows (flattened (b*H + h)*S_q + i; all when
     None) for upstream gradient ``dout`` [B,H,S_q,D] (bf16), in float64:
-    an array [n, D]."""
+    an array [n, D].  Mods as for :func:`attn_rows`."""
     lib = _load()
     qb, kb, vb, gb = _bits(q), _bits(k), _bits(v), _bits(dout)
     B, H, S_q, D = qb.shape
@@ -237,25 +246,23 @@ def attn_bwd_rows(q, k, v, dout, *, scale: float, rows: Optional[Sequence[int]] 
     assert gb.shape == qb.shape and vb.shape == kb.shape
     rows_a = (np.arange(B * H * S_q, dtype=np.int64) if rows is None
               else np.ascontiguousarray(np.asarray(rows, dtype=np.int64)))
-    mask, score, docs, pref, slopes, cap32 = _mod_args(
-        B, H, S_k, causal, window, doc_ids, prefix_len, alibi, alibi_slopes, softcap)
+    m, keep = _mods(B, H, S_q, S_k, **mods)
     dq = np.empty((rows_a.shape[0], D), dtype=np.float64)
     rc = lib.oracle_attn_bwd_rows(
         _ptr(qb), _ptr(kb), _ptr(vb), _ptr(gb), B, H, H_kv, S_q, S_k, D,
-        float(np.float32(scale)), mask, score, int(window or 0), int(q_offset), _ptr(docs),
-        _ptr(pref), _ptr(slopes), cap32, _ptr(rows_a), rows_a.shape[0], _ptr(dq))
+        float(np.float32(scale)), ctypes.byref(m), _ptr(rows_a), rows_a.shape[0], _ptr(dq))
+    del keep
     if rc != 0:
         raise ValueError("oracle_attn_bwd_rows rejected its arguments")
     return dq
 
 
 def attn_bwd_keys(q, k, v, dout, *, scale: float, keys: Optional[Sequence[int]] = None,
-                  causal: bool = False, window: int = 0, doc_ids=None, prefix_len=None,
-                  alibi: bool = False, alibi_slopes: Optional[Sequence[float]] = None,
-                  softcap: float = 0.0, q_offset: int = 0):
+                  **mods):
     """dK and dV of the requested key positions (flattened
     (b*H_kv + hk)*S_k + j; all when None), summed over the query heads that
-    share each K/V head, in float64: two arrays [n, D]."""
+    share each K/V head, in float64: two arrays [n, D].  Mods as for
+    :func:`attn_rows`."""
     lib = _load()
     qb, kb, vb, gb = _bits(q), _bits(k), _bits(v), _bits(dout)
     B, H, S_q, D = qb.shape
@@ -263,14 +270,14 @@ def attn_bwd_keys(q, k, v, dout, *, scale: float, keys: Optional[Sequence[int]] 
     assert gb.shape == qb.shape and vb.shape == kb.shape
     keys_a = (np.arange(B * H_kv * S_k, dtype=np.int64) if keys is None
               else np.ascontiguousarray(np.asarray(keys, dtype=np.int64)))
-    mask, score, docs, pref, slopes, cap32 = _mod_args(
-        B, H, S_k, causal, window, doc_ids, prefix_len, alibi, alibi_slopes, softcap)
+    m, keep = _mods(B, H, S_q, S_k, **mods)
     dk = np.empty((keys_a.shape[0], D), dtype=np.float64)
     dv = np.empty((keys_a.shape[0], D), dtype=np.float64)
     rc = lib.oracle_attn_bwd_keys(
         _ptr(qb), _ptr(kb), _ptr(vb), _ptr(gb), B, H, H_kv, S_q, S_k, D,
-        float(np.float32(scale)), mask, score, int(window or 0), int(q_offset), _ptr(docs),
-        _ptr(pref), _ptr(slopes), cap32, _ptr(keys_a), keys_a.shape[0], _ptr(dk), _ptr(dv))
+        float(np.float32(scale)), ctypes.byref(m), _ptr(keys_a), keys_a.shape[0], _ptr(dk),
+        _ptr(dv))
+    del keep
     if rc != 0:
         raise ValueError("oracle_attn_bwd_keys rejected its arguments")
     return dk, dv

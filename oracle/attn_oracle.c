@@ -35,6 +35,11 @@
  *    qpos - W < kpos <= qpos; document: doc[i] == doc[j]; prefix-LM:
  *    kpos <= qpos OR kpos < prefix_len[b]; qpos = i + q_offset, kpos = j;
  *  - GQA: query head h reads KV head h / (H / H_kv);
+ *  - a relative-position bias table adds rel_bias[h][clamp(kpos - qpos,
+ *    -R, R) + R] after ALiBi and before the soft cap; a block map hides
+ *    every (query, key) pair whose 128 x 128 tile it marks 0 (both are the
+ *    "further descriptor mods" of the design: a generic relative-position
+ *    bias and a user block mask);
  *  - LSE is the natural-log log-sum-exp of the modified scores over visible
  *    keys; a row with no visible key has O = 0 and LSE = -inf.
  */
@@ -51,11 +56,28 @@ enum {
     OR_MASK_WINDOW = 2,
     OR_MASK_DOCUMENT = 4,
     OR_MASK_PREFIX_LM = 8,
+    OR_MASK_BLOCKS = 16,
 };
 enum {
     OR_SCORE_ALIBI = 1,
     OR_SCORE_SOFTCAP = 2,
+    OR_SCORE_RELBIAS = 4,
 };
+enum { OR_BLOCK = 128 };  /* edge of a block-map tile, in rows and keys */
+
+/* The score and mask modifications of one call. */
+typedef struct or_mods {
+    uint32_t mask_flags, score_flags;
+    int window, q_offset;
+    const int32_t *doc_ids;     /* [B][S_k] */
+    const int32_t *prefix_len;  /* [B] */
+    const double *alibi_slopes; /* [H] or NULL for 2^(-8(h+1)/H) */
+    double softcap;
+    const uint8_t *blocks;      /* [B or 1][ceil(S_q/128)][ceil(S_k/128)] */
+    int blocks_batched;         /* 1: one map per batch entry */
+    const double *rel_bias;     /* [H][2 * rel_max + 1] */
+    int rel_max;
+} or_mods;
 
 /* A bfloat16 value is the upper 16 bits of an IEEE binary32 value, so the
  * conversion to double is exact. */
@@ -78,22 +100,68 @@ int oracle_num_threads(void)
 
 /* Is key j visible to query row i of batch b?  Each enabled mask is
  * evaluated as written and the results are combined with AND. */
-static int visible(int64_t i, int64_t j, int b, int S_k, uint32_t mask_flags,
-                   int window, int q_offset, const int32_t *doc_ids,
-                   const int32_t *prefix_len)
+static int visible(int64_t i, int64_t j, int b, int S_q, int S_k, const or_mods *m)
 {
-    int64_t qpos = i + (int64_t)q_offset;
+    int64_t qpos = i + (int64_t)m->q_offset;
     int64_t kpos = j;
     int vis = 1;
-    if (mask_flags & OR_MASK_CAUSAL)
+    if (m->mask_flags & OR_MASK_CAUSAL)
         vis = vis && (kpos <= qpos);
-    if (mask_flags & OR_MASK_WINDOW)
-        vis = vis && (qpos - (int64_t)window < kpos) && (kpos <= qpos);
-    if (mask_flags & OR_MASK_DOCUMENT)
-        vis = vis && (doc_ids[(int64_t)b * S_k + i] == doc_ids[(int64_t)b * S_k + j]);
-    if (mask_flags & OR_MASK_PREFIX_LM)
-        vis = vis && ((kpos <= qpos) || (kpos < (int64_t)prefix_len[b]));
+    if (m->mask_flags & OR_MASK_WINDOW)
+        vis = vis && (qpos - (int64_t)m->window < kpos) && (kpos <= qpos);
+    if (m->mask_flags & OR_MASK_DOCUMENT)
+        vis = vis && (m->doc_ids[(int64_t)b * S_k + i] == m->doc_ids[(int64_t)b * S_k + j]);
+    if (m->mask_flags & OR_MASK_PREFIX_LM)
+        vis = vis && ((kpos <= qpos) || (kpos < (int64_t)m->prefix_len[b]));
+    if (m->mask_flags & OR_MASK_BLOCKS) {
+        const int64_t nq = (S_q + OR_BLOCK - 1) / OR_BLOCK, nk = (S_k + OR_BLOCK - 1) / OR_BLOCK;
+        const int64_t mb = m->blocks_batched ? b : 0;
+        vis = vis && m->blocks[(mb * nq + i / OR_BLOCK) * nk + j / OR_BLOCK] != 0;
+    }
     return vis;
+}
+
+/* The modified score of (row i of head h, key j) from the scaled dot
+ * product x: ALiBi, then the relative-position bias, then the soft cap. */
+static double modified_score(double x, int64_t i, int64_t j, int h, int H, const or_mods *m)
+{
+    const double qpos = (double)(i + m->q_offset);
+    double s = x;
+    if (m->score_flags & OR_SCORE_ALIBI) {
+        const double slope = m->alibi_slopes ? m->alibi_slopes[h]
+                                             : pow(2.0, -8.0 * (double)(h + 1) / (double)H);
+        s += -slope * (qpos - (double)j);
+    }
+    if (m->score_flags & OR_SCORE_RELBIAS) {
+        int64_t r = j - (i + (int64_t)m->q_offset);
+        if (r < -(int64_t)m->rel_max)
+            r = -(int64_t)m->rel_max;
+        if (r > (int64_t)m->rel_max)
+            r = (int64_t)m->rel_max;
+        s += m->rel_bias[(int64_t)h * (2 * (int64_t)m->rel_max + 1) + r + m->rel_max];
+    }
+    if (m->score_flags & OR_SCORE_SOFTCAP)
+        s = m->softcap * tanh(s / m->softcap);
+    return s;
+}
+
+static int check_dims(int B, int H, int H_kv, int S_q, int S_k, int D, const or_mods *m)
+{
+    if (B <= 0 || H <= 0 || H_kv <= 0 || S_q <= 0 || S_k <= 0 || D <= 0)
+        return -1;
+    if (H % H_kv != 0)
+        return -1;
+    if ((m->mask_flags & OR_MASK_DOCUMENT) && (m->doc_ids == NULL || S_q != S_k))
+        return -1;
+    if ((m->mask_flags & OR_MASK_PREFIX_LM) && m->prefix_len == NULL)
+        return -1;
+    if ((m->mask_flags & OR_MASK_BLOCKS) && m->blocks == NULL)
+        return -1;
+    if ((m->score_flags & OR_SCORE_SOFTCAP) && !(m->softcap > 0.0))
+        return -1;
+    if ((m->score_flags & OR_SCORE_RELBIAS) && (m->rel_bias == NULL || m->rel_max < 0))
+        return -1;
+    return 0;
 }
 
 /*
@@ -115,21 +183,10 @@ static int visible(int64_t i, int64_t j, int b, int S_k, uint32_t mask_flags,
  */
 int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                      int B, int H, int H_kv, int S_q, int S_k, int D,
-                     double scale, uint32_t mask_flags, uint32_t score_flags,
-                     int window, int q_offset, const int32_t *doc_ids,
-                     const int32_t *prefix_len, const double *alibi_slopes,
-                     double softcap, const int64_t *rows, int64_t n_rows,
+                     double scale, const or_mods *m, const int64_t *rows, int64_t n_rows,
                      double *out, double *lse, double *probs)
 {
-    if (B <= 0 || H <= 0 || H_kv <= 0 || S_q <= 0 || S_k <= 0 || D <= 0)
-        return -1;
-    if (H % H_kv != 0)
-        return -1;
-    if ((mask_flags & OR_MASK_DOCUMENT) && (doc_ids == NULL || S_q != S_k))
-        return -1;
-    if ((mask_flags & OR_MASK_PREFIX_LM) && prefix_len == NULL)
-        return -1;
-    if ((score_flags & OR_SCORE_SOFTCAP) && !(softcap > 0.0))
+    if (check_dims(B, H, H_kv, S_q, S_k, D, m))
         return -1;
     const int group = H / H_kv;
     int bad = 0;
@@ -160,11 +217,6 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                 const uint16_t *vb = v + ((int64_t)b * H_kv + hk) * (int64_t)S_k * D;
                 for (int d = 0; d < D; ++d)
                     qrow[d] = bf16_to_double(qp[d]);
-                double slope = 0.0;
-                if (score_flags & OR_SCORE_ALIBI)
-                    slope = alibi_slopes ? alibi_slopes[h]
-                                         : pow(2.0, -8.0 * (double)(h + 1) / (double)H);
-                double qpos = (double)(i + q_offset);
 
                 /* scores of every key, then the mods, then the mask */
                 double M = -INFINITY;
@@ -173,14 +225,9 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                     double dot = 0.0;
                     for (int d = 0; d < D; ++d)
                         dot += qrow[d] * bf16_to_double(kp[d]);
-                    double sj = scale * dot;
-                    if (score_flags & OR_SCORE_ALIBI)
-                        sj += -slope * (qpos - (double)j);
-                    if (score_flags & OR_SCORE_SOFTCAP)
-                        sj = softcap * tanh(sj / softcap);
+                    const double sj = modified_score(scale * dot, i, j, h, H, m);
                     s[j] = sj;
-                    vis[j] = (unsigned char)visible(i, j, b, S_k, mask_flags, window,
-                                                    q_offset, doc_ids, prefix_len);
+                    vis[j] = (unsigned char)visible(i, j, b, S_q, S_k, m);
                     if (vis[j] && sj > M)
                         M = sj;
                 }
@@ -249,10 +296,7 @@ int oracle_attn_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
  * visible. */
 static int row_forward(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                        int b, int h, int64_t i, int H, int H_kv, int S_q, int S_k,
-                       int D, double scale, uint32_t mask_flags,
-                       uint32_t score_flags, int window, int q_offset,
-                       const int32_t *doc_ids, const int32_t *prefix_len,
-                       const double *alibi_slopes, double softcap, double *qrow,
+                       int D, double scale, const or_mods *m, double *qrow,
                        double *s, unsigned char *vis, double *p, double *o,
                        double *lse)
 {
@@ -262,24 +306,15 @@ static int row_forward(const uint16_t *q, const uint16_t *k, const uint16_t *v,
     const uint16_t *vb = v + ((int64_t)b * H_kv + hk) * (int64_t)S_k * D;
     for (int d = 0; d < D; ++d)
         qrow[d] = bf16_to_double(qp[d]);
-    double slope = 0.0;
-    if (score_flags & OR_SCORE_ALIBI)
-        slope = alibi_slopes ? alibi_slopes[h] : pow(2.0, -8.0 * (double)(h + 1) / (double)H);
-    const double qpos = (double)(i + q_offset);
     double M = -INFINITY;
     for (int64_t j = 0; j < S_k; ++j) {
         const uint16_t *kp = kb + j * D;
         double dot = 0.0;
         for (int d = 0; d < D; ++d)
             dot += qrow[d] * bf16_to_double(kp[d]);
-        double sj = scale * dot;
-        if (score_flags & OR_SCORE_ALIBI)
-            sj += -slope * (qpos - (double)j);
-        if (score_flags & OR_SCORE_SOFTCAP)
-            sj = softcap * tanh(sj / softcap);
+        const double sj = modified_score(scale * dot, i, j, h, H, m);
         s[j] = sj;
-        vis[j] = (unsigned char)visible(i, j, b, S_k, mask_flags, window, q_offset,
-                                        doc_ids, prefix_len);
+        vis[j] = (unsigned char)visible(i, j, b, S_q, S_k, m);
         if (vis[j] && sj > M)
             M = sj;
     }
@@ -307,30 +342,13 @@ static int row_forward(const uint16_t *q, const uint16_t *k, const uint16_t *v,
 }
 
 /* d s / d x of the score modification at modified score s. */
-static double mod_slope(double s, uint32_t score_flags, double softcap)
+static double mod_slope(double s, const or_mods *m)
 {
-    if (score_flags & OR_SCORE_SOFTCAP) {
-        double t = s / softcap;
+    if (m->score_flags & OR_SCORE_SOFTCAP) {
+        double t = s / m->softcap;
         return 1.0 - t * t;
     }
     return 1.0;
-}
-
-static int check_dims(int B, int H, int H_kv, int S_q, int S_k, int D, uint32_t mask_flags,
-                      uint32_t score_flags, const int32_t *doc_ids,
-                      const int32_t *prefix_len, double softcap)
-{
-    if (B <= 0 || H <= 0 || H_kv <= 0 || S_q <= 0 || S_k <= 0 || D <= 0)
-        return -1;
-    if (H % H_kv != 0)
-        return -1;
-    if ((mask_flags & OR_MASK_DOCUMENT) && (doc_ids == NULL || S_q != S_k))
-        return -1;
-    if ((mask_flags & OR_MASK_PREFIX_LM) && prefix_len == NULL)
-        return -1;
-    if ((score_flags & OR_SCORE_SOFTCAP) && !(softcap > 0.0))
-        return -1;
-    return 0;
 }
 
 /*
@@ -342,13 +360,10 @@ static int check_dims(int B, int H, int H_kv, int S_q, int S_k, int D, uint32_t 
  */
 int oracle_attn_bwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                          const uint16_t *dout, int B, int H, int H_kv, int S_q, int S_k,
-                         int D, double scale, uint32_t mask_flags, uint32_t score_flags,
-                         int window, int q_offset, const int32_t *doc_ids,
-                         const int32_t *prefix_len, const double *alibi_slopes,
-                         double softcap, const int64_t *rows, int64_t n_rows, double *dq)
+                         int D, double scale, const or_mods *m, const int64_t *rows,
+                         int64_t n_rows, double *dq)
 {
-    if (check_dims(B, H, H_kv, S_q, S_k, D, mask_flags, score_flags, doc_ids, prefix_len,
-                   softcap))
+    if (check_dims(B, H, H_kv, S_q, S_k, D, m))
         return -1;
     const int group = H / H_kv;
     int bad = 0;
@@ -380,9 +395,8 @@ int oracle_attn_bwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v
                 for (int d = 0; d < D; ++d)
                     dqr[d] = 0.0;
                 double lse;
-                if (row_forward(q, k, v, b, h, i, H, H_kv, S_q, S_k, D, scale, mask_flags,
-                                score_flags, window, q_offset, doc_ids, prefix_len,
-                                alibi_slopes, softcap, qrow, s, vis, p, o, &lse) != 0)
+                if (row_forward(q, k, v, b, h, i, H, H_kv, S_q, S_k, D, scale, m, qrow, s, vis,
+                                p, o, &lse) != 0)
                     continue;
                 const uint16_t *dop = dout + (((int64_t)b * H + h) * S_q + i) * D;
                 const uint16_t *kb = k + ((int64_t)b * H_kv + hk) * (int64_t)S_k * D;
@@ -399,7 +413,7 @@ int oracle_attn_bwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v
                     double dp = 0.0;
                     for (int d = 0; d < D; ++d)
                         dp += g[d] * bf16_to_double(vp[d]);
-                    const double dx = p[j] * (dp - delta) * mod_slope(s[j], score_flags, softcap);
+                    const double dx = p[j] * (dp - delta) * mod_slope(s[j], m);
                     const uint16_t *kp = kb + j * D;
                     for (int d = 0; d < D; ++d)
                         dqr[d] += scale * dx * bf16_to_double(kp[d]);
@@ -428,14 +442,10 @@ int oracle_attn_bwd_rows(const uint16_t *q, const uint16_t *k, const uint16_t *v
  */
 int oracle_attn_bwd_keys(const uint16_t *q, const uint16_t *k, const uint16_t *v,
                          const uint16_t *dout, int B, int H, int H_kv, int S_q, int S_k,
-                         int D, double scale, uint32_t mask_flags, uint32_t score_flags,
-                         int window, int q_offset, const int32_t *doc_ids,
-                         const int32_t *prefix_len, const double *alibi_slopes,
-                         double softcap, const int64_t *keys, int64_t n_keys, double *dk,
-                         double *dv)
+                         int D, double scale, const or_mods *m, const int64_t *keys,
+                         int64_t n_keys, double *dk, double *dv)
 {
-    if (check_dims(B, H, H_kv, S_q, S_k, D, mask_flags, score_flags, doc_ids, prefix_len,
-                   softcap))
+    if (check_dims(B, H, H_kv, S_q, S_k, D, m))
         return -1;
     const int group = H / H_kv;
     for (int64_t r = 0; r < n_keys; ++r)
@@ -475,9 +485,8 @@ int oracle_attn_bwd_keys(const uint16_t *q, const uint16_t *k, const uint16_t *v
                     const int h = hk * group + (int)(rr / S_q);
                     const int64_t i = rr % S_q;
                     double l;
-                    row_forward(q, k, v, b, h, i, H, H_kv, S_q, S_k, D, scale, mask_flags,
-                                score_flags, window, q_offset, doc_ids, prefix_len,
-                                alibi_slopes, softcap, qrow, s, vis, p, o, &l);
+                    row_forward(q, k, v, b, h, i, H, H_kv, S_q, S_k, D, scale, m, qrow, s, vis, p,
+                                o, &l);
                     const uint16_t *dop = dout + (((int64_t)b * H + h) * S_q + i) * D;
                     double dd = 0.0;
                     for (int d = 0; d < D; ++d)
@@ -508,7 +517,7 @@ int oracle_attn_bwd_keys(const uint16_t *q, const uint16_t *k, const uint16_t *v
                     continue;
                 const int h = hk * group + (int)(rr / S_q);
                 const int64_t i = rr % S_q;
-                if (!visible(i, j, b, S_k, mask_flags, window, q_offset, doc_ids, prefix_len))
+                if (!visible(i, j, b, S_q, S_k, m))
                     continue;
                 const uint16_t *qp = q + (((int64_t)b * H + h) * S_q + i) * D;
                 const uint16_t *dop = dout + (((int64_t)b * H + h) * S_q + i) * D;
@@ -517,17 +526,9 @@ int oracle_attn_bwd_keys(const uint16_t *q, const uint16_t *k, const uint16_t *v
                     dot += bf16_to_double(qp[d]) * bf16_to_double(kp[d]);
                     dp += bf16_to_double(dop[d]) * bf16_to_double(vp[d]);
                 }
-                double sj = scale * dot;
-                if (score_flags & OR_SCORE_ALIBI) {
-                    const double slope = alibi_slopes
-                                             ? alibi_slopes[h]
-                                             : pow(2.0, -8.0 * (double)(h + 1) / (double)H);
-                    sj += -slope * ((double)(i + q_offset) - (double)j);
-                }
-                if (score_flags & OR_SCORE_SOFTCAP)
-                    sj = softcap * tanh(sj / softcap);
+                const double sj = modified_score(scale * dot, i, j, h, H, m);
                 const double pj = exp(sj - lse[rr]);
-                const double dx = pj * (dp - delta[rr]) * mod_slope(sj, score_flags, softcap);
+                const double dx = pj * (dp - delta[rr]) * mod_slope(sj, m);
                 for (int d = 0; d < D; ++d) {
                     dvr[d] += pj * bf16_to_double(dop[d]);
                     dkr[d] += scale * dx * bf16_to_double(qp[d]);

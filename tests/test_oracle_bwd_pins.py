@@ -210,3 +210,37 @@ def test_rows_without_keys_have_zero_gradient():
     assert np.all(dq[:5] == 0.0) and np.any(dq[5:] != 0.0)
     dk, dv = oracle.attn_bwd_keys(q, k, v, do, scale=0.3, causal=True, q_offset=-5)
     assert np.all(dk[S - 5:] == 0.0) and np.all(dv[S - 5:] == 0.0)  # keys no row sees
+
+
+def test_backward_with_rel_bias_and_blocks_equals_autograd():
+    # additive relative-position bias and a block map, against float64
+    # autograd of the definition (the bias enters the scores, the map the mask)
+    B, H, Hkv, S, D = 2, 2, 1, 260, 4
+    q, k, v, do = rand_inputs(B, H, Hkv, S, S, D, seed=71)
+    R = 5
+    g = np.random.default_rng(72)
+    table = g.standard_normal((H, 2 * R + 1)).astype(np.float32).astype(np.float64)
+    blk = (g.random((B, 3, 3)) < 0.7).astype(np.uint8)
+    blk[:, :, 0] = 1
+    full = np.stack([np.kron(blk[b], np.ones((128, 128), dtype=np.uint8))[:S, :S]
+                     for b in range(B)]).astype(bool)
+    causal = np.arange(S)[None, :] <= np.arange(S)[:, None]
+    vis = torch.from_numpy(full & causal[None])
+    idx = np.clip(np.arange(S)[None, :] - np.arange(S)[:, None], -R, R) + R
+    bias = torch.from_numpy(table[:, idx])  # [H, S, S]
+
+    qd = q.double().requires_grad_(True)
+    kd = k.double().requires_grad_(True)
+    vd = v.double().requires_grad_(True)
+    kr, vr = kd.repeat_interleave(H // Hkv, dim=1), vd.repeat_interleave(H // Hkv, dim=1)
+    s = torch.matmul(qd, kr.transpose(-1, -2)) * float(np.float32(0.5)) + bias[None]
+    s = s.masked_fill(~vis[:, None], float("-inf"))
+    o = torch.matmul(torch.softmax(s, dim=-1), vr)
+    (o * do.double()).sum().backward()
+
+    mods = dict(causal=True, rel_bias=table, blocks=blk)
+    dq = oracle.attn_bwd_rows(q, k, v, do, scale=0.5, **mods).reshape(B, H, S, D)
+    dk, dv = oracle.attn_bwd_keys(q, k, v, do, scale=0.5, **mods)
+    np.testing.assert_allclose(dq, qd.grad.numpy(), rtol=0, atol=1e-10)
+    np.testing.assert_allclose(dk.reshape(B, Hkv, S, D), kd.grad.numpy(), rtol=0, atol=1e-10)
+    np.testing.assert_allclose(dv.reshape(B, Hkv, S, D), vd.grad.numpy(), rtol=0, atol=1e-10)

@@ -379,3 +379,88 @@ def test_golden_worked_examples(name):
             assert lse[r] == -np.inf
         else:
             assert lse[r] == pytest.approx(_eval_closed_form(e), abs=tol), r
+
+
+# ------------------------------------------- relative-position bias, blocks ---
+
+def rel_table(H, R, seed):
+    g = np.random.default_rng(seed)
+    return g.standard_normal((H, 2 * R + 1)).astype(np.float32).astype(np.float64)
+
+
+def expand_rel(table, S_q, S_k, q_offset=0):
+    """bias[h, i, j] = table[h, clip(j - (i + q_offset), -R, R) + R], built by
+    explicit indexing (independent of the oracle)."""
+    H, W = table.shape
+    R = (W - 1) // 2
+    i = np.arange(S_q)[:, None] + q_offset
+    j = np.arange(S_k)[None, :]
+    idx = np.clip(j - i, -R, R) + R
+    return table[:, idx]
+
+
+def test_rel_bias_with_alibi_table_equals_alibi_exactly():
+    # a table holding m_h * r reproduces ALiBi's -m_h * (qpos - kpos) term for
+    # term (the same products up to sign), so the oracle outputs are identical
+    B, H, S, D = 1, 4, 48, 16
+    q, k, v = rand_qkv(B, H, H, S, S, D, seed=31)
+    R = S
+    m = 2.0 ** (-8.0 * (np.arange(H) + 1) / H)
+    table = m[:, None] * np.arange(-R, R + 1)[None, :]
+    o1, l1 = oracle.attn_rows(q, k, v, scale=0.25, causal=True, alibi=True)
+    o2, l2 = oracle.attn_rows(q, k, v, scale=0.25, causal=True, rel_bias=table)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("R,q_offset,causal", [(3, 0, False), (0, 0, True), (7, 5, True), (40, -3, False)])
+def test_rel_bias_matches_sdpa_additive_mask(R, q_offset, causal):
+    B, H, Sq, Sk, D = 2, 3, 20, 26, 8
+    q, k, v = rand_qkv(B, H, H, Sq, Sk, D, seed=32 + R)
+    table = rel_table(H, R, seed=R)
+    bias = torch.from_numpy(expand_rel(table, Sq, Sk, q_offset))[None]  # [1,H,Sq,Sk]
+    if causal:
+        i = np.arange(Sq)[:, None] + q_offset
+        keep = torch.from_numpy(np.arange(Sk)[None, :] <= i)
+        bias = bias.masked_fill(~keep, float("-inf"))
+    qd, kd, vd = q.double(), k.double(), v.double()
+    sc = f32(0.3)
+    o_ref = F.scaled_dot_product_attention(qd, kd, vd, attn_mask=bias, scale=sc).numpy()
+    s = torch.matmul(qd, kd.transpose(-1, -2)) * sc + bias
+    l_ref = torch.logsumexp(s, dim=-1).numpy()
+    o, l = oracle.attn_rows(q, k, v, scale=0.3, rel_bias=table, q_offset=q_offset, causal=causal)
+    rows_ok = np.isfinite(l_ref.reshape(-1))
+    np.testing.assert_allclose(o[rows_ok], o_ref.reshape(-1, D)[rows_ok], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l[rows_ok], l_ref.reshape(-1)[rows_ok], rtol=0, atol=1e-12)
+
+
+def random_blocks(Bb, S_q, S_k, seed, p=0.6):
+    g = np.random.default_rng(seed)
+    nq, nk = -(-S_q // 128), -(-S_k // 128)
+    return (g.random((Bb, nq, nk)) < p).astype(np.uint8)
+
+
+def test_block_map_matches_sdpa_boolean_mask():
+    B, H, Sq, Sk, D = 2, 2, 300, 400, 8
+    q, k, v = rand_qkv(B, H, H, Sq, Sk, D, seed=40)
+    blk = random_blocks(B, Sq, Sk, seed=41)
+    blk[:, :, 0] = 1  # every row sees some key
+    full = np.stack([np.kron(blk[b], np.ones((128, 128), dtype=np.uint8))[:Sq, :Sk]
+                     for b in range(B)]).astype(bool)
+    causal = np.arange(Sk)[None, :] <= np.arange(Sq)[:, None]
+    mask = torch.from_numpy(full & causal[None])[:, None]
+    o_ref, l_ref = ref_sdpa(q, k, v, f32(0.35), attn_mask=mask)
+    o, l = oracle.attn_rows(q, k, v, scale=0.35, blocks=blk, causal=True)
+    np.testing.assert_allclose(o, o_ref.reshape(-1, D), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l, l_ref.reshape(-1), rtol=0, atol=1e-12)
+    # one map shared by the batch, and an all-ones map that changes nothing
+    o1, l1 = oracle.attn_rows(q, k, v, scale=0.35, blocks=blk[:1], causal=True)
+    full1 = torch.from_numpy(np.kron(blk[0], np.ones((128, 128), dtype=np.uint8))[:Sq, :Sk]
+                             .astype(bool) & causal)[None, None]
+    o_ref1, _ = ref_sdpa(q, k, v, f32(0.35), attn_mask=full1.expand(B, 1, Sq, Sk))
+    np.testing.assert_allclose(o1, o_ref1.reshape(-1, D), rtol=0, atol=1e-12)
+    ones = np.ones_like(blk[:1])
+    o2, l2 = oracle.attn_rows(q, k, v, scale=0.35, blocks=ones, causal=True)
+    o3, l3 = oracle.attn_rows(q, k, v, scale=0.35, causal=True)
+    np.testing.assert_array_equal(o2, o3)
+    np.testing.assert_array_equal(l2, l3)
