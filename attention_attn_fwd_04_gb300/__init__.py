@@ -38,16 +38,17 @@ __all__ = [
     "get_option",
     "status_string",
     "library_path",
-    "MASK_CAUSAL", "MASK_WINDOW", "MASK_DOCUMENT", "MASK_PREFIX_LM",
-    "SCORE_ALIBI", "SCORE_SOFTCAP",
+    "MASK_CAUSAL", "MASK_WINDOW", "MASK_DOCUMENT", "MASK_PREFIX_LM", "MASK_BLOCKS",
+    "SCORE_ALIBI", "SCORE_SOFTCAP", "SCORE_RELBIAS", "BLOCK",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libattn_gb300.so")
 
-MOD_DESC_VERSION = 1
-MASK_CAUSAL, MASK_WINDOW, MASK_DOCUMENT, MASK_PREFIX_LM = 1, 2, 4, 8
-SCORE_ALIBI, SCORE_SOFTCAP = 1, 2
+MOD_DESC_VERSION = 2
+MASK_CAUSAL, MASK_WINDOW, MASK_DOCUMENT, MASK_PREFIX_LM, MASK_BLOCKS = 1, 2, 4, 8, 16
+SCORE_ALIBI, SCORE_SOFTCAP, SCORE_RELBIAS = 1, 2, 4
+BLOCK = 128  # edge of a block-map tile
 
 OPT_RESCALE_THRESHOLD = 1
 OPT_FORCE_PARTIAL = 2
@@ -97,6 +98,10 @@ class ModDesc(ctypes.Structure):
         ("alibi_slopes", ctypes.c_void_p),
         ("block_mask", ctypes.c_void_p),
         ("block_mask_bytes", ctypes.c_size_t),
+        ("blocks", ctypes.c_void_p),
+        ("blocks_batched", ctypes.c_int32),
+        ("rel_max", ctypes.c_int32),
+        ("rel_bias", ctypes.c_void_p),
     ]
 
 
@@ -208,7 +213,8 @@ class BlockMask:
 
 
 def _mod_desc(*, causal=False, window=None, doc_ids=None, prefix_len=None, alibi=False,
-              alibi_slopes=None, softcap=None, q_offset=0, block_mask=None) -> Tuple[ModDesc, tuple]:
+              alibi_slopes=None, softcap=None, q_offset=0, block_mask=None, blocks=None,
+              rel_bias=None) -> Tuple[ModDesc, tuple]:
     m = ModDesc()
     m.version = MOD_DESC_VERSION
     keep = []
@@ -233,6 +239,19 @@ def _mod_desc(*, causal=False, window=None, doc_ids=None, prefix_len=None, alibi
     if softcap is not None and softcap != 0:
         m.score_flags |= SCORE_SOFTCAP
         m.softcap = float(softcap)
+    if blocks is not None:
+        # [B, nQ, nK] (one map per batch entry) or [nQ, nK] / [1, nQ, nK]
+        m.mask_flags |= MASK_BLOCKS
+        m.blocks = _ptr(blocks)
+        m.blocks_batched = 1 if (blocks.dim() == 3 and blocks.shape[0] > 1) else 0
+        keep.append(blocks)
+    if rel_bias is not None:
+        if rel_bias.dim() != 2 or rel_bias.shape[1] % 2 != 1:
+            raise ValueError("rel_bias must be [H, 2R+1]")
+        m.score_flags |= SCORE_RELBIAS
+        m.rel_bias = _ptr(rel_bias)
+        m.rel_max = (rel_bias.shape[1] - 1) // 2
+        keep.append(rel_bias)
     m.q_offset = int(q_offset)
     if block_mask is not None:
         m.block_mask = _ptr(block_mask.buf)
@@ -241,9 +260,10 @@ def _mod_desc(*, causal=False, window=None, doc_ids=None, prefix_len=None, alibi
     return m, tuple(keep)
 
 
-def _check_mask_arrays(device, doc_ids, prefix_len, alibi_slopes):
+def _check_mask_arrays(device, doc_ids, prefix_len, alibi_slopes, blocks=None, rel_bias=None):
     for name, t, dt in (("doc_ids", doc_ids, torch.int32), ("prefix_len", prefix_len, torch.int32),
-                        ("alibi_slopes", alibi_slopes, torch.float32)):
+                        ("alibi_slopes", alibi_slopes, torch.float32),
+                        ("blocks", blocks, torch.uint8), ("rel_bias", rel_bias, torch.float32)):
         if t is None:
             continue
         if t.device != device or t.dtype != dt or not t.is_contiguous():
@@ -260,7 +280,8 @@ def build_block_mask(B: int, H: int, S_q: int, S_k: int, *, device=None,
     """Build the tile classification for a problem on the device.  ``mods``
     take the same keywords as :func:`attn_fwd` (score mods are ignored)."""
     device = torch.device(device if device is not None else "cuda")
-    _check_mask_arrays(device, mods.get("doc_ids"), mods.get("prefix_len"), None)
+    _check_mask_arrays(device, mods.get("doc_ids"), mods.get("prefix_len"), None,
+                       mods.get("blocks"))
     m, keep = _mod_desc(**mods)
     n = int(_lib.attn_block_mask_bytes(B, H, S_q, S_k, ctypes.byref(m)))
     if n == 0:
@@ -287,8 +308,13 @@ def attn_fwd_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.
                   prefix_len: Optional[torch.Tensor] = None, alibi: bool = False,
                   alibi_slopes: Optional[torch.Tensor] = None, softcap: Optional[float] = None,
                   q_offset: int = 0, block_mask: Optional[BlockMask] = None,
+                  blocks: Optional[torch.Tensor] = None,
+                  rel_bias: Optional[torch.Tensor] = None,
                   stream: Optional[torch.cuda.Stream] = None) -> None:
-    """Attention forward into caller-provided ``out`` (and ``lse``)."""
+    """Attention forward into caller-provided ``out`` (and ``lse``).
+    ``blocks``: uint8 block map [B or 1, ceil(S_q/128), ceil(S_k/128)]
+    (0 hides the 128 x 128 tile); ``rel_bias``: float32 [H, 2R+1] added as
+    rel_bias[h, clamp(kpos - qpos, -R, R) + R]."""
     if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
         raise ValueError("q, k, v must be [B, H, S, D]")
     B, H, S_q, D = q.shape
@@ -304,12 +330,13 @@ def attn_fwd_into(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.
     if lse is not None and (lse.device != dev or lse.dtype != torch.float32
                             or not lse.is_contiguous() or tuple(lse.shape) != (B, H, S_q)):
         raise ValueError("lse must be a contiguous float32 [B, H, S_q] tensor on %s" % dev)
-    _check_mask_arrays(dev, doc_ids, prefix_len, alibi_slopes)
+    _check_mask_arrays(dev, doc_ids, prefix_len, alibi_slopes, blocks, rel_bias)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     m, keep = _mod_desc(causal=causal, window=window, doc_ids=doc_ids, prefix_len=prefix_len,
                         alibi=alibi, alibi_slopes=alibi_slopes, softcap=softcap,
-                        q_offset=q_offset, block_mask=block_mask)
+                        q_offset=q_offset, block_mask=block_mask, blocks=blocks,
+                        rel_bias=rel_bias)
     with torch.cuda.device(dev):
         st = _lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), _ptr(lse),
                            B, H, H_kv, S_q, S_k, D, float(scale), ctypes.byref(m),
@@ -351,7 +378,8 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tenso
         if (t.device != dev or t.dtype != dt or not t.is_contiguous()
                 or tuple(t.shape) != shape):
             raise ValueError("%s must be a contiguous %s %s tensor on %s" % (name, dt, shape, dev))
-    _check_mask_arrays(dev, mods.get("doc_ids"), mods.get("prefix_len"), mods.get("alibi_slopes"))
+    _check_mask_arrays(dev, mods.get("doc_ids"), mods.get("prefix_len"), mods.get("alibi_slopes"),
+                       mods.get("blocks"), mods.get("rel_bias"))
     if "block_mask" in mods:
         raise ValueError("attn_bwd builds its own block masks")
     if scale is None:
@@ -404,7 +432,8 @@ def attn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *,
     if lse is not None and (lse.device != cpu or lse.dtype != torch.float32
                             or not lse.is_contiguous() or tuple(lse.shape) != (B, H, S_q)):
         raise ValueError("lse must be a contiguous float32 [B, H, S_q] CPU tensor")
-    _check_mask_arrays(cpu, mods.get("doc_ids"), mods.get("prefix_len"), mods.get("alibi_slopes"))
+    _check_mask_arrays(cpu, mods.get("doc_ids"), mods.get("prefix_len"), mods.get("alibi_slopes"),
+                       mods.get("blocks"), mods.get("rel_bias"))
     if "block_mask" in mods:
         raise ValueError("attn_fwd_host builds its own block mask")
     if scale is None:
@@ -437,7 +466,7 @@ def get_option(name: str) -> float:
     return v.value
 
 
-_HDR_FMT = "<IIiiiiiiiiIiiiiiQQQQQQQii"  # mirrors the device block-mask header
+_HDR_FMT = "<IIiiiiiiiiIiiiiiQQQQQQQiiQQ"  # mirrors the device block-mask header
 
 
 def decode_block_mask(bm: BlockMask) -> dict:
@@ -456,7 +485,7 @@ def decode_block_mask(bm: BlockMask) -> dict:
     keys = ("magic", "version", "B", "S_q", "S_k", "nQ", "nK", "nP", "bm", "n_entries",
             "mask_flags", "window", "q_offset", "force_partial", "uniform", "max_cnt",
             "doc_ptr", "prefix_ptr", "order_off", "cnt_off", "list_off", "total_bytes",
-            "doc_off", "docs_sorted", "pad")
+            "doc_off", "docs_sorted", "pad", "blocks_ptr", "pad2")
     h = dict(zip(keys, f))
     n, nK, nP, nQ = h["n_entries"], h["nK"], h["nP"], h["nQ"]
     order = raw[h["order_off"]:h["order_off"] + 4 * n].view(np.int32).copy()

@@ -4,6 +4,7 @@
 // forward kernel.
 #include <cuda_runtime.h>
 #include <math.h>
+#include <stddef.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -113,15 +114,44 @@ attn_status bwd_scratch(int dev, size_t bytes, void** out) {
   return ATTN_OK;
 }
 
-// Shape and mod checks shared by every entry point.
+// A caller's descriptor as the current layout: a version-1 descriptor is
+// copied up to its end (it has no version-2 fields) and the rest zeroed.
+// Returns nullptr for no descriptor; *st is INVALID_ARG for an unknown
+// version.
+const attn_mod_desc* load_mod(const attn_mod_desc* in, attn_mod_desc* buf, attn_status* st) {
+  *st = ATTN_OK;
+  if (in == nullptr) return nullptr;
+  memset(buf, 0, sizeof(*buf));
+  if (in->version == 1u) {
+    memcpy(buf, in, offsetof(attn_mod_desc, blocks));
+  } else if (in->version == ATTN_MOD_DESC_VERSION) {
+    *buf = *in;
+  } else {
+    *st = ATTN_ERR_INVALID_ARG;
+    return nullptr;
+  }
+  buf->version = ATTN_MOD_DESC_VERSION;
+  return buf;
+}
+
+// The mask flags the kernels see: the caller's, plus the internal bit
+// that makes the block mask per batch entry for a per-batch block map.
+uint32_t kernel_mask_flags(const attn_mod_desc* mod) {
+  if (mod == nullptr) return 0u;
+  uint32_t f = mod->mask_flags;
+  if ((f & ATTN_MASK_BLOCKS) && mod->blocks_batched) f |= kMaskBlocksBatched;
+  return f;
+}
+
+// Shape and mod checks shared by every entry point (on a loaded descriptor).
 attn_status check_problem(int B, int H, int S_q, int S_k, const attn_mod_desc* mod) {
   if (B <= 0 || H <= 0 || S_q <= 0 || S_k <= 0) return ATTN_ERR_INVALID_ARG;
   if (S_q >= (1 << 30) || S_k >= (1 << 30)) return ATTN_ERR_INVALID_ARG;
   if (mod == nullptr) return ATTN_OK;
   if (mod->version != ATTN_MOD_DESC_VERSION) return ATTN_ERR_INVALID_ARG;
-  const uint32_t known_mask =
-      ATTN_MASK_CAUSAL | ATTN_MASK_WINDOW | ATTN_MASK_DOCUMENT | ATTN_MASK_PREFIX_LM;
-  const uint32_t known_score = ATTN_SCORE_ALIBI | ATTN_SCORE_SOFTCAP;
+  const uint32_t known_mask = ATTN_MASK_CAUSAL | ATTN_MASK_WINDOW | ATTN_MASK_DOCUMENT |
+                              ATTN_MASK_PREFIX_LM | ATTN_MASK_BLOCKS;
+  const uint32_t known_score = ATTN_SCORE_ALIBI | ATTN_SCORE_SOFTCAP | ATTN_SCORE_RELBIAS;
   if ((mod->mask_flags & ~known_mask) || (mod->score_flags & ~known_score))
     return ATTN_ERR_INVALID_ARG;
   if (mod->q_offset <= -(1 << 30) || mod->q_offset >= (1 << 30)) return ATTN_ERR_INVALID_ARG;
@@ -138,6 +168,13 @@ attn_status check_problem(int B, int H, int S_q, int S_k, const attn_mod_desc* m
   if ((mod->score_flags & ATTN_SCORE_ALIBI) && mod->alibi_slopes != nullptr &&
       !aligned(mod->alibi_slopes, 4))
     return ATTN_ERR_INVALID_ARG;
+  if ((mod->mask_flags & ATTN_MASK_BLOCKS) &&
+      (mod->blocks == nullptr || (mod->blocks_batched != 0 && mod->blocks_batched != 1)))
+    return ATTN_ERR_INVALID_ARG;
+  if ((mod->score_flags & ATTN_SCORE_RELBIAS) &&
+      (mod->rel_bias == nullptr || !aligned(mod->rel_bias, 4) || mod->rel_max < 0 ||
+       mod->rel_max >= (1 << 30)))
+    return ATTN_ERR_INVALID_ARG;
   return ATTN_OK;
 }
 
@@ -147,11 +184,12 @@ MaskParams mask_params(int S_q, int S_k, const attn_mod_desc* mod) {
   mp.S_q = S_q;
   mp.S_k = S_k;
   if (mod != nullptr) {
-    mp.flags = mod->mask_flags;
+    mp.flags = kernel_mask_flags(mod);
     mp.window = (mod->mask_flags & ATTN_MASK_WINDOW) ? mod->window : 0;
     mp.q_offset = mod->q_offset;
     mp.doc_ids = (mod->mask_flags & ATTN_MASK_DOCUMENT) ? mod->doc_ids : nullptr;
     mp.prefix_len = (mod->mask_flags & ATTN_MASK_PREFIX_LM) ? mod->prefix_len : nullptr;
+    mp.blocks = (mod->mask_flags & ATTN_MASK_BLOCKS) ? mod->blocks : nullptr;
   }
   return mp;
 }
@@ -226,6 +264,10 @@ attn_status enqueue_forward(const void* q, const void* k, const void* v, void* o
   a.score_flags = mod ? mod->score_flags : 0u;
   a.softcap = mod ? mod->softcap : 0.f;
   a.alibi_slopes = (mod && (mod->score_flags & ATTN_SCORE_ALIBI)) ? mod->alibi_slopes : nullptr;
+  if (mod && (mod->score_flags & ATTN_SCORE_RELBIAS)) {
+    a.rel_bias = mod->rel_bias;
+    a.rel_max = mod->rel_max;
+  }
   a.block_mask = bmask;
   a.n_entries = g.n_entries;
   a.bm = g.bm;
@@ -325,7 +367,8 @@ attn_status host_pipe(int dev, HostPipe** out) {
 
 // Byte offsets of one call's device copies inside a slot.
 struct HostLayout {
-  size_t q, k, v, o, lse, doc, prefix, slopes, mask, total;
+  size_t q, k, v, o, lse, doc, prefix, slopes, blocks, rel, mask, total;
+  size_t blocks_bytes, rel_bytes;
 };
 HostLayout host_layout(int B, int H, int H_kv, int S_q, int S_k, int D, const attn_mod_desc* mod) {
   HostLayout l;
@@ -344,7 +387,15 @@ HostLayout host_layout(int B, int H, int H_kv, int S_q, int S_k, int D, const at
   l.doc = take((size_t)B * S_k * 4);
   l.prefix = take((size_t)B * 4);
   l.slopes = take((size_t)H * 4);
-  l.mask = take(block_mask_geom(1, S_q, S_k, mod ? mod->mask_flags : 0u).total);  // one batch entry
+  l.blocks_bytes = l.rel_bytes = 0;
+  if (mod != nullptr && (mod->mask_flags & ATTN_MASK_BLOCKS))
+    l.blocks_bytes = (size_t)(mod->blocks_batched ? B : 1) * ((S_q + kTileM - 1) / kTileM) *
+                     ((S_k + kTileN - 1) / kTileN);
+  if (mod != nullptr && (mod->score_flags & ATTN_SCORE_RELBIAS))
+    l.rel_bytes = (size_t)H * (2 * (size_t)mod->rel_max + 1) * 4;
+  l.blocks = take(l.blocks_bytes);
+  l.rel = take(l.rel_bytes);
+  l.mask = take(block_mask_geom(1, S_q, S_k, kernel_mask_flags(mod) & ~kMaskBlocksBatched).total);  // one batch entry
   l.total = at;
   return l;
 }
@@ -450,17 +501,25 @@ attn_status attn_get_option(attn_option opt, double* value) {
   return ATTN_ERR_INVALID_ARG;
 }
 
-size_t attn_block_mask_bytes(int B, int H, int S_q, int S_k, const attn_mod_desc* mod) {
+size_t attn_block_mask_bytes(int B, int H, int S_q, int S_k, const attn_mod_desc* mod_in) {
+  attn_mod_desc mod_buf;
+  attn_status lst;
+  const attn_mod_desc* mod = load_mod(mod_in, &mod_buf, &lst);
+  if (lst != ATTN_OK) return 0;
   if (check_problem(B, H, S_q, S_k, mod) != ATTN_OK) return 0;
-  return block_mask_geom(B, S_q, S_k, mod ? mod->mask_flags : 0u).total;
+  return block_mask_geom(B, S_q, S_k, kernel_mask_flags(mod)).total;
 }
 
-attn_status attn_build_block_mask(int B, int H, int S_q, int S_k, const attn_mod_desc* mod,
+attn_status attn_build_block_mask(int B, int H, int S_q, int S_k, const attn_mod_desc* mod_in,
                                   void* dst, size_t bytes, attn_stream_t stream) {
+  attn_mod_desc mod_buf;
+  attn_status lst;
+  const attn_mod_desc* mod = load_mod(mod_in, &mod_buf, &lst);
+  if (lst != ATTN_OK) return lst;
   attn_status st = check_problem(B, H, S_q, S_k, mod);
   if (st != ATTN_OK) return st;
   if (dst == nullptr || !aligned(dst, 16)) return ATTN_ERR_INVALID_ARG;
-  const size_t need = block_mask_geom(B, S_q, S_k, mod ? mod->mask_flags : 0u).total;
+  const size_t need = block_mask_geom(B, S_q, S_k, kernel_mask_flags(mod)).total;
   if (bytes < need) return ATTN_ERR_INVALID_ARG;
   const Options o = options_snapshot();
   cudaError_t err = launch_build_block_mask(B, S_q, S_k, mask_params(S_q, S_k, mod),
@@ -529,13 +588,17 @@ attn_status attn_get_device_status(attn_stream_t stream) {
 
 attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B,
                      int H, int H_kv, int S_q, int S_k, int D, float scale,
-                     const attn_mod_desc* mod, attn_stream_t stream) {
+                     const attn_mod_desc* mod_in, attn_stream_t stream) {
+  attn_mod_desc mod_buf;
+  attn_status lst;
+  const attn_mod_desc* mod = load_mod(mod_in, &mod_buf, &lst);
+  if (lst != ATTN_OK) return lst;
   // ---- host-side validation: nothing is enqueued on failure ------------
   attn_status st = check_problem(B, H, S_q, S_k, mod);
   if (st != ATTN_OK) return st;
   st = check_device_tensors(q, k, v, out, lse, B, H, H_kv, S_q, S_k, D, scale);
   if (st != ATTN_OK) return st;
-  const uint32_t mflags = mod ? mod->mask_flags : 0u;
+  const uint32_t mflags = kernel_mask_flags(mod);
   const BlockMaskGeom g = block_mask_geom(B, S_q, S_k, mflags);
   if (mod != nullptr && mod->block_mask != nullptr &&
       (!aligned(mod->block_mask, 16) || mod->block_mask_bytes < g.total))
@@ -559,7 +622,11 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, flo
 
 attn_status attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse,
                              int B, int H, int H_kv, int S_q, int S_k, int D, float scale,
-                             const attn_mod_desc* mod, attn_stream_t stream) {
+                             const attn_mod_desc* mod_in, attn_stream_t stream) {
+  attn_mod_desc mod_buf;
+  attn_status lst;
+  const attn_mod_desc* mod = load_mod(mod_in, &mod_buf, &lst);
+  if (lst != ATTN_OK) return lst;
   // ---- host-side validation (same rules as attn_fwd) -----------------------
   attn_status st = check_problem(B, H, S_q, S_k, mod);
   if (st != ATTN_OK) return st;
@@ -567,7 +634,7 @@ attn_status attn_fwd_noalloc(const void* q, const void* k, const void* v, void* 
   if (st != ATTN_OK) return st;
   // The block mask is always built into the fixed scratch array.
   if (mod != nullptr && mod->block_mask != nullptr) return ATTN_ERR_INVALID_ARG;
-  const uint32_t mflags = mod ? mod->mask_flags : 0u;
+  const uint32_t mflags = kernel_mask_flags(mod);
   const BlockMaskGeom g = block_mask_geom(B, S_q, S_k, mflags);
   if (g.total > ATTN_NOALLOC_SCRATCH_BYTES - kNoAllocStatusBytes) return ATTN_ERR_UNSUPPORTED;
 
@@ -588,7 +655,11 @@ attn_status attn_fwd_noalloc(const void* q, const void* k, const void* v, void* 
 
 attn_status attn_fwd_host(const void* q, const void* k, const void* v, void* out, float* lse,
                           int B, int H, int H_kv, int S_q, int S_k, int D, float scale,
-                          const attn_mod_desc* mod, attn_stream_t stream) {
+                          const attn_mod_desc* mod_in, attn_stream_t stream) {
+  attn_mod_desc mod_buf;
+  attn_status lst;
+  const attn_mod_desc* mod = load_mod(mod_in, &mod_buf, &lst);
+  if (lst != ATTN_OK) return lst;
   // ---- host-side validation: nothing is enqueued on failure --------------
   attn_status st = check_problem(B, H, S_q, S_k, mod);
   if (st != ATTN_OK) return st;
@@ -614,7 +685,7 @@ attn_status attn_fwd_host(const void* q, const void* k, const void* v, void* out
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   char* base = static_cast<char*>(slot.buf);
   auto ck = [](cudaError_t e) { return e == cudaSuccess; };
-  const uint32_t mflags = mod ? mod->mask_flags : 0u;
+  const uint32_t mflags = kernel_mask_flags(mod);
   const uint32_t sflags = mod ? mod->score_flags : 0u;
   const int group = H / H_kv;
   const size_t q_head = (size_t)S_q * D * 2, k_head = (size_t)S_k * D * 2;
@@ -633,6 +704,12 @@ attn_status attn_fwd_host(const void* q, const void* k, const void* v, void* out
   if (ok && alibi && mod->alibi_slopes != nullptr)
     ok = ck(cudaMemcpyAsync(base + lay.slopes, mod->alibi_slopes, (size_t)H * 4,
                             cudaMemcpyHostToDevice, pipe->h2d));
+  if (ok && lay.blocks_bytes)
+    ok = ck(cudaMemcpyAsync(base + lay.blocks, mod->blocks, lay.blocks_bytes,
+                            cudaMemcpyHostToDevice, pipe->h2d));
+  if (ok && lay.rel_bytes)
+    ok = ck(cudaMemcpyAsync(base + lay.rel, mod->rel_bias, lay.rel_bytes, cudaMemcpyHostToDevice,
+                            pipe->h2d));
   if (!ok) return ATTN_ERR_CUDA;
   // Slices of heads run as separate forwards, so the default ALiBi slopes
   // (which depend on the head's index among all H) are written out once.
@@ -647,7 +724,8 @@ attn_status attn_fwd_host(const void* q, const void* k, const void* v, void* out
   // bounds this path; about eight chunks hide nearly all of the compute.
   const int units = B * H_kv;
   const int per = (units + kHostChunks - 1) / kHostChunks;  // K/V heads per chunk
-  const bool mask_per_batch = (mflags & (ATTN_MASK_DOCUMENT | ATTN_MASK_PREFIX_LM)) != 0;
+  const bool per_batch = mask_per_batch(mflags);
+  const size_t map_bytes = (size_t)((S_q + kTileM - 1) / kTileM) * ((S_k + kTileN - 1) / kTileN);
   int mask_b = -1;  // batch entry whose block mask is in the slot
   for (int b = 0; b < B && ok; ++b) {
     for (int kv0 = 0; kv0 < H_kv && ok; kv0 += per) {
@@ -677,10 +755,18 @@ attn_status attn_fwd_host(const void* q, const void* k, const void* v, void* out
       if (mflags & ATTN_MASK_PREFIX_LM)
         cm.prefix_len = reinterpret_cast<const int32_t*>(base + lay.prefix) + b;
       if (alibi) cm.alibi_slopes = dslopes + (size_t)kv0 * group;
+      if (mflags & ATTN_MASK_BLOCKS) {  // batch b's map (one batch entry here)
+        cm.blocks = reinterpret_cast<const uint8_t*>(base + lay.blocks) +
+                    (mod->blocks_batched ? (size_t)b * map_bytes : 0);
+        cm.blocks_batched = 0;
+      }
+      if (sflags & ATTN_SCORE_RELBIAS)
+        cm.rel_bias = reinterpret_cast<const float*>(base + lay.rel) +
+                      (size_t)kv0 * group * (2 * (size_t)mod->rel_max + 1);
       // one block mask per batch entry (or one for all when the mask does
       // not depend on the batch); the stream orders each rebuild after the
       // forwards that read the previous one
-      const int want_b = mask_per_batch ? b : 0;
+      const int want_b = per_batch ? b : 0;
       if (mask_b != want_b) {
         const Options o = options_snapshot();
         if (launch_build_block_mask(1, S_q, S_k, mask_params(S_q, S_k, &cm),
@@ -714,7 +800,11 @@ attn_status attn_fwd_host(const void* q, const void* k, const void* v, void* out
 attn_status attn_bwd(const void* q, const void* k, const void* v, const void* out,
                      const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
                      int H, int H_kv, int S_q, int S_k, int D, float scale,
-                     const attn_mod_desc* mod, attn_stream_t stream) {
+                     const attn_mod_desc* mod_in, attn_stream_t stream) {
+  attn_mod_desc mod_buf;
+  attn_status lst;
+  const attn_mod_desc* mod = load_mod(mod_in, &mod_buf, &lst);
+  if (lst != ATTN_OK) return lst;
   // ---- host-side validation: nothing is enqueued on failure --------------
   attn_status st = check_problem(B, H, S_q, S_k, mod);
   if (st != ATTN_OK) return st;
@@ -745,7 +835,7 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* ou
   DeviceScratch* scr = nullptr;
   st = scratch_for(dev, &scr);
   if (st != ATTN_OK) return st;
-  const uint32_t mflags = mod ? mod->mask_flags : 0u;
+  const uint32_t mflags = kernel_mask_flags(mod);
   const BlockMaskGeom g = block_mask_geom(B, S_q, S_k, mflags);
   const BlockMaskTGeom gt = block_mask_t_geom(B, S_q, S_k, mflags);
   const size_t off_t = align_up(g.total, 256);
@@ -783,6 +873,10 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* ou
   a.score_flags = mod ? mod->score_flags : 0u;
   a.softcap = mod ? mod->softcap : 0.f;
   a.alibi_slopes = (mod && (mod->score_flags & ATTN_SCORE_ALIBI)) ? mod->alibi_slopes : nullptr;
+  if (mod && (mod->score_flags & ATTN_SCORE_RELBIAS)) {
+    a.rel_bias = mod->rel_bias;
+    a.rel_max = mod->rel_max;
+  }
   a.block_mask = base;
   a.block_mask_t = base + off_t;
   a.rowstat = reinterpret_cast<float*>(base + off_r);

@@ -101,6 +101,9 @@ struct BParams {
   const int32_t* doc_lo;
   const int32_t* doc_hi;
   const float* alibi_slopes;
+  int alibi_on;           // the ALiBi variant also serves a bias table alone
+  const float* rel_bias;  // [H][2 rel_max + 1], or null
+  int rel_max;
   const BlockMaskHeader* hdr;
   const int32_t* cnt;      // forward block mask: per query-tile pair
   const uint32_t* list;
@@ -218,11 +221,32 @@ __device__ __forceinline__ ScoreMod make_mod(const BParams& p, int h) {
   m.capl2 = p.softcap * kBLog2e;
   m.slope2 = 0.f;
   if constexpr (ALIBI) {
-    const float mh =
-        p.alibi_slopes ? p.alibi_slopes[h] : exp2f(-8.0f * (float)(h + 1) / (float)p.H);
-    m.slope2 = SOFTCAP ? mh * (2.0f * kBLog2e / p.softcap) : mh * kBLog2e;
+    if (p.alibi_on) {
+      const float mh =
+          p.alibi_slopes ? p.alibi_slopes[h] : exp2f(-8.0f * (float)(h + 1) / (float)p.H);
+      m.slope2 = SOFTCAP ? mh * (2.0f * kBLog2e / p.softcap) : mh * kBLog2e;
+    }
   }
   return m;
+}
+
+// Adds the relative-position bias of head h to raw scores tv[0..127] whose
+// relative positions (kpos - qpos) are pos0 + step * c, pre-divided by the
+// score scale so that score_t applies it as table * (units of t); a
+// uniform branch around its own loop keeps the other loops branch-free.
+template <bool ALIBI, bool SOFTCAP>
+__device__ __forceinline__ void add_rel_bias(float (&tv)[128], const BParams& p, int h, int pos0,
+                                             int step, const ScoreMod& m) {
+  if constexpr (ALIBI) {
+    if (p.rel_bias == nullptr) return;
+    const float* row = p.rel_bias + (size_t)h * (2 * (size_t)p.rel_max + 1);
+    const float rs = (SOFTCAP ? 2.0f * kBLog2e / p.softcap : kBLog2e) / m.sc;
+#pragma unroll
+    for (int c = 0; c < 128; ++c) {
+      const int r = min(max(pos0 + step * c, -p.rel_max), p.rel_max);
+      tv[c] = fmaf(__ldg(row + r + p.rel_max), rs, tv[c]);
+    }
+  }
 }
 
 // Visible key interval of query row i (forward orientation).
@@ -560,12 +584,14 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
           }
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const int c0 = 64 * hh + c;
-            tv[c0] = score_t<ALIBI, SOFTCAP>(__uint_as_float(ra[c]), (float)(j0 + c0 - qpos), md);
-            tv[c0 + 32] =
-                score_t<ALIBI, SOFTCAP>(__uint_as_float(rb[c]), (float)(j0 + c0 + 32 - qpos), md);
+            tv[64 * hh + c] = __uint_as_float(ra[c]);
+            tv[64 * hh + 32 + c] = __uint_as_float(rb[c]);
           }
         }
+        add_rel_bias<ALIBI, SOFTCAP>(tv, p, it.h, j0 - qpos, 1, md);
+#pragma unroll
+        for (int c = 0; c < kTileN; ++c)
+          tv[c] = score_t<ALIBI, SOFTCAP>(tv[c], (float)(j0 + c - qpos), md);
         if (cls == kPartial) {
           const int clo = lo - j0, chi = hi - j0;
           if (has_doc) {
@@ -915,11 +941,13 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
             ptx::tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-              const int c0 = 64 * hh + c;
-              tv[c0] = score_t<ALIBI, SOFTCAP>(__uint_as_float(ra[c]), jb - (float)c0, md);
-              tv[c0 + 32] = score_t<ALIBI, SOFTCAP>(__uint_as_float(rb[c]), jb - (float)(c0 + 32), md);
+              tv[64 * hh + c] = __uint_as_float(ra[c]);
+              tv[64 * hh + 32 + c] = __uint_as_float(rb[c]);
             }
           }
+          add_rel_bias<ALIBI, SOFTCAP>(tv, p, h, j - (i0 + p.q_offset), -1, md);
+#pragma unroll
+          for (int c = 0; c < kTileM; ++c) tv[c] = score_t<ALIBI, SOFTCAP>(tv[c], jb - (float)c, md);
           // the mask in a loop of its own (rows beyond S_k see nothing)
           if (!valid || cls == kPartial) {
             const int clo = ilo - i0, chi = ihi - i0;
@@ -1148,6 +1176,9 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
   bp.doc_ids = a.mask.doc_ids;
   bp.prefix_len = a.mask.prefix_len;
   bp.alibi_slopes = a.alibi_slopes;
+  bp.alibi_on = (a.score_flags & ATTN_SCORE_ALIBI) ? 1 : 0;
+  bp.rel_bias = (a.score_flags & ATTN_SCORE_RELBIAS) ? a.rel_bias : nullptr;
+  bp.rel_max = a.rel_max;
   const char* base = reinterpret_cast<const char*>(a.block_mask);
   bp.hdr = reinterpret_cast<const BlockMaskHeader*>(base);
   bp.cnt = reinterpret_cast<const int32_t*>(base + g.cnt_off);
@@ -1188,7 +1219,7 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return cudaErrorUnknown;
-  const bool alibi = (a.score_flags & ATTN_SCORE_ALIBI) != 0;
+  const bool alibi = (a.score_flags & (ATTN_SCORE_ALIBI | ATTN_SCORE_RELBIAS)) != 0;
   const bool softcap = (a.score_flags & ATTN_SCORE_SOFTCAP) != 0;
   if (a.D == 64) return launch_bwd_d<64>(bp, alibi, softcap, sms, stream);
   return launch_bwd_d<128>(bp, alibi, softcap, sms, stream);

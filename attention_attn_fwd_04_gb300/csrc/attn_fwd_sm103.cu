@@ -108,6 +108,10 @@ struct KParams {
   const int32_t* doc_ids;
   const int32_t* prefix_len;
   const float* alibi_slopes;
+  int alibi_on;           // the BIAS variant also serves a bias table alone
+  const float* rel_bias;  // [H][2 rel_max + 1], or null
+  int rel_max;
+  const uint8_t* blocks;  // user block map the mask was built from (header check)
   float softcap;
   const BlockMaskHeader* hdr;
   const int32_t* order;
@@ -259,7 +263,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                       (!(p.mask_flags & ATTN_MASK_WINDOW) || hdr->window == p.window) &&
                       hdr->q_offset == p.q_offset &&
                       hdr->doc_ptr == reinterpret_cast<uint64_t>(p.doc_ids) &&
-                      hdr->prefix_ptr == reinterpret_cast<uint64_t>(p.prefix_len);
+                      hdr->prefix_ptr == reinterpret_cast<uint64_t>(p.prefix_len) &&
+                      hdr->blocks_ptr == reinterpret_cast<uint64_t>(p.blocks);
   if (!hdr_ok) {
     if (threadIdx.x == 0 && atomicCAS(&p.status->code, 0, ATTN_ERR_DEVICE_CHECK) == 0) {
       p.status->where = kSiteHeader;
@@ -589,10 +594,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const int doc_i = (has_doc && valid) ? doc_b[i] : 0;
       float slope2 = 0.f;  // ALiBi slope in the units of the transformed score
       if constexpr (ALIBI) {
-        float m = p.alibi_slopes ? p.alibi_slopes[it.h]
-                                 : exp2f(-8.0f * (float)(it.h + 1) / (float)p.H);
-        slope2 = SOFTCAP ? m * (2.0f * kLog2e / p.softcap) : m * kLog2e;
+        if (p.alibi_on) {
+          float m = p.alibi_slopes ? p.alibi_slopes[it.h]
+                                   : exp2f(-8.0f * (float)(it.h + 1) / (float)p.H);
+          slope2 = SOFTCAP ? m * (2.0f * kLog2e / p.softcap) : m * kLog2e;
+        }
       }
+      // relative-position bias table row of this head, and its factor to
+      // the units of the transformed score
+      const float* relrow =
+          p.rel_bias ? p.rel_bias + (size_t)it.h * (2 * (size_t)p.rel_max + 1) : nullptr;
+      const float rel_scale = SOFTCAP ? 2.0f * kLog2e / p.softcap : kLog2e;
       // Score transform coefficients.
       //   plain:   t = s * scale * log2(e)             (folded into the exp)
       //   ALiBi:   t = s * scale * log2(e) + slope2 * (j - qpos)
@@ -652,6 +664,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             }
           }
           // score mods
+          if constexpr (ALIBI) {
+            // relative-position bias (a uniform branch around a loop of its
+            // own, so the loops stay branch-free): scaled so that it adds
+            // table * rel_scale to s * sc below
+            if (relrow != nullptr) {
+              const float rs = rel_scale / sc;
+#pragma unroll
+              for (int c = 0; c < kTileN; ++c) {
+                const int r = min(max(j0 + c - qpos, -p.rel_max), p.rel_max);
+                tv[c] = fmaf(__ldg(relrow + r + p.rel_max), rs, tv[c]);
+              }
+            }
+          }
           if constexpr (ALIBI || SOFTCAP) {
             // paired fp32 instructions, two columns at a time
             const float b0 = ALIBI ? slope2 * (float)(j0 - qpos) : 0.f;
@@ -950,6 +975,10 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
   kp.doc_ids = a.mask.doc_ids;
   kp.prefix_len = a.mask.prefix_len;
   kp.alibi_slopes = a.alibi_slopes;
+  kp.alibi_on = (a.score_flags & ATTN_SCORE_ALIBI) ? 1 : 0;
+  kp.rel_bias = (a.score_flags & ATTN_SCORE_RELBIAS) ? a.rel_bias : nullptr;
+  kp.rel_max = a.rel_max;
+  kp.blocks = a.mask.blocks;
   kp.softcap = (a.score_flags & ATTN_SCORE_SOFTCAP) ? a.softcap : 0.f;
   const char* base = reinterpret_cast<const char*>(a.block_mask);
   kp.hdr = reinterpret_cast<const BlockMaskHeader*>(base);
@@ -982,7 +1011,8 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
   if (grid > kp.n_items) grid = kp.n_items;
   if (grid < 1) grid = 1;
 
-  const bool alibi = (a.score_flags & ATTN_SCORE_ALIBI) != 0;
+  // ALiBi and the bias table share one variant (additive position biases)
+  const bool alibi = (a.score_flags & (ATTN_SCORE_ALIBI | ATTN_SCORE_RELBIAS)) != 0;
   const bool softcap = (a.score_flags & ATTN_SCORE_SOFTCAP) != 0;
   if (a.D == 128) return launch_d<128>(kp, alibi, softcap, grid, stream);
   if (a.D == 64) return launch_d<64>(kp, alibi, softcap, grid, stream);

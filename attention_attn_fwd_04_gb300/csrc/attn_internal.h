@@ -52,6 +52,8 @@ struct BlockMaskHeader {
   uint64_t doc_off;         // DOCUMENT: int32 doc_lo[bm][S_k], doc_hi[bm][S_k]
   int32_t docs_sorted;      // 1: every batch's doc ids are non-decreasing
   int32_t pad_;
+  uint64_t blocks_ptr;      // BLOCKS: the block map the mask was built from
+  uint64_t pad2_;
 };
 static_assert(sizeof(BlockMaskHeader) % 16 == 0, "header alignment");
 
@@ -70,12 +72,19 @@ constexpr int kDocPrepTokens = 1024;
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Internal mask-flag bit (never accepted from callers): the user block map
+// has one map per batch entry, so the block mask depends on the batch.
+constexpr uint32_t kMaskBlocksBatched = 1u << 31;
+inline bool mask_per_batch(uint32_t mask_flags) {
+  return (mask_flags & (ATTN_MASK_DOCUMENT | ATTN_MASK_PREFIX_LM | kMaskBlocksBatched)) != 0;
+}
+
 inline BlockMaskGeom block_mask_geom(int B, int S_q, int S_k, uint32_t mask_flags) {
   BlockMaskGeom g;
   g.nQ = (S_q + kTileM - 1) / kTileM;
   g.nK = (S_k + kTileN - 1) / kTileN;
   g.nP = (g.nQ + kTilesPerItem - 1) / kTilesPerItem;
-  g.bm = (mask_flags & (ATTN_MASK_DOCUMENT | ATTN_MASK_PREFIX_LM)) ? B : 1;
+  g.bm = mask_per_batch(mask_flags) ? B : 1;
   g.n_entries = g.bm * g.nP;
   g.order_off = align_up(sizeof(BlockMaskHeader), 16);
   g.cnt_off = align_up(g.order_off + sizeof(int32_t) * (size_t)g.n_entries, 16);
@@ -108,7 +117,7 @@ inline BlockMaskTGeom block_mask_t_geom(int B, int S_q, int S_k, uint32_t mask_f
   BlockMaskTGeom g;
   g.nQ = (S_q + kTileM - 1) / kTileM;
   g.nK = (S_k + kTileN - 1) / kTileN;
-  g.bm = (mask_flags & (ATTN_MASK_DOCUMENT | ATTN_MASK_PREFIX_LM)) ? B : 1;
+  g.bm = mask_per_batch(mask_flags) ? B : 1;
   g.n_entries = g.bm * g.nK;
   g.list_off = align_up(sizeof(int32_t) * (size_t)g.n_entries, 16);
   g.total = align_up(g.list_off + sizeof(uint32_t) * (size_t)g.n_entries * (size_t)g.nQ, 16);
@@ -123,6 +132,7 @@ struct MaskParams {
   int32_t S_q, S_k;
   const int32_t* doc_ids;     // [B][S_k]
   const int32_t* prefix_len;  // [B]
+  const uint8_t* blocks;      // [B or 1][nQ][nK] (flags & ATTN_MASK_BLOCKS)
 };
 
 // Status codes the device writes (first error wins).
@@ -155,6 +165,8 @@ struct FwdArgs {
   uint32_t score_flags;
   float softcap;
   const float* alibi_slopes;
+  const float* rel_bias;       // [H][2 rel_max + 1] (score_flags & ATTN_SCORE_RELBIAS)
+  int rel_max;
   const void* block_mask;      // device, built for this call
   int n_entries;
   int bm;
@@ -186,6 +198,8 @@ struct BwdArgs {
   uint32_t score_flags;
   float softcap;
   const float* alibi_slopes;
+  const float* rel_bias;
+  int rel_max;
   const void* block_mask;    // forward block mask, built for this call
   const void* block_mask_t;  // transposed block mask, built for this call
   float* rowstat;            // scratch: [2][B*H][nQ*128] (LSE in log2 units, dO . O)

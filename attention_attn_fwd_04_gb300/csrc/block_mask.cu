@@ -67,6 +67,15 @@ __device__ __forceinline__ bool row_meets(long long i, long long pl, int c0, int
 // Documents (dq/dk: id ranges of the rows and of the keys) are then applied
 // conservatively: EMPTY when the ranges do not meet, FULL only when both are
 // one and the same document.
+// The user block map's verdict on tile (qt, kt) of mask batch bb: false
+// hides the whole tile.
+__device__ __forceinline__ bool block_open(const MaskParams& mp, int bb, int qt, int kt, int nQ,
+                                           int nK) {
+  if (!(mp.flags & ATTN_MASK_BLOCKS)) return true;
+  const size_t mb = (mp.flags & kMaskBlocksBatched) ? (size_t)bb : 0;
+  return mp.blocks[(mb * nQ + qt) * nK + kt] != 0;
+}
+
 __device__ uint32_t classify_tile(int r0, int r1, int c0, long long pl, const MaskParams& mp,
                                   Range dq, Range dk) {
   if (r0 > r1) return kEmpty;  // no valid query row
@@ -138,8 +147,12 @@ __global__ void __launch_bounds__(kClassifyThreads) classify_kernel(BlockMaskHea
       const int kt = nK - 1 - idx;
       const int c0 = kt * kTileN;
       const Range dk = docs ? Range{t_lo[kt], t_hi[kt]} : Range{0, 0};
-      uint32_t c_0 = classify_tile(r0[0], r1[0], c0, pl, mp, dq[0], dk);
-      uint32_t c_1 = classify_tile(r0[1], r1[1], c0, pl, mp, dq[1], dk);
+      uint32_t c_0 = block_open(mp, bb, 2 * p, kt, nQ, nK)
+                         ? classify_tile(r0[0], r1[0], c0, pl, mp, dq[0], dk)
+                         : kEmpty;
+      uint32_t c_1 = (2 * p + 1 < nQ && block_open(mp, bb, 2 * p + 1, kt, nQ, nK))
+                         ? classify_tile(r0[1], r1[1], c0, pl, mp, dq[1], dk)
+                         : kEmpty;
       if (force_partial) {
         if (c_0 == kFull) c_0 = kPartial;
         if (c_1 == kFull) c_1 = kPartial;
@@ -197,7 +210,9 @@ __global__ void __launch_bounds__(kClassifyThreads) classify_t_kernel(char* dst_
     if (qt < gt.nQ) {
       const int r0 = qt * kTileM, r1 = min(r0 + kTileM - 1, mp.S_q - 1);
       const Range dq = docs ? Range{t_lo[qt], t_hi[qt]} : Range{0, 0};
-      uint32_t c = classify_tile(r0, r1, c0, pl, mp, dq, dk);
+      uint32_t c = block_open(mp, bb, qt, kt, gt.nQ, gt.nK)
+                       ? classify_tile(r0, r1, c0, pl, mp, dq, dk)
+                       : kEmpty;
       if (force_partial && c == kFull) c = kPartial;
       keep = c != kEmpty;
       entry = (uint32_t)qt | (c << 24);
@@ -384,6 +399,8 @@ __global__ void __launch_bounds__(kBuildThreads) order_kernel(BlockMaskHeader* h
     h.doc_off = g.doc_off;
     h.docs_sorted = (g.flag_off != 0 && !disorder) ? 1 : 0;
     h.pad_ = 0;
+    h.blocks_ptr = reinterpret_cast<uint64_t>(mp.blocks);
+    h.pad2_ = 0;
     *hdr = h;
   }
 }

@@ -70,7 +70,10 @@ typedef enum attn_status {
     ATTN_ERR_DEVICE_CHECK = 5  /* a device-side consistency check failed     */
 } attn_status;
 
-#define ATTN_MOD_DESC_VERSION 1u
+/* Descriptor layout version.  Version 2 appended the block-map and
+ * relative-position-bias fields; a version-1 descriptor (without them) is
+ * still accepted and reads as if those fields were zero. */
+#define ATTN_MOD_DESC_VERSION 2u
 
 /* Mask modifications.  Enabled masks are combined with AND.  With
  * qpos = i + q_offset for query row i and kpos = j for key j:
@@ -82,28 +85,39 @@ typedef enum attn_status {
  *   PREFIX_LM  key visible iff kpos <= qpos or kpos < prefix_len[b]
  *              (already causal outside the prefix; combining it with
  *              CAUSAL gives plain causal)
+ *   BLOCKS     key visible iff blocks[b'][i / 128][j / 128] != 0, a user
+ *              block map over 128 x 128 tiles (b' = b when blocks_batched,
+ *              else 0): block-sparse attention
  * A row that sees no key gets O = 0 and LSE = -inf. */
 enum {
     ATTN_MASK_CAUSAL = 1u,
     ATTN_MASK_WINDOW = 2u,
     ATTN_MASK_DOCUMENT = 4u,
-    ATTN_MASK_PREFIX_LM = 8u
+    ATTN_MASK_PREFIX_LM = 8u,
+    ATTN_MASK_BLOCKS = 16u
 };
+
+/* Edge of a block-map tile, in query rows and keys. */
+#define ATTN_BLOCK 128
 
 /* Score modifications, applied after the scale in this order:
  *   ALIBI    s += -m_h * (qpos - kpos), with m_h = alibi_slopes[h] or, when
  *            alibi_slopes is NULL, m_h = 2^(-8 (h + 1) / H) for 0-based
  *            query head h;
+ *   RELBIAS  s += rel_bias[h][clamp(kpos - qpos, -R, R) + R] with
+ *            R = rel_max: a learned relative-position bias table per head;
  *   SOFTCAP  s = softcap * tanh(s / softcap). */
 enum {
     ATTN_SCORE_ALIBI = 1u,
-    ATTN_SCORE_SOFTCAP = 2u
+    ATTN_SCORE_SOFTCAP = 2u,
+    ATTN_SCORE_RELBIAS = 4u
 };
 
 /* Fixed descriptor of score and mask modifications (replaces a JIT).
  * Zero-initialise it, set `version`, then the fields the flags use. */
 typedef struct attn_mod_desc {
-    uint32_t version;          /* ATTN_MOD_DESC_VERSION, else INVALID_ARG   */
+    uint32_t version;          /* 1 or ATTN_MOD_DESC_VERSION (2), else
+                                  INVALID_ARG                                */
     uint32_t mask_flags;       /* ATTN_MASK_* bits                           */
     uint32_t score_flags;      /* ATTN_SCORE_* bits                          */
     int32_t window;            /* WINDOW: > 0                                */
@@ -119,6 +133,14 @@ typedef struct attn_mod_desc {
                                   B, S_q, S_k, mask fields and mask arrays;
                                   NULL: the library builds one internally    */
     size_t block_mask_bytes;   /* size of block_mask                         */
+    /* version >= 2 */
+    const uint8_t *blocks;     /* BLOCKS: device, [B or 1][ceil(S_q/128)]
+                                  [ceil(S_k/128)], nonzero = tile may be
+                                  visible                                    */
+    int32_t blocks_batched;    /* BLOCKS: 1 = one map per batch entry,
+                                  0 = one map for all                        */
+    int32_t rel_max;           /* RELBIAS: R >= 0, R < 2^30                  */
+    const float *rel_bias;     /* RELBIAS: device, [H][2 R + 1]              */
 } attn_mod_desc;
 
 /*
@@ -258,9 +280,10 @@ attn_status attn_fwd_noalloc(const void *q, const void *k, const void *v,
  *                      alignment needed; page-locked memory (cudaHostAlloc,
  *                      torch pin_memory) for full copy speed, pageable
  *                      memory works but its copies are synchronous
- *  mod                 as for attn_fwd, except that doc_ids, prefix_len and
- *                      alibi_slopes are host memory too and block_mask must
- *                      be NULL (else ATTN_ERR_INVALID_ARG)
+ *  mod                 as for attn_fwd, except that doc_ids, prefix_len,
+ *                      alibi_slopes, blocks and rel_bias are host memory too
+ *                      and block_mask must be NULL (else
+ *                      ATTN_ERR_INVALID_ARG)
  *  stream              the call starts after the work already enqueued on
  *                      `stream`, and work enqueued on `stream` afterwards
  *                      starts once O and LSE are in host memory

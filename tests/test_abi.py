@@ -113,6 +113,45 @@ def test_host_entry_point_validation(attn):
     assert call(mod=m) == INVALID
 
 
+def test_descriptor_versions(attn):
+    # version 1 (no block map / bias-table fields) is read without them;
+    # unknown versions are rejected.  attn_block_mask_bytes validates the
+    # descriptor on the host only (0 = rejected) and touches no memory.
+    lib = attn.lib()
+    big = 1 << 40
+
+    def nbytes(m):
+        return lib.attn_block_mask_bytes(1, 2, 256, 256, ctypes.byref(m))
+
+    m = attn.ModDesc()
+    m.version = 2
+    m.mask_flags = attn.MASK_BLOCKS
+    m.blocks = 5 * big
+    assert nbytes(m) > 0
+    m.version = 1                       # the v2 field is not part of a v1 descriptor
+    assert nbytes(m) == 0
+    m.version = 3
+    assert nbytes(m) == 0
+    m.version = 2
+    m.blocks_batched = 2
+    assert nbytes(m) == 0               # blocks_batched not 0 or 1
+    m.blocks_batched = 0
+    m.mask_flags = 0
+    m.score_flags = attn.SCORE_RELBIAS
+    m.rel_bias = 6 * big
+    m.rel_max = -1
+    assert nbytes(m) == 0               # rel_max < 0
+    m.rel_max = 4
+    assert nbytes(m) > 0
+    m.rel_bias = None
+    assert nbytes(m) == 0               # table missing
+    # a v1 descriptor keeps working for the v1 mods
+    m1 = attn.ModDesc()
+    m1.version = 1
+    m1.mask_flags = attn.MASK_CAUSAL
+    assert nbytes(m1) > 0
+
+
 def test_block_mask_bytes_is_host_only(attn):
     lib = attn.lib()
     m = attn.ModDesc()

@@ -123,3 +123,25 @@ def test_backward_sampled_at_size(attn):
     check("dQ", dq.reshape(-1, D)[torch.from_numpy(rows)], ref_dq)
     check("dK", dk.reshape(-1, D)[torch.from_numpy(keys)], ref_dk)
     check("dV", dv.reshape(-1, D)[torch.from_numpy(keys)], ref_dv)
+
+
+MODS3 = [
+    (1, 2, 2, 300, 128, {"rel": 6, "causal": True}),
+    (2, 2, 2, 400, 64, {"blocks": "batched", "rel": 3, "softcap": 8.0}),
+    (1, 4, 2, 520, 128, {"blocks": "shared", "causal": True, "alibi": True, "rel": 40}),
+]
+
+
+@pytest.mark.parametrize("case", range(len(MODS3)))
+def test_backward_rel_bias_and_block_map(attn, case):
+    B, H, Hkv, S, D, mods = MODS3[case]
+    mods = dict(mods)
+    g = torch.Generator().manual_seed(700 + case)
+    if "rel" in mods:
+        R = mods.pop("rel")
+        mods["rel_bias"] = (torch.randn((H, 2 * R + 1), generator=g) * 0.7).to(torch.float32)
+    if "blocks" in mods:
+        nb = -(-S // 128)
+        Bb = B if mods["blocks"] == "batched" else 1
+        mods["blocks"] = (torch.rand((Bb, nb, nb), generator=g) < 0.6).to(torch.uint8)
+    run_case(attn, B, H, Hkv, S, D, mods, seed=700 + case)

@@ -103,3 +103,19 @@ def test_default_alibi_slopes_across_head_chunks(attn):
     o_ref, lse_ref = on_device(attn, q, k, v, mods)
     assert torch.equal(o, o_ref)
     assert torch.equal(lse, lse_ref)
+
+
+def test_host_rel_bias_and_block_map(attn):
+    # a per-batch block map and a bias table across head chunks
+    B, H, S, D = 2, 8, 400, 64
+    q, k, v = (t.pin_memory() for t in inputs(B, H, H, S, D, seed=50))
+    g = torch.Generator().manual_seed(51)
+    nb = -(-S // 128)
+    mods = dict(causal=True,
+                blocks=(torch.rand((B, nb, nb), generator=g) < 0.6).to(torch.uint8),
+                rel_bias=(torch.randn((H, 2 * 9 + 1), generator=g) * 0.5).to(torch.float32))
+    o, lse = attn.attn_fwd_host(q, k, v, **mods)
+    torch.cuda.current_stream(DEV).synchronize()
+    o_ref, lse_ref = on_device(attn, q, k, v, mods)
+    assert torch.equal(o, o_ref)
+    assert torch.equal(lse, lse_ref)

@@ -55,6 +55,10 @@ def oracle_kw(kw):
         ok["alibi"] = True
     if kw.get("alibi_slopes") is not None:
         ok["alibi_slopes"] = kw["alibi_slopes"].double().tolist()
+    if kw.get("rel_bias") is not None:
+        ok["rel_bias"] = kw["rel_bias"].double().numpy()
+    if kw.get("blocks") is not None:
+        ok["blocks"] = kw["blocks"].numpy()
     return ok
 
 
@@ -448,3 +452,55 @@ def test_workload_parity(attn, name):
     msg, _, _ = run_and_compare(attn, inp["q"], inp["k"], inp["v"], w.scale,
                                 rows=rows.numpy(), **kw)
     print(name, msg)
+
+
+# ------------------------- relative-position bias table and block map ---
+
+def rel_table(H, R, seed):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn((H, 2 * R + 1), generator=g) * 0.7).to(torch.float32)
+
+
+def block_map(Bb, S_q, S_k, seed, p=0.6):
+    g = torch.Generator().manual_seed(seed)
+    nq, nk = -(-S_q // 128), -(-S_k // 128)
+    return (torch.rand((Bb, nq, nk), generator=g) < p).to(torch.uint8)
+
+
+MODS3 = [
+    (1, 2, 2, 300, 300, 128, {"rel": 4}),
+    (1, 2, 2, 300, 300, 64, {"rel": 500, "causal": True}),
+    (1, 4, 2, 260, 260, 128, {"rel": 16, "alibi": True, "softcap": 10.0, "causal": True}),
+    (1, 2, 2, 384, 384, 128, {"rel": 0, "q_offset": 50, "causal": True}),
+    (2, 2, 2, 400, 520, 128, {"blocks": "batched"}),
+    (1, 2, 2, 500, 500, 64, {"blocks": "shared", "causal": True}),
+    (2, 2, 2, 600, 600, 128, {"blocks": "batched", "doc_ids": "packed", "causal": True, "rel": 8}),
+]
+
+
+def mods3(B, H, Sq, Sk, mods, seed):
+    mods = dict(mods)
+    if "rel" in mods:
+        mods["rel_bias"] = rel_table(H, mods.pop("rel"), seed)
+    if mods.get("blocks") is not None:
+        mods["blocks"] = block_map(B if mods["blocks"] == "batched" else 1, Sq, Sk, seed + 1)
+    if mods.get("doc_ids") == "packed":
+        mods["doc_ids"] = torch.stack([workloads.doc_ids_for(Sk, seed=seed + b, lo=64, hi=300)
+                                       for b in range(B)]).contiguous()
+    return mods
+
+
+@pytest.mark.parametrize("case", range(len(MODS3)))
+def test_rel_bias_and_block_map(attn, case):
+    B, H, Hkv, Sq, Sk, D, mods = MODS3[case]
+    mods = mods3(B, H, Sq, Sk, mods, seed=600 + case)
+    q, k, v = rand_inputs(B, H, Hkv, Sq, Sk, D, seed=600 + case)
+    run_and_compare(attn, q, k, v, 1.0 / math.sqrt(D), **mods)
+    if "blocks" in mods:  # the tile classes honour the map exactly
+        mk = {n: mods[n] for n in ("causal", "doc_ids", "blocks", "q_offset") if n in mods}
+        want = expected_classes(B, Sq, Sk, mk)
+        got = attn.decode_block_mask(attn.build_block_mask(B, H, Sq, Sk, device=DEV, **to_dev(mk)))
+        cls = got["cls"]
+        if cls.shape[0] == 1:
+            want = want[:1]
+        np.testing.assert_array_equal(cls, want)
