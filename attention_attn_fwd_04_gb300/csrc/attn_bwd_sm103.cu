@@ -241,6 +241,23 @@ __device__ __forceinline__ void add_rel_bias(float (&tv)[128], const BParams& p,
     if (p.rel_bias == nullptr) return;
     const float* row = p.rel_bias + (size_t)h * (2 * (size_t)p.rel_max + 1);
     const float rs = (SOFTCAP ? 2.0f * kBLog2e / p.softcap : kBLog2e) / m.sc;
+    // beyond +-R of every position of the warp the clamped bias is one entry
+    const int lo_r = min(pos0, pos0 + step * 127), hi_r = max(pos0, pos0 + step * 127);
+    float cst = 0.f;
+    bool flat = true;
+    if (__all_sync(0xffffffffu, hi_r <= -p.rel_max)) {
+      cst = __ldg(row);
+    } else if (__all_sync(0xffffffffu, lo_r >= p.rel_max)) {
+      cst = __ldg(row + 2 * p.rel_max);
+    } else {
+      flat = false;
+    }
+    if (flat) {
+      const float add = cst * rs;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) tv[c] += add;
+      return;
+    }
 #pragma unroll
     for (int c = 0; c < 128; ++c) {
       const int r = min(max(pos0 + step * c, -p.rel_max), p.rel_max);

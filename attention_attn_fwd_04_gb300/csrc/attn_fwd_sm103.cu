@@ -664,22 +664,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             }
           }
           // score mods
+          // relative-position bias: where the whole tile lies beyond +-R of
+          // every row of the warp, the clamped bias is one table entry,
+          // folded into the constant term below; otherwise a loop of its own
+          // (a uniform branch, so the loops stay branch-free), scaled so it
+          // adds table * rel_scale to s * sc
+          float rel_const = 0.f;
           if constexpr (ALIBI) {
-            // relative-position bias (a uniform branch around a loop of its
-            // own, so the loops stay branch-free): scaled so that it adds
-            // table * rel_scale to s * sc below
             if (relrow != nullptr) {
-              const float rs = rel_scale / sc;
+              const int lo_r = j0 - qpos, hi_r = j0 + kTileN - 1 - qpos;
+              if (__all_sync(0xffffffffu, hi_r <= -p.rel_max)) {
+                rel_const = __ldg(relrow) * rel_scale;
+              } else if (__all_sync(0xffffffffu, lo_r >= p.rel_max)) {
+                rel_const = __ldg(relrow + 2 * p.rel_max) * rel_scale;
+              } else {
+                const float rs = rel_scale / sc;
 #pragma unroll
-              for (int c = 0; c < kTileN; ++c) {
-                const int r = min(max(j0 + c - qpos, -p.rel_max), p.rel_max);
-                tv[c] = fmaf(__ldg(relrow + r + p.rel_max), rs, tv[c]);
+                for (int c = 0; c < kTileN; ++c) {
+                  const int r = min(max(j0 + c - qpos, -p.rel_max), p.rel_max);
+                  tv[c] = fmaf(__ldg(relrow + r + p.rel_max), rs, tv[c]);
+                }
               }
             }
           }
           if constexpr (ALIBI || SOFTCAP) {
             // paired fp32 instructions, two columns at a time
-            const float b0 = ALIBI ? slope2 * (float)(j0 - qpos) : 0.f;
+            const float b0 = ALIBI ? fmaf(slope2, (float)(j0 - qpos), rel_const) : 0.f;
             const uint64_t sc2 = ptx::f2(sc, sc), sl2 = ptx::f2(slope2, slope2),
                            b02 = ptx::f2(b0, b0), one2 = ptx::f2(1.0f, 1.0f),
                            m2c2 = ptx::f2(-2.0f * capl2, -2.0f * capl2),

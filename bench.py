@@ -281,6 +281,45 @@ def time_backward(attn, w, inp, dev, steps, warmup):
     return start.elapsed_time(end) / steps
 
 
+def time_mods3(attn, w, inp, dev, steps, warmup, R=256, p_open=0.5, seed=11):
+    """The headline shape with the two descriptor mods of the next-step row:
+    a seeded block map opening about half of the 128 x 128 tiles
+    (block-sparse attention) and a relative-position bias table with R = 256.
+    Returns (visible pairs, forward ms, backward ms)."""
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    g = torch.Generator().manual_seed(seed)
+    nq, nk = -(-w.S_q // 128), -(-w.S_k // 128)
+    blocks = (torch.rand((1, nq, nk), generator=g) < p_open).to(torch.uint8)
+    rel = (torch.randn((w.H, 2 * R + 1), generator=g) * 0.5).to(torch.float32)
+    kw = dict(blocks=blocks.to(dev), rel_bias=rel.to(dev))
+    pairs = w.B * w.H * int(blocks.sum()) * 128 * 128  # S is a multiple of 128 here
+    stream = torch.cuda.current_stream(dev)
+    o, lse = attn.attn_fwd(q, k, v, scale=w.scale, **kw)
+    do = torch.randn(o.shape, device=dev, generator=torch.Generator(device=dev).manual_seed(3))
+    do = do.to(torch.bfloat16)
+
+    def timed(fn, n):
+        for _ in range(warmup):
+            fn()
+        torch.cuda.synchronize(dev)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return a.elapsed_time(b) / n
+
+    fwd_ms = timed(lambda: attn.attn_fwd_into(q, k, v, o, lse, scale=w.scale, stream=stream, **kw),
+                   steps)
+    bwd_ms = timed(lambda: attn.attn_bwd(q, k, v, o, lse, do, scale=w.scale, stream=stream, **kw),
+                   max(3, steps // 10))
+    st = attn.get_device_status(device=dev)
+    if st != 0:
+        raise RuntimeError("device status %s" % attn.status_string(st))
+    return pairs, fwd_ms, bwd_ms
+
+
 def time_e2e(attn, w, inp, dev, steps, warmup):
     """Same metric through the public host-memory entry point
     (attn_fwd_host): every step copies Q, K, V (+ mask arrays) in from
@@ -467,6 +506,13 @@ def main():
             bms = time_backward(attn, wx, ix, dev, bsteps, 3)
             per[name].update(bwd_ms=bms, bwd_tflops=2.5 * fx / (bms * 1e-3) / 1e12)
             del ix
+        # the descriptor mods of the next-step row on the headline shape
+        pm, fm, bmm = time_mods3(attn, w, inp, dev, min(max(5, args.steps // 4), 200), 3)
+        fm_flops = 4.0 * w.D * pm
+        per["blocks50_relbias256_" + w.name.split("_", 1)[1]] = {
+            "tflops": fm_flops / (fm * 1e-3) / 1e12, "ms_per_step": fm,
+            "frac": fm_flops / (fm * 1e-3) / 1e12 / peak, "visible_pairs": pm,
+            "bwd_ms": bmm, "bwd_tflops": 2.5 * fm_flops / (bmm * 1e-3) / 1e12}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
