@@ -56,6 +56,7 @@ OPT_WAIT_BUDGET_MS = 3
 OPT_NUM_CTAS = 4
 OPT_EXP_POLY_FRACTION = 5
 OPT_DEBUG_STALL = 6
+OPT_CTA_PAIR = 7
 _OPTIONS = {
     "rescale_threshold": OPT_RESCALE_THRESHOLD,
     "force_partial": OPT_FORCE_PARTIAL,
@@ -63,6 +64,7 @@ _OPTIONS = {
     "num_ctas": OPT_NUM_CTAS,
     "exp_poly_fraction": OPT_EXP_POLY_FRACTION,
     "debug_stall": OPT_DEBUG_STALL,
+    "cta_pair": OPT_CTA_PAIR,
 }
 
 STATUS_NAMES = {
@@ -485,20 +487,21 @@ def decode_block_mask(bm: BlockMask) -> dict:
     keys = ("magic", "version", "B", "S_q", "S_k", "nQ", "nK", "nP", "bm", "n_entries",
             "mask_flags", "window", "q_offset", "force_partial", "uniform", "max_cnt",
             "doc_ptr", "prefix_ptr", "order_off", "cnt_off", "list_off", "total_bytes",
-            "doc_off", "docs_sorted", "pad", "blocks_ptr", "pad2")
+            "doc_off", "docs_sorted", "tiles_per_entry", "blocks_ptr", "pad2")
     h = dict(zip(keys, f))
     n, nK, nP, nQ = h["n_entries"], h["nK"], h["nP"], h["nQ"]
     order = raw[h["order_off"]:h["order_off"] + 4 * n].view(np.int32).copy()
     cnt = raw[h["cnt_off"]:h["cnt_off"] + 4 * n].view(np.int32).copy()
     lst = raw[h["list_off"]:h["list_off"] + 4 * n * nK].view(np.uint32).reshape(n, nK).copy()
+    tpe = h["tiles_per_entry"]  # query tiles per entry: 2, or 4 for the CTA-pair forward
     cls = np.zeros((h["bm"], nQ, nK), dtype=np.int8)
     for e in range(n):
         b, p = divmod(e, nP)
         for x in lst[e, :cnt[e]]:
             kt = int(x) & 0xFFFFFF
-            for t in range(2):
-                if 2 * p + t < nQ:
-                    cls[b, 2 * p + t, kt] = (int(x) >> (24 + 2 * t)) & 3
+            for t in range(tpe):
+                if tpe * p + t < nQ:
+                    cls[b, tpe * p + t, kt] = (int(x) >> (24 + 2 * t)) & 3
     h.update(order=order, cnt=cnt, list=lst, cls=cls)
     if h["doc_off"]:  # document mask: first / last key of each token's run of equal ids
         bm_, S = h["bm"], h["S_k"]

@@ -23,6 +23,7 @@ struct Options {
   double num_ctas = 0.0;
   double poly_fraction = 0.0;
   double debug_stall = 0.0;
+  double cta_pair = 0.0;
 };
 Options g_opts;
 std::mutex g_opts_mu;
@@ -31,6 +32,9 @@ Options options_snapshot() {
   std::lock_guard<std::mutex> lk(g_opts_mu);
   return g_opts;
 }
+
+// Query tiles per entry of the forward's block masks under these options.
+int mask_tpe(const Options& o) { return o.cta_pair != 0.0 ? kTilesPerQuad : kTilesPerItem; }
 
 // Per-device scratch owned by the library: the status word and the block
 // mask built when the caller passes none.  Allocated on first need, grown
@@ -236,13 +240,13 @@ attn_status check_device_tensors(const void* q, const void* k, const void* v, co
 attn_status enqueue_forward(const void* q, const void* k, const void* v, void* out, float* lse,
                             int B, int H, int H_kv, int S_q, int S_k, int D, float scale,
                             const attn_mod_desc* mod, const void* bmask, void* mask_buf,
-                            DeviceStatus* status, cudaStream_t s) {
-  const Options o = options_snapshot();
+                            DeviceStatus* status, const Options& o, cudaStream_t s) {
   const MaskParams mp = mask_params(S_q, S_k, mod);
-  const BlockMaskGeom g = block_mask_geom(B, S_q, S_k, mp.flags);
+  const int tpe = mask_tpe(o);
+  const BlockMaskGeom g = block_mask_geom(B, S_q, S_k, mp.flags, tpe);
   if (bmask == nullptr) {
-    if (launch_build_block_mask(B, S_q, S_k, mp, o.force_partial != 0.0 ? 1 : 0, mask_buf, s) !=
-        cudaSuccess)
+    if (launch_build_block_mask(B, S_q, S_k, mp, o.force_partial != 0.0 ? 1 : 0, mask_buf, s,
+                                tpe) != cudaSuccess)
       return ATTN_ERR_CUDA;
     bmask = mask_buf;
   }
@@ -276,6 +280,8 @@ attn_status enqueue_forward(const void* q, const void* k, const void* v, void* o
   a.rescale_threshold = (float)o.rescale_threshold;
   a.wait_budget_ms = o.wait_budget_ms;
   a.num_ctas = (int)o.num_ctas;
+  a.cta_pair = o.cta_pair != 0.0 ? 1 : 0;
+  a.tpe = tpe;
   a.poly_fraction = (float)o.poly_fraction;
   a.debug_stall = o.debug_stall != 0.0 ? 1 : 0;
   return launch_attn_fwd(a, s) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
@@ -370,7 +376,8 @@ struct HostLayout {
   size_t q, k, v, o, lse, doc, prefix, slopes, blocks, rel, mask, total;
   size_t blocks_bytes, rel_bytes;
 };
-HostLayout host_layout(int B, int H, int H_kv, int S_q, int S_k, int D, const attn_mod_desc* mod) {
+HostLayout host_layout(int B, int H, int H_kv, int S_q, int S_k, int D, const attn_mod_desc* mod,
+                       int tpe) {
   HostLayout l;
   const size_t qb = (size_t)B * H * S_q * D * 2, kb = (size_t)B * H_kv * S_k * D * 2;
   size_t at = 0;
@@ -395,7 +402,8 @@ HostLayout host_layout(int B, int H, int H_kv, int S_q, int S_k, int D, const at
     l.rel_bytes = (size_t)H * (2 * (size_t)mod->rel_max + 1) * 4;
   l.blocks = take(l.blocks_bytes);
   l.rel = take(l.rel_bytes);
-  l.mask = take(block_mask_geom(1, S_q, S_k, kernel_mask_flags(mod) & ~kMaskBlocksBatched).total);  // one batch entry
+  // one batch entry
+  l.mask = take(block_mask_geom(1, S_q, S_k, kernel_mask_flags(mod) & ~kMaskBlocksBatched, tpe).total);
   l.total = at;
   return l;
 }
@@ -471,6 +479,10 @@ attn_status attn_set_option(attn_option opt, double value) {
       if (value != 0.0 && value != 1.0) return ATTN_ERR_INVALID_ARG;
       g_opts.debug_stall = value;
       return ATTN_OK;
+    case ATTN_OPT_CTA_PAIR:
+      if (value != 0.0 && value != 1.0) return ATTN_ERR_INVALID_ARG;
+      g_opts.cta_pair = value;
+      return ATTN_OK;
   }
   return ATTN_ERR_INVALID_ARG;
 }
@@ -497,6 +509,9 @@ attn_status attn_get_option(attn_option opt, double* value) {
     case ATTN_OPT_DEBUG_STALL:
       *value = g_opts.debug_stall;
       return ATTN_OK;
+    case ATTN_OPT_CTA_PAIR:
+      *value = g_opts.cta_pair;
+      return ATTN_OK;
   }
   return ATTN_ERR_INVALID_ARG;
 }
@@ -507,7 +522,7 @@ size_t attn_block_mask_bytes(int B, int H, int S_q, int S_k, const attn_mod_desc
   const attn_mod_desc* mod = load_mod(mod_in, &mod_buf, &lst);
   if (lst != ATTN_OK) return 0;
   if (check_problem(B, H, S_q, S_k, mod) != ATTN_OK) return 0;
-  return block_mask_geom(B, S_q, S_k, kernel_mask_flags(mod)).total;
+  return block_mask_geom(B, S_q, S_k, kernel_mask_flags(mod), mask_tpe(options_snapshot())).total;
 }
 
 attn_status attn_build_block_mask(int B, int H, int S_q, int S_k, const attn_mod_desc* mod_in,
@@ -519,12 +534,12 @@ attn_status attn_build_block_mask(int B, int H, int S_q, int S_k, const attn_mod
   attn_status st = check_problem(B, H, S_q, S_k, mod);
   if (st != ATTN_OK) return st;
   if (dst == nullptr || !aligned(dst, 16)) return ATTN_ERR_INVALID_ARG;
-  const size_t need = block_mask_geom(B, S_q, S_k, kernel_mask_flags(mod)).total;
-  if (bytes < need) return ATTN_ERR_INVALID_ARG;
   const Options o = options_snapshot();
+  const size_t need = block_mask_geom(B, S_q, S_k, kernel_mask_flags(mod), mask_tpe(o)).total;
+  if (bytes < need) return ATTN_ERR_INVALID_ARG;
   cudaError_t err = launch_build_block_mask(B, S_q, S_k, mask_params(S_q, S_k, mod),
                                             o.force_partial != 0.0 ? 1 : 0, dst,
-                                            reinterpret_cast<cudaStream_t>(stream));
+                                            reinterpret_cast<cudaStream_t>(stream), mask_tpe(o));
   return err == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
@@ -537,7 +552,8 @@ attn_status attn_block_mask_stats(const void* block_mask, size_t bytes, attn_str
   BlockMaskHeader h;
   if (cudaMemcpy(&h, block_mask, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
     return ATTN_ERR_CUDA;
-  if (h.magic != kBlockMaskMagic || h.version != kBlockMaskVersion || h.total_bytes > bytes)
+  if (h.magic != kBlockMaskMagic || h.version != kBlockMaskVersion || h.total_bytes > bytes ||
+      (h.tiles_per_entry != kTilesPerItem && h.tiles_per_entry != kTilesPerQuad))
     return ATTN_ERR_INVALID_ARG;
   std::vector<int32_t> cnt(h.n_entries);
   std::vector<uint32_t> list((size_t)h.n_entries * h.nK);
@@ -553,8 +569,8 @@ attn_status attn_block_mask_stats(const void* block_mask, size_t bytes, attn_str
     for (int j = 0; j < cnt[e]; ++j) {
       const uint32_t x = list[(size_t)e * h.nK + j];
       ++ent;
-      for (int t = 0; t < 2; ++t) {
-        if (2 * p + t >= h.nQ) continue;
+      for (int t = 0; t < h.tiles_per_entry; ++t) {
+        if (h.tiles_per_entry * p + t >= h.nQ) continue;
         const uint32_t c = entry_cls(x, t);
         full += c == kFull;
         part += c == kPartial;
@@ -599,7 +615,8 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, flo
   st = check_device_tensors(q, k, v, out, lse, B, H, H_kv, S_q, S_k, D, scale);
   if (st != ATTN_OK) return st;
   const uint32_t mflags = kernel_mask_flags(mod);
-  const BlockMaskGeom g = block_mask_geom(B, S_q, S_k, mflags);
+  const Options o = options_snapshot();
+  const BlockMaskGeom g = block_mask_geom(B, S_q, S_k, mflags, mask_tpe(o));
   if (mod != nullptr && mod->block_mask != nullptr &&
       (!aligned(mod->block_mask, 16) || mod->block_mask_bytes < g.total))
     return ATTN_ERR_INVALID_ARG;
@@ -617,7 +634,7 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* out, flo
     if (st != ATTN_OK) return st;
   }
   return enqueue_forward(q, k, v, out, lse, B, H, H_kv, S_q, S_k, D, scale, mod, bmask, scr->mask,
-                         scr->status, s);
+                         scr->status, o, s);
 }
 
 attn_status attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, float* lse,
@@ -635,7 +652,8 @@ attn_status attn_fwd_noalloc(const void* q, const void* k, const void* v, void* 
   // The block mask is always built into the fixed scratch array.
   if (mod != nullptr && mod->block_mask != nullptr) return ATTN_ERR_INVALID_ARG;
   const uint32_t mflags = kernel_mask_flags(mod);
-  const BlockMaskGeom g = block_mask_geom(B, S_q, S_k, mflags);
+  const Options o = options_snapshot();
+  const BlockMaskGeom g = block_mask_geom(B, S_q, S_k, mflags, mask_tpe(o));
   if (g.total > ATTN_NOALLOC_SCRATCH_BYTES - kNoAllocStatusBytes) return ATTN_ERR_UNSUPPORTED;
 
   // ---- device work: no allocation from here on ----------------------------
@@ -650,7 +668,7 @@ attn_status attn_fwd_noalloc(const void* q, const void* k, const void* v, void* 
   // The status word must start at zero; the block mask is rewritten whole.
   if (cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s) != cudaSuccess) return ATTN_ERR_CUDA;
   return enqueue_forward(q, k, v, out, lse, B, H, H_kv, S_q, S_k, D, scale, mod, nullptr, bmask,
-                         status, s);
+                         status, o, s);
 }
 
 attn_status attn_fwd_host(const void* q, const void* k, const void* v, void* out, float* lse,
@@ -666,7 +684,8 @@ attn_status attn_fwd_host(const void* q, const void* k, const void* v, void* out
   st = check_tensors(q, k, v, out, lse, B, H, H_kv, S_q, S_k, D, scale);
   if (st != ATTN_OK) return st;
   if (mod != nullptr && mod->block_mask != nullptr) return ATTN_ERR_INVALID_ARG;
-  const HostLayout lay = host_layout(B, H, H_kv, S_q, S_k, D, mod);
+  const Options o = options_snapshot();
+  const HostLayout lay = host_layout(B, H, H_kv, S_q, S_k, D, mod, mask_tpe(o));
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
@@ -768,17 +787,16 @@ attn_status attn_fwd_host(const void* q, const void* k, const void* v, void* out
       // forwards that read the previous one
       const int want_b = per_batch ? b : 0;
       if (mask_b != want_b) {
-        const Options o = options_snapshot();
         if (launch_build_block_mask(1, S_q, S_k, mask_params(S_q, S_k, &cm),
-                                    o.force_partial != 0.0 ? 1 : 0, base + lay.mask,
-                                    pipe->comp) != cudaSuccess)
+                                    o.force_partial != 0.0 ? 1 : 0, base + lay.mask, pipe->comp,
+                                    mask_tpe(o)) != cudaSuccess)
           return ATTN_ERR_CUDA;
         mask_b = want_b;
       }
       float* dl = lse != nullptr ? reinterpret_cast<float*>(base + lay.lse) + qh0 * S_q : nullptr;
       st = enqueue_forward(base + lay.q + qh0 * q_head, base + lay.k + kh0 * k_head,
                            base + lay.v + kh0 * k_head, base + lay.o + qh0 * q_head, dl, 1, nh,
-                           nkv, S_q, S_k, D, scale, &cm, base + lay.mask, nullptr, scr->status,
+                           nkv, S_q, S_k, D, scale, &cm, base + lay.mask, nullptr, scr->status, o,
                            pipe->comp);
       if (st != ATTN_OK) return st;
       ok = ck(cudaEventRecord(pipe->comp_ev, pipe->comp)) &&

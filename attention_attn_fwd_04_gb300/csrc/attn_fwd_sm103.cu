@@ -27,9 +27,23 @@
 // Tensor Memory that P_t(j) occupies; it is issued after PV_t(j) by the same
 // thread and tcgen05 MMAs execute in issue order.
 //
+// CTA-pair form (PAIR, D = 128; "FlashAttention-4 explained", "TMEM and
+// 2-CTA MMA", "2-CTA MMA mode"): two CTAs of a cluster share one work item
+// of four query tiles; CTA r holds query tiles 2t + r of it.  Every S and PV
+// product of tile t is one tcgen05 MMA with M = 256 (cta_group::2) issued by
+// rank 0, which reads each CTA's own Q rows (or P in Tensor Memory) and half
+// of the key / value tile from each CTA's shared memory: keys
+// [64 r, 64 r + 64) of K, columns [64 r, 64 r + 64) of V.  Each CTA thus
+// stages half of every K/V tile, the per-SM shared-memory traffic of the B
+// operand halves, and one K/V tile serves 512 query rows.  The softmax is
+// unchanged: each CTA's accumulators hold its own 128 rows.  Shared
+// barriers (operands landed, P ready, O free) live in rank 0, the rest in
+// both CTAs, signalled by multicast commits.
+//
 // Every mbarrier wait is bounded by a time budget; on expiry the kernel
-// records ATTN_ERR_TIMEOUT in the device status word, drains its own
-// in-flight copies and MMAs, frees Tensor Memory and returns.
+// records ATTN_ERR_TIMEOUT in the device status word (and raises the abort
+// flag of both CTAs of a pair), drains its own in-flight copies and MMAs,
+// frees Tensor Memory and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -75,16 +89,24 @@ enum Site : int {
   kSiteSmxOFull = 31,
 };
 
-template <int D>
+// PAIR: the CTA is one of a pair (a cluster of two) whose MMAs span both
+// CTAs (M = 256, cta_group::2).  Each CTA then stages its own Q tiles and
+// half of every key / value tile: keys [64 r, 64 r + 64) of a K tile and
+// columns [64 r, 64 r + 64) of a V tile for the CTA of rank r, 16 KB either
+// way, so a ring stage holds 16 KB instead of a whole 32 KB tile.
+template <int D, bool PAIR = false>
 struct Cfg {
+  static_assert(!PAIR || D == 128, "the CTA-pair forward is built for D = 128");
   static constexpr int kHalfBytes = kTileM * 64 * 2;  // 128 rows x 64 bf16, 128-byte swizzle
   static constexpr int kHalves = D / 64;
   static constexpr int kTileBytes = kHalves * kHalfBytes;
-  static constexpr int kStages = (D == 128) ? 4 : 8;
+  static constexpr int kKPartHalfBytes = 64 * 64 * 2;  // PAIR: 64 keys x 64 columns of K
+  static constexpr int kStageBytes = PAIR ? kTileBytes / 2 : kTileBytes;
+  static constexpr int kStages = PAIR ? 8 : ((D == 128) ? 4 : 8);
   static constexpr int kOCol = 256;  // O_t at column 256 + t * D; S_t at t * 128
   static constexpr int kSmemQ = 0;
   static constexpr int kSmemKV = kSmemQ + 2 * kTileBytes;
-  static constexpr int kSmemBar = kSmemKV + kStages * kTileBytes;
+  static constexpr int kSmemBar = kSmemKV + kStages * kStageBytes;
   // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2]
   //           o_full[2] o_empty[2] drain never (the test hook's)
   static constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 2 + 2 + 2 + 1 + 1;
@@ -98,6 +120,7 @@ struct KParams {
   CUtensorMap tmap_q;
   CUtensorMap tmap_k;
   CUtensorMap tmap_v;
+  CUtensorMap tmap_kh;  // K with 64-row boxes (the CTA pair's half tiles)
   __nv_bfloat16* out;
   float* lse;
   int B, H, H_kv, S_q, S_k, group;
@@ -135,6 +158,8 @@ struct Ctl {
   uint64_t budget_ns;
 };
 
+// Records the first failure and raises the abort flag (PAIR: of both CTAs).
+template <bool PAIR>
 __device__ __noinline__ void report(const Ctl& c, int code, int site, int detail) {
   if (atomicCAS(&c.status->code, 0, code) == 0) {
     c.status->where = site;
@@ -142,6 +167,7 @@ __device__ __noinline__ void report(const Ctl& c, int code, int site, int detail
     c.status->detail = detail;
   }
   *c.abort = 1;
+  if constexpr (PAIR) ptx::st_cluster_u32(ptx::mapa(c.abort_smem, ptx::cluster_ctarank() ^ 1u), 1u);
 }
 
 // Bounded wait on an mbarrier phase.  Returns false when the wait was given
@@ -151,6 +177,15 @@ __device__ __noinline__ void report(const Ctl& c, int code, int site, int detail
 // phase completes) and checks the abort flag and the time budget only every
 // 16 suspensions, instead of spinning through the issue slots.
 constexpr uint32_t kSuspendHintNs = 20000;
+// After an abort, how long rank 1 of a CTA pair lets its copies in flight
+// land before it leaves (they complete on rank 0's barriers, which it cannot
+// poll): far above the latency of one tile copy.
+constexpr uint64_t kPeerDrainNs = 200000;
+// Phases completed by the peer CTA of a pair need no cluster-scope acquire
+// either: the data behind every such barrier is Tensor Memory or shared
+// memory filled by TMA, whose visibility the tcgen05 fences and the
+// transaction count give.
+template <bool PAIR>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ctl& c, int site) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = 0;
@@ -162,21 +197,29 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ct
       if (t0 == 0) {
         t0 = now;
       } else if (now - t0 > c.budget_ns) {
-        report(c, ATTN_ERR_TIMEOUT, site, (int)parity);
+        report<PAIR>(c, ATTN_ERR_TIMEOUT, site, (int)parity);
         return false;
       }
     }
   }
 }
 
-// Item w -> (batch, head, entry).  Entries are (mask batch, query-tile pair)
-// ordered by descending work; when every entry has the same work the pairs
-// of one (batch, head) run next to each other so their K/V stay in L2.
+// Item w -> (batch, head, entry, half).  Entries are (mask batch, group of
+// query tiles) ordered by descending work; when every entry has the same
+// work the entries of one (batch, head) run next to each other so their K/V
+// stay in L2.  A single CTA takes two query tiles at a time, so an entry of
+// four tiles gives it two items, half 0 and 1 (HALVES).
 struct Item {
-  int b, h, e, pair;
+  int b, h, e, pair, half;
 };
+template <bool HALVES>
 __device__ __forceinline__ Item decode_item(const KParams& p, int w, int uniform) {
   Item it;
+  it.half = 0;
+  if constexpr (HALVES) {
+    it.half = w & 1;
+    w >>= 1;
+  }
   const int nb = p.B / p.bm;  // batches sharing one mask entry
   int b_local;
   if (uniform) {
@@ -198,10 +241,12 @@ __device__ __forceinline__ Item decode_item(const KParams& p, int w, int uniform
   return it;
 }
 
-// Static snake schedule over the items: round r gives CTA c item
-// r*G + c (even r) or r*G + G-1-c (odd r).
+// Static snake schedule over the items: round r gives unit c (a CTA, or a
+// CTA pair) of G item r*G + c (even r) or r*G + G-1-c (odd r).
+template <bool PAIR>
 __device__ __forceinline__ int item_of(int r) {
-  const int G = gridDim.x, c = blockIdx.x;
+  const int G = PAIR ? (int)ptx::cluster_count_x() : (int)gridDim.x;
+  const int c = PAIR ? (int)ptx::cluster_id_x() : (int)blockIdx.x;
   return r * G + ((r & 1) ? (G - 1 - c) : c);
 }
 
@@ -216,32 +261,50 @@ struct Desc {
 };
 
 // S = Q K^T: D/16 MMAs (K = 16 each) over the two 64-column halves of the
-// swizzled tiles.  Warp-wide; one elected lane issues.
-template <int D>
+// swizzled tiles.  Warp-wide; one elected lane issues.  PAIR: M = 256 rows
+// over the CTA pair, each CTA's K part 64 keys deep (8 KB per column half).
+template <int D, bool PAIR>
 __device__ __forceinline__ void issue_s(uint32_t tmem_s, uint64_t q_desc, uint64_t k_desc) {
-  constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTileM, kTileN, false);
+  constexpr uint32_t idesc = ptx::idesc_bf16_f32(PAIR ? 2 * kTileM : kTileM, kTileN, false);
+  constexpr int kKHalf = PAIR ? Cfg<D, PAIR>::kKPartHalfBytes : Cfg<D, PAIR>::kHalfBytes;
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
-    const uint64_t off = (uint64_t)(((kk / 4) * Cfg<D>::kHalfBytes + (kk % 4) * 32) >> 4);
-    ptx::mma_ss_elect(tmem_s, q_desc + off, k_desc + off, idesc, kk > 0 ? 1u : 0u);
+    const uint64_t qoff = (uint64_t)(((kk / 4) * Cfg<D, PAIR>::kHalfBytes + (kk % 4) * 32) >> 4);
+    const uint64_t koff = (uint64_t)(((kk / 4) * kKHalf + (kk % 4) * 32) >> 4);
+    if constexpr (PAIR)
+      ptx::mma_ss_pair_elect(tmem_s, q_desc + qoff, k_desc + koff, idesc, kk > 0 ? 1u : 0u);
+    else
+      ptx::mma_ss_elect(tmem_s, q_desc + qoff, k_desc + koff, idesc, kk > 0 ? 1u : 0u);
   }
 }
 
 // O (+)= P V: 8 MMAs of 16 keys (16 rows of V = 2 KB of the swizzled tile;
-// 8 packed bf16 columns of P in Tensor Memory).  Warp-wide.
-template <int D>
+// 8 packed bf16 columns of P in Tensor Memory).  Warp-wide.  PAIR: M = 256,
+// each CTA's V part is its 64 columns of the tile.
+template <int D, bool PAIR>
 __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint64_t v_desc,
                                          bool accumulate) {
-  constexpr uint32_t idesc = ptx::idesc_bf16_f32(kTileM, D, true);
+  constexpr uint32_t idesc = ptx::idesc_bf16_f32(PAIR ? 2 * kTileM : kTileM, D, true);
 #pragma unroll
-  for (int kk = 0; kk < kTileN / 16; ++kk)
-    ptx::mma_ts_elect(tmem_o, tmem_p + (uint32_t)(kk * 8), v_desc + (uint64_t)((kk * 2048) >> 4),
-                      idesc, (accumulate || kk > 0) ? 1u : 0u);
+  for (int kk = 0; kk < kTileN / 16; ++kk) {
+    const uint32_t tp = tmem_p + (uint32_t)(kk * 8);
+    const uint64_t vd = v_desc + (uint64_t)((kk * 2048) >> 4);
+    const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
+    if constexpr (PAIR)
+      ptx::mma_ts_pair_elect(tmem_o, tp, vd, idesc, acc);
+    else
+      ptx::mma_ts_elect(tmem_o, tp, vd, idesc, acc);
+  }
 }
 
-template <int D, bool ALIBI, bool SOFTCAP>
+// QUAD: the block mask groups four query tiles per entry (kTilesPerQuad);
+// a CTA pair always uses such masks, a single CTA takes them in halves.
+template <int D, bool ALIBI, bool SOFTCAP, bool PAIR, bool QUAD>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ KParams p) {
-  using C = Cfg<D>;
+  static_assert(!PAIR || QUAD, "a CTA pair works on four-tile entries");
+  using C = Cfg<D, PAIR>;
+  constexpr int kTpe = QUAD ? kTilesPerQuad : kTilesPerItem;  // query tiles per entry
+  constexpr bool kHalves = QUAD && !PAIR;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -264,7 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                       hdr->q_offset == p.q_offset &&
                       hdr->doc_ptr == reinterpret_cast<uint64_t>(p.doc_ids) &&
                       hdr->prefix_ptr == reinterpret_cast<uint64_t>(p.prefix_len) &&
-                      hdr->blocks_ptr == reinterpret_cast<uint64_t>(p.blocks);
+                      hdr->blocks_ptr == reinterpret_cast<uint64_t>(p.blocks) &&
+                      hdr->tiles_per_entry == kTpe;
   if (!hdr_ok) {
     if (threadIdx.x == 0 && atomicCAS(&p.status->code, 0, ATTN_ERR_DEVICE_CHECK) == 0) {
       p.status->where = kSiteHeader;
@@ -275,6 +339,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   }
   const int uniform = hdr->uniform;
   const int docs_sorted = hdr->docs_sorted;
+
+  // ---- CTA pair --------------------------------------------------------
+  // rank 0 issues every MMA of the pair; the work units of the persistent
+  // schedule are CTA pairs.  Query tile t of this CTA within an item is
+  // tile ci(t) of the block-mask entry.
+  const int rank = PAIR ? (int)ptx::cluster_ctarank() : 0;
+  auto ci = [&](const Item& it, int t) {
+    return PAIR ? 2 * t + rank : (kHalves ? 2 * it.half + t : t);
+  };
 
   // ---- shared memory map ------------------------------------------------
   auto bar = [&](int i) { return sbase + (uint32_t)(C::kSmemBar + 8 * i); };
@@ -296,10 +369,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       ptx::mbar_init(bar(B_KVE + s), 2);  // one commit per MMA issuer
     }
     for (int t = 0; t < 2; ++t) {
+      // P ready / O free: one arrival per softmax warp (of both CTAs of a
+      // pair, on rank 0's barriers)
       ptx::mbar_init(bar(B_SF + t), 1);
-      ptx::mbar_init(bar(B_PF + t), 4);  // one arrival per softmax warp
+      ptx::mbar_init(bar(B_PF + t), PAIR ? 8 : 4);
       ptx::mbar_init(bar(B_OF + t), 1);
-      ptx::mbar_init(bar(B_OE + t), 4);
+      ptx::mbar_init(bar(B_OE + t), PAIR ? 8 : 4);
     }
     ptx::mbar_init(bar(B_DRAIN), 2);
     ptx::mbar_init(bar(B_NEVER), 1);
@@ -308,16 +383,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     ptx::fence_mbar_init();
   }
   if (warp == kMmaWarp) {
-    ptx::tmem_alloc(ptx::smem_addr(s_tmem), kTmemCols);
-    ptx::tmem_relinquish();
+    // a pair allocates the same columns in both CTAs, one warp of each
+    if constexpr (PAIR) {
+      ptx::tmem_alloc_pair(ptx::smem_addr(s_tmem), kTmemCols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_addr(s_tmem), kTmemCols);
+      ptx::tmem_relinquish();
+    }
   }
   ptx::tc_fence_before();
-  __syncthreads();
+  // a pair's barriers must be initialised before the peer signals them
+  if constexpr (PAIR)
+    ptx::cluster_sync();
+  else
+    __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
   Ctl ctl{s_abort, sbase + (uint32_t)(C::kSmemMisc + 4), p.status, p.budget_ns};
   const uint32_t s_turn_smem = sbase + (uint32_t)(C::kSmemMisc + 8);
+  // rank 0's copy of barrier i (the pair's shared barriers live there)
+  auto bar0 = [&](int i) { return PAIR ? ptx::mapa(bar(i), 0u) : bar(i); };
 
   if (warp >= 8) {
     // Producer warpgroup: give registers away first (whole warpgroup).
@@ -326,15 +413,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // ===================== TMA producer: K / V ring ====================
       // Streams the key/value tiles of every item back to back, so the next
       // item's first tiles load while the current item finishes.
-      ptx::prefetch_tmap(&p.tmap_k);
+      // PAIR: each CTA loads its part of every tile (K: its 64 keys, V:
+      // its 64 columns) and the copies of both CTAs complete on rank 0's
+      // full barrier, which rank 0 arms for the bytes of both parts.
+      ptx::prefetch_tmap(PAIR ? &p.tmap_kh : &p.tmap_k);
       ptx::prefetch_tmap(&p.tmap_v);
       const uint64_t pol_kv = ptx::policy_evict_last();
       uint32_t kv_cnt = 0;
       bool ok = true;
       for (int r = 0; ok; ++r) {
-        const int w = item_of(r);
+        const int w = item_of<PAIR>(r);
         if (w >= p.n_items) break;
-        const Item it = decode_item(p, w, uniform);
+        const Item it = decode_item<kHalves>(p, w, uniform);
         const int n = p.cnt[it.e];
         if (n == 0) continue;
         const uint32_t* lst = p.list + (size_t)it.e * p.nK;
@@ -344,16 +434,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           for (int which = 0; which < 2; ++which) {
             const int st = (int)(kv_cnt % C::kStages);
             if (kv_cnt >= (uint32_t)C::kStages) {
-              ok = wait_bar(bar(B_KVE + st), ((kv_cnt / C::kStages) - 1) & 1, ctl,
-                            kSiteLoadKvEmpty);
+              ok = wait_bar<PAIR>(bar(B_KVE + st), ((kv_cnt / C::kStages) - 1) & 1, ctl,
+                                  kSiteLoadKvEmpty);
               if (!ok) break;
             }
-            ptx::mbar_arrive_expect_tx(bar(B_KVF + st), C::kTileBytes);
-            const CUtensorMap* map = which == 0 ? &p.tmap_k : &p.tmap_v;
+            const uint32_t dst = sbase + C::kSmemKV + st * C::kStageBytes;
+            if constexpr (PAIR) {
+              if (rank == 0) ptx::mbar_arrive_expect_tx(bar(B_KVF + st), 2 * C::kStageBytes);
+              const uint32_t cb = bar0(B_KVF + st);
+              if (which == 0) {
 #pragma unroll
-            for (int hx = 0; hx < C::kHalves; ++hx)
-              ptx::tma_load_3d(sbase + C::kSmemKV + st * C::kTileBytes + hx * C::kHalfBytes, map,
-                               bar(B_KVF + st), hx * 64, row0, kvz, pol_kv);
+                for (int hx = 0; hx < C::kHalves; ++hx)
+                  ptx::tma_load_3d_pair(dst + hx * C::kKPartHalfBytes, &p.tmap_kh, cb, hx * 64,
+                                        row0 + 64 * rank, kvz, pol_kv);
+              } else {
+                ptx::tma_load_3d_pair(dst, &p.tmap_v, cb, 64 * rank, row0, kvz, pol_kv);
+              }
+            } else {
+              ptx::mbar_arrive_expect_tx(bar(B_KVF + st), C::kTileBytes);
+              const CUtensorMap* map = which == 0 ? &p.tmap_k : &p.tmap_v;
+#pragma unroll
+              for (int hx = 0; hx < C::kHalves; ++hx)
+                ptx::tma_load_3d(dst + hx * C::kHalfBytes, map, bar(B_KVF + st), hx * 64, row0,
+                                 kvz, pol_kv);
+            }
             ++kv_cnt;
           }
         }
@@ -361,11 +465,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (!ok) {
         // Let the copies already issued land before the CTA exits: wait (with
         // a bound) for the last phase issued on every stage still in use.
-        const uint32_t first = kv_cnt > (uint32_t)C::kStages ? kv_cnt - C::kStages : 0;
-        for (uint32_t c = first; c < kv_cnt; ++c) {
+        // Rank 1 of a pair cannot see its copies complete (they count on
+        // rank 0's barriers) and waits a fixed time instead.
+        if (PAIR && rank != 0) {
           const uint64_t t0 = ptx::globaltimer_ns();
-          while (!ptx::mbar_try_wait(bar(B_KVF + (int)(c % C::kStages)), (c / C::kStages) & 1) &&
-                 ptx::globaltimer_ns() - t0 < ctl.budget_ns) {
+          while (ptx::globaltimer_ns() - t0 < kPeerDrainNs) {
+          }
+        } else {
+          const uint32_t first = kv_cnt > (uint32_t)C::kStages ? kv_cnt - C::kStages : 0;
+          for (uint32_t c = first; c < kv_cnt; ++c) {
+            const uint64_t t0 = ptx::globaltimer_ns();
+            while (!ptx::mbar_try_wait(bar(B_KVF + (int)(c % C::kStages)), (c / C::kStages) & 1) &&
+                   ptx::globaltimer_ns() - t0 < ctl.budget_ns) {
+            }
           }
         }
       }
@@ -373,39 +485,57 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // ===================== TMA producer: Q tiles =======================
       // Loads Q_t of the next item as soon as the last S_t MMA of the
       // current item has read its buffer, independently of the K/V stream.
+      // PAIR: each CTA loads its own query tiles; the copies complete on
+      // rank 0's barrier, armed by rank 0 for both CTAs' bytes.
       ptx::prefetch_tmap(&p.tmap_q);
       const uint64_t pol_q = ptx::policy_evict_first();
       int act = 0;
       bool ok = true;
       int q_phase[2] = {-1, -1};  // parity of the last Q_t load issued
       for (int r = 0; ok; ++r) {
-        const int w = item_of(r);
+        const int w = item_of<PAIR>(r);
         if (w >= p.n_items) break;
-        const Item it = decode_item(p, w, uniform);
+        const Item it = decode_item<kHalves>(p, w, uniform);
         if (p.cnt[it.e] == 0) continue;
         for (int t = 0; t < 2 && ok; ++t) {
-          if (act > 0) ok = wait_bar(bar(B_QE + t), (act - 1) & 1, ctl, kSiteLoadQEmpty);
+          if (act > 0) ok = wait_bar<PAIR>(bar(B_QE + t), (act - 1) & 1, ctl, kSiteLoadQEmpty);
           if (!ok) break;
-          const int row0 = (2 * it.pair + t) * kTileM;
-          ptx::mbar_arrive_expect_tx(bar(B_QF + t), C::kTileBytes);
+          const int row0 = (it.pair * kTpe + ci(it, t)) * kTileM;
+          const uint32_t dst = sbase + C::kSmemQ + t * C::kTileBytes;
+          if constexpr (PAIR) {
+            if (rank == 0) ptx::mbar_arrive_expect_tx(bar(B_QF + t), 2 * C::kTileBytes);
+            const uint32_t cb = bar0(B_QF + t);
 #pragma unroll
-          for (int hx = 0; hx < C::kHalves; ++hx)
-            ptx::tma_load_3d(sbase + C::kSmemQ + t * C::kTileBytes + hx * C::kHalfBytes,
-                             &p.tmap_q, bar(B_QF + t), hx * 64, row0, it.b * p.H + it.h, pol_q);
+            for (int hx = 0; hx < C::kHalves; ++hx)
+              ptx::tma_load_3d_pair(dst + hx * C::kHalfBytes, &p.tmap_q, cb, hx * 64, row0,
+                                    it.b * p.H + it.h, pol_q);
+          } else {
+            ptx::mbar_arrive_expect_tx(bar(B_QF + t), C::kTileBytes);
+#pragma unroll
+            for (int hx = 0; hx < C::kHalves; ++hx)
+              ptx::tma_load_3d(dst + hx * C::kHalfBytes, &p.tmap_q, bar(B_QF + t), hx * 64, row0,
+                               it.b * p.H + it.h, pol_q);
+          }
           q_phase[t] = act & 1;
         }
         ++act;
       }
       if (!ok) {
-        for (int t = 0; t < 2; ++t) {
-          if (q_phase[t] < 0) continue;
+        if (PAIR && rank != 0) {
           const uint64_t t0 = ptx::globaltimer_ns();
-          while (!ptx::mbar_try_wait(bar(B_QF + t), (uint32_t)q_phase[t]) &&
-                 ptx::globaltimer_ns() - t0 < ctl.budget_ns) {
+          while (ptx::globaltimer_ns() - t0 < kPeerDrainNs) {
+          }
+        } else {
+          for (int t = 0; t < 2; ++t) {
+            if (q_phase[t] < 0) continue;
+            const uint64_t t0 = ptx::globaltimer_ns();
+            while (!ptx::mbar_try_wait(bar(B_QF + t), (uint32_t)q_phase[t]) &&
+                   ptx::globaltimer_ns() - t0 < ctl.budget_ns) {
+            }
           }
         }
       }
-    } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    } else if ((warp == kMmaWarp || warp == kMmaWarp + 1) && rank == 0) {
       // ===================== MMA issuers =================================
       // Two issuing warps, one per query tile.  tcgen05.mma issue blocks
       // until the tensor pipe accepts the MMA, and every mbarrier wait costs
@@ -423,6 +553,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // deadlock.  The loop is warp-uniform (all lanes wait and compute the
       // same descriptors, one elected lane issues), which keeps descriptors
       // in uniform registers and the MMAs back to back.
+      //
+      // PAIR: only rank 0 issues; each MMA spans both CTAs, and each commit
+      // arrives on the barrier of that name in both CTAs (the peer's
+      // softmax and producers wait on their own copies).
       const int t = warp - kMmaWarp;
       const uint32_t tS = tmem + (uint32_t)(t * kTileN);
       const uint32_t tO = tmem + (uint32_t)(C::kOCol + t * D);
@@ -430,16 +564,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const uint64_t kv0 = (sbase + C::kSmemKV) >> 4;
       auto stage = [&](uint32_t idx) { return idx % C::kStages; };
       auto k_desc = [&](uint32_t idx) {
-        return Desc<D>::kKMajor + kv0 + (uint64_t)(stage(idx) * (C::kTileBytes >> 4));
+        return Desc<D>::kKMajor + kv0 + (uint64_t)(stage(idx) * (C::kStageBytes >> 4));
       };
       auto v_desc = [&](uint32_t idx) {
-        return Desc<D>::kVMajor + kv0 + (uint64_t)(stage(idx) * (C::kTileBytes >> 4));
+        return Desc<D>::kVMajor + kv0 + (uint64_t)(stage(idx) * (C::kStageBytes >> 4));
       };
       auto kv_full = [&](uint32_t idx) { return bar(B_KVF + (int)stage(idx)); };
       auto kv_empty = [&](uint32_t idx) { return bar(B_KVE + (int)stage(idx)); };
       auto kv_par = [&](uint32_t idx) { return (idx / C::kStages) & 1; };
       auto wait_all = [&](uint32_t b, uint32_t par, int site) {
-        return __all_sync(0xffffffffu, wait_bar(b, par, ctl, site));
+        return __all_sync(0xffffffffu, wait_bar<PAIR>(b, par, ctl, site));
+      };
+      auto commit = [&](uint32_t b) {
+        if constexpr (PAIR)
+          ptx::mma_commit_pair_elect(b, (uint16_t)0x3);
+        else
+          ptx::mma_commit_elect(b);
       };
       int grp = 0;  // groups this issuer has issued
       auto take_turn = [&]() -> bool {
@@ -455,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             if ((spin & 255) == 0) {
               if (ptx::ld_volatile_shared(ctl.abort_smem)) { got = false; break; }
               if (ptx::globaltimer_ns() - t0 > p.budget_ns) {
-                if (lane == 0) report(ctl, ATTN_ERR_TIMEOUT, kSiteMmaTurn, want);
+                if (lane == 0) report<PAIR>(ctl, ATTN_ERR_TIMEOUT, kSiteMmaTurn, want);
                 got = false;
                 break;
               }
@@ -474,9 +614,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       int act = 0;
       bool ok = true;
       for (int r = 0; ok; ++r) {
-        const int w = item_of(r);
+        const int w = item_of<PAIR>(r);
         if (w >= p.n_items) break;
-        const Item it = decode_item(p, w, uniform);
+        const Item it = decode_item<kHalves>(p, w, uniform);
         const int n = p.cnt[it.e];
         if (n == 0) continue;
         const uint32_t k0 = kv_cnt;
@@ -488,11 +628,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
              wait_all(kv_full(k0), kv_par(k0), kSiteMmaKvFull) && take_turn();
         if (!ok) break;
         ptx::tc_fence_after();
-        issue_s<D>(tS, q_desc, k_desc(k0));
+        issue_s<D, PAIR>(tS, q_desc, k_desc(k0));
         pass_turn();
-        ptx::mma_commit_elect(bar(B_SF + t));
-        if (n == 1) ptx::mma_commit_elect(bar(B_QE + t));
-        ptx::mma_commit_elect(kv_empty(k0));
+        commit(bar(B_SF + t));
+        if (n == 1) commit(bar(B_QE + t));
+        commit(kv_empty(k0));
         for (int j = 0; j < n && ok; ++j) {
           const uint32_t vi = k0 + 2 * j + 1;  // V_j
           const uint32_t ki = k0 + 2 * j + 2;  // K_{j+1}
@@ -509,16 +649,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           if (!ok) break;
           ++p_cnt;
           ptx::tc_fence_after();
-          issue_pv<D>(tO, tS, v_desc(vi), j > 0);
-          if (has_next) issue_s<D>(tS, q_desc, k_desc(ki));
+          issue_pv<D, PAIR>(tO, tS, v_desc(vi), j > 0);
+          if (has_next) issue_s<D, PAIR>(tS, q_desc, k_desc(ki));
           pass_turn();
-          ptx::mma_commit_elect(kv_empty(vi));
+          commit(kv_empty(vi));
           if (has_next) {
-            ptx::mma_commit_elect(bar(B_SF + t));
-            if (j + 2 == n) ptx::mma_commit_elect(bar(B_QE + t));
-            ptx::mma_commit_elect(kv_empty(ki));
+            commit(bar(B_SF + t));
+            if (j + 2 == n) commit(bar(B_QE + t));
+            commit(kv_empty(ki));
           } else {
-            ptx::mma_commit_elect(bar(B_OF + t));
+            commit(bar(B_OF + t));
           }
         }
         kv_cnt = k0 + 2 * (uint32_t)n;
@@ -526,7 +666,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       }
       // Wait for every MMA of both issuers before Tensor Memory is freed.
       __syncwarp();
-      ptx::mma_commit_elect(bar(B_DRAIN));
+      if constexpr (PAIR)
+        ptx::mma_commit_pair_elect(bar(B_DRAIN), (uint16_t)0x1);  // rank 0's barrier only
+      else
+        ptx::mma_commit_elect(bar(B_DRAIN));
       const uint64_t t0 = ptx::globaltimer_ns();
       bool drained = true;
       while (!ptx::mbar_try_wait(bar(B_DRAIN), 0)) {
@@ -536,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
       }
       if (!__all_sync(0xffffffffu, drained) && lane == 0)
-        report(ctl, ATTN_ERR_TIMEOUT, kSiteMmaDrain, 0);
+        report<PAIR>(ctl, ATTN_ERR_TIMEOUT, kSiteMmaDrain, 0);
     }
   } else {
     ptx::setmaxnreg_inc<kRegsSoftmax>();
@@ -549,15 +692,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const uint32_t tO = lane_base + (uint32_t)(C::kOCol + t * D);
     int* sdoc = s_doc + t * kTileN;
     const float tau = p.tau;
+    // P ready / O free: arrivals on rank 0's barriers in a CTA pair
+    auto arrive = [&](int i) {
+      if constexpr (PAIR)
+        ptx::mbar_arrive_cluster(bar0(i));
+      else
+        ptx::mbar_arrive(bar(i));
+    };
     uint32_t s_cnt = 0;
     int act = 0;
     bool ok = true;
     for (int r = 0; ok; ++r) {
-      const int w = item_of(r);
+      const int w = item_of<PAIR>(r);
       if (w >= p.n_items) break;
-      const Item it = decode_item(p, w, uniform);
+      const Item it = decode_item<kHalves>(p, w, uniform);
       const int n = p.cnt[it.e];
-      const int i = (2 * it.pair + t) * kTileM + row;  // query row
+      const int tc = ci(it, t);                             // tile of the entry
+      const int i = (it.pair * kTpe + tc) * kTileM + row;  // query row
       const bool valid = i < p.S_q;
       const size_t row_id = ((size_t)it.b * p.H + it.h) * (size_t)p.S_q + (size_t)i;
       __nv_bfloat16* orow = p.out + row_id * D;
@@ -619,9 +770,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       for (int j = 0; j < n && ok; ++j) {
         const uint32_t entry = lst[j];
         const int kt = (int)entry_tile(entry);
-        const uint32_t cls = entry_cls(entry, t);
+        const uint32_t cls = entry_cls(entry, tc);
         const int j0 = kt * kTileN;
-        bool got = wait_bar(bar(B_SF + t), s_cnt & 1, ctl, kSiteSmxSFull);
+        bool got = wait_bar<PAIR>(bar(B_SF + t), s_cnt & 1, ctl, kSiteSmxSFull);
         ok = __all_sync(0xffffffffu, got);
         if (!ok) break;
         ++s_cnt;
@@ -644,7 +795,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           ptx::tmem_wait_st();
           ptx::tc_fence_before();
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(bar(B_PF + t));
+          if (lane == 0) arrive(B_PF + t);
         } else {
           float tv[kTileN];
           {
@@ -831,7 +982,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           ptx::tmem_wait_st();
           ptx::tc_fence_before();
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(bar(B_PF + t));
+          if (lane == 0) arrive(B_PF + t);
           l += (la[0] + la[1]) + (la[2] + la[3]);
         }
       }
@@ -839,7 +990,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
       // ---- epilogue: O / l -> bf16, LSE --------------------------------
       {
-        bool got = wait_bar(bar(B_OF + t), act & 1, ctl, kSiteSmxOFull);
+        bool got = wait_bar<PAIR>(bar(B_OF + t), act & 1, ctl, kSiteSmxOFull);
         ok = __all_sync(0xffffffffu, got);
         if (!ok) break;
       }
@@ -867,19 +1018,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       }
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(B_OE + t));
+      if (lane == 0) arrive(B_OE + t);
       if (valid && p.lse) p.lse[row_id] = seen ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
       ++act;
     }
   }
 
   // ---- teardown --------------------------------------------------------
+  // A pair leaves together: rank 0's MMAs write the peer's Tensor Memory and
+  // signal its barriers, and the peer's copies signal rank 0's, so neither
+  // CTA frees or exits before both are done.
   ptx::tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    ptx::cluster_sync();
+  else
+    __syncthreads();
   if (warp == kMmaWarp) {
     __syncwarp();
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, kTmemCols);
+    if constexpr (PAIR)
+      ptx::tmem_dealloc_pair(tmem, kTmemCols);
+    else
+      ptx::tmem_dealloc(tmem, kTmemCols);
   }
 }
 
@@ -903,14 +1063,15 @@ EncodeTiledFn get_encode_tiled() {
   return fn;
 }
 
-// [rows_outer][S][D] bf16 viewed as 3-D (D, S, rows_outer); box 64 x 128 x 1
-// with 128-byte swizzle.  Rows beyond S read as zero.
-bool make_map(CUtensorMap* map, const void* ptr, int D, int S, int outer) {
+// [rows_outer][S][D] bf16 viewed as 3-D (D, S, rows_outer); box 64 x
+// box_rows x 1 with 128-byte swizzle.  Rows beyond S read as zero.
+bool make_map(CUtensorMap* map, const void* ptr, int D, int S, int outer,
+              int box_rows = kTileM) {
   EncodeTiledFn enc = get_encode_tiled();
   if (enc == nullptr) return false;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)outer};
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * (cuuint64_t)D * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)kTileM, 1};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -918,31 +1079,50 @@ bool make_map(CUtensorMap* map, const void* ptr, int D, int S, int outer) {
   return r == CUDA_SUCCESS;
 }
 
-template <int D, bool ALIBI, bool SOFTCAP>
+// grid: CTAs wanted (a CTA pair counts two); PAIR launches clusters of two
+// and caps the grid at the pairs that fit on the GPU at once, so that every
+// pair of the persistent schedule is resident.
+template <int D, bool ALIBI, bool SOFTCAP, bool PAIR, bool QUAD>
 cudaError_t launch_variant(const KParams& kp, int grid, cudaStream_t stream) {
-  auto kern = attn_fwd_kernel<D, ALIBI, SOFTCAP>;
+  auto kern = attn_fwd_kernel<D, ALIBI, SOFTCAP, PAIR, QUAD>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<D>::kSmemAlloc);
+                                         Cfg<D, PAIR>::kSmemAlloc);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<D>::kSmemAlloc;
+  cfg.dynamicSmemBytes = Cfg<D, PAIR>::kSmemAlloc;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if constexpr (PAIR) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+    int pairs = (grid + 1) / 2;
+    cfg.gridDim = dim3(2u * (unsigned)pairs, 1, 1);
+    int resident = 0;
+    err = cudaOccupancyMaxActiveClusters(&resident, kern, &cfg);
+    if (err != cudaSuccess) return err;
+    if (resident < 1) return cudaErrorInvalidConfiguration;
+    if (pairs > resident) pairs = resident;
+    cfg.gridDim = dim3(2u * (unsigned)pairs, 1, 1);
+  } else {
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  }
   return cudaLaunchKernelEx(&cfg, kern, kp);
 }
 
-template <int D>
+template <int D, bool PAIR, bool QUAD>
 cudaError_t launch_d(const KParams& kp, bool alibi, bool softcap, int grid, cudaStream_t s) {
-  if (alibi && softcap) return launch_variant<D, true, true>(kp, grid, s);
-  if (alibi) return launch_variant<D, true, false>(kp, grid, s);
-  if (softcap) return launch_variant<D, false, true>(kp, grid, s);
-  return launch_variant<D, false, false>(kp, grid, s);
+  if (alibi && softcap) return launch_variant<D, true, true, PAIR, QUAD>(kp, grid, s);
+  if (alibi) return launch_variant<D, true, false, PAIR, QUAD>(kp, grid, s);
+  if (softcap) return launch_variant<D, false, true, PAIR, QUAD>(kp, grid, s);
+  return launch_variant<D, false, false, PAIR, QUAD>(kp, grid, s);
 }
 
 }  // namespace
@@ -964,11 +1144,14 @@ cudaError_t launch_default_alibi_slopes(float* dst, int H, cudaStream_t stream) 
 cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
   KParams kp;
   memset(&kp, 0, sizeof(kp));
+  const bool pair = a.cta_pair != 0 && a.D == 128;
+  if (pair && a.tpe != kTilesPerQuad) return cudaErrorInvalidValue;
   if (!make_map(&kp.tmap_q, a.q, a.D, a.S_q, a.B * a.H) ||
       !make_map(&kp.tmap_k, a.k, a.D, a.S_k, a.B * a.H_kv) ||
-      !make_map(&kp.tmap_v, a.v, a.D, a.S_k, a.B * a.H_kv))
+      !make_map(&kp.tmap_v, a.v, a.D, a.S_k, a.B * a.H_kv) ||
+      !make_map(&kp.tmap_kh, a.k, a.D, a.S_k, a.B * a.H_kv, kTileN / 2))
     return cudaErrorInvalidValue;
-  BlockMaskGeom g = block_mask_geom(a.B, a.S_q, a.S_k, a.mask.flags);
+  BlockMaskGeom g = block_mask_geom(a.B, a.S_q, a.S_k, a.mask.flags, a.tpe);
   kp.out = reinterpret_cast<__nv_bfloat16*>(a.out);
   kp.lse = a.lse;
   kp.B = a.B;
@@ -1003,7 +1186,8 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
   kp.nP = g.nP;
   kp.bm = g.bm;
   kp.n_entries = g.n_entries;
-  kp.n_items = g.n_entries * (a.B / g.bm) * a.H;
+  const int sub = pair ? 1 : g.tpe / kTilesPerItem;  // work items per entry
+  kp.n_items = g.n_entries * (a.B / g.bm) * a.H * sub;
   kp.status = a.status;
   kp.tau = a.rescale_threshold;
   kp.budget_ns = (uint64_t)(a.wait_budget_ms * 1.0e6);
@@ -1018,15 +1202,19 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
   err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (err != cudaSuccess) return err;
   int grid = a.num_ctas > 0 ? a.num_ctas : sms;
-  if (grid > kp.n_items) grid = kp.n_items;
-  if (grid < 1) grid = 1;
+  const int per_unit = pair ? 2 : 1;  // CTAs per work unit
+  if (grid > kp.n_items * per_unit) grid = kp.n_items * per_unit;
+  if (grid < per_unit) grid = per_unit;
 
   // ALiBi and the bias table share one variant (additive position biases)
   const bool alibi = (a.score_flags & (ATTN_SCORE_ALIBI | ATTN_SCORE_RELBIAS)) != 0;
   const bool softcap = (a.score_flags & ATTN_SCORE_SOFTCAP) != 0;
-  if (a.D == 128) return launch_d<128>(kp, alibi, softcap, grid, stream);
-  if (a.D == 64) return launch_d<64>(kp, alibi, softcap, grid, stream);
-  return cudaErrorInvalidValue;
+  const bool quad = g.tpe == kTilesPerQuad;
+  if (a.D == 128 && pair) return launch_d<128, true, true>(kp, alibi, softcap, grid, stream);
+  if (a.D == 128 && !quad) return launch_d<128, false, false>(kp, alibi, softcap, grid, stream);
+  if (a.D == 64 && quad) return launch_d<64, false, true>(kp, alibi, softcap, grid, stream);
+  if (a.D == 64) return launch_d<64, false, false>(kp, alibi, softcap, grid, stream);
+  return cudaErrorInvalidValue;  // four-tile masks at D = 128 run on CTA pairs
 }
 
 }  // namespace attn

@@ -10,17 +10,20 @@
 
 namespace attn {
 
-// Tile shape: 128 query rows x 128 keys.  A work item is a pair of query
-// tiles (256 rows) processed in ping-pong by two softmax warpgroups.
+// Tile shape: 128 query rows x 128 keys.  A block-mask entry groups
+// kTilesPerItem query tiles (256 rows, the work of one CTA whose two softmax
+// warpgroups ping-pong) or, for the CTA-pair forward, kTilesPerQuad query
+// tiles (512 rows, the work of one CTA pair).
 constexpr int kTileM = 128;
 constexpr int kTileN = 128;
 constexpr int kTilesPerItem = 2;
+constexpr int kTilesPerQuad = 4;
 
 // Tile classes.
 enum TileClass : uint32_t { kEmpty = 0, kPartial = 1, kFull = 2 };
 
-// Entry of a pair's key-tile list: key tile index in bits 0..23, the class
-// for the first query tile in bits 24..25, for the second in bits 26..27.
+// Entry of an entry's key-tile list: key tile index in bits 0..23, then two
+// bits of class per query tile of the entry: tile t in bits 24 + 2t .. 25 + 2t.
 constexpr uint32_t kListIdxMask = 0x00FFFFFFu;
 __host__ __device__ inline uint32_t list_entry(uint32_t kt, uint32_t c0, uint32_t c1) {
   return kt | (c0 << 24) | (c1 << 26);
@@ -29,14 +32,14 @@ __host__ __device__ inline uint32_t entry_tile(uint32_t e) { return e & kListIdx
 __host__ __device__ inline uint32_t entry_cls(uint32_t e, int t) { return (e >> (24 + 2 * t)) & 3u; }
 
 constexpr uint32_t kBlockMaskMagic = 0x4B4D4241u;  // "ABMK"
-constexpr uint32_t kBlockMaskVersion = 1u;
+constexpr uint32_t kBlockMaskVersion = 2u;
 
 // Device block-mask buffer: header, then order[], cnt[], list[][nK].
 struct BlockMaskHeader {
   uint32_t magic;
   uint32_t version;
   int32_t B, S_q, S_k;
-  int32_t nQ, nK, nP;       // query tiles, key tiles, query-tile pairs
+  int32_t nQ, nK, nP;       // query tiles, key tiles, entries per mask batch
   int32_t bm;               // batches the mask depends on (B or 1)
   int32_t n_entries;        // bm * nP
   uint32_t mask_flags;
@@ -51,13 +54,14 @@ struct BlockMaskHeader {
   uint64_t total_bytes;
   uint64_t doc_off;         // DOCUMENT: int32 doc_lo[bm][S_k], doc_hi[bm][S_k]
   int32_t docs_sorted;      // 1: every batch's doc ids are non-decreasing
-  int32_t pad_;
+  int32_t tiles_per_entry;  // query tiles per entry: kTilesPerItem or kTilesPerQuad
   uint64_t blocks_ptr;      // BLOCKS: the block map the mask was built from
   uint64_t pad2_;
 };
 static_assert(sizeof(BlockMaskHeader) % 16 == 0, "header alignment");
 
 struct BlockMaskGeom {
+  int tpe;  // query tiles per entry
   int nQ, nK, nP, bm, n_entries;
   size_t order_off, cnt_off, list_off;
   size_t doc_off;   // DOCUMENT only: per-token document key interval
@@ -79,11 +83,13 @@ inline bool mask_per_batch(uint32_t mask_flags) {
   return (mask_flags & (ATTN_MASK_DOCUMENT | ATTN_MASK_PREFIX_LM | kMaskBlocksBatched)) != 0;
 }
 
-inline BlockMaskGeom block_mask_geom(int B, int S_q, int S_k, uint32_t mask_flags) {
+inline BlockMaskGeom block_mask_geom(int B, int S_q, int S_k, uint32_t mask_flags,
+                                     int tpe = kTilesPerItem) {
   BlockMaskGeom g;
+  g.tpe = tpe;
   g.nQ = (S_q + kTileM - 1) / kTileM;
   g.nK = (S_k + kTileN - 1) / kTileN;
-  g.nP = (g.nQ + kTilesPerItem - 1) / kTilesPerItem;
+  g.nP = (g.nQ + tpe - 1) / tpe;
   g.bm = mask_per_batch(mask_flags) ? B : 1;
   g.n_entries = g.bm * g.nP;
   g.order_off = align_up(sizeof(BlockMaskHeader), 16);
@@ -144,8 +150,11 @@ struct DeviceStatus {
 };
 
 // Launchers (defined in the .cu files, called by the host API).
+// tpe: query tiles per entry (kTilesPerItem, or kTilesPerQuad for the
+// CTA-pair forward).
 cudaError_t launch_build_block_mask(int B, int S_q, int S_k, const MaskParams& mp,
-                                    int force_partial, void* dst, cudaStream_t stream);
+                                    int force_partial, void* dst, cudaStream_t stream,
+                                    int tpe = kTilesPerItem);
 
 // Builds the transposed block mask into dst_t from the block mask fwd_mask
 // already built (on the same stream) for the same problem.
@@ -175,6 +184,8 @@ struct FwdArgs {
   float rescale_threshold;
   double wait_budget_ms;
   int num_ctas;                // 0 = SM count
+  int cta_pair;                // D = 128: CTA-pair kernel (block mask of quads)
+  int tpe;                     // query tiles per block-mask entry
   float poly_fraction;
   int debug_stall;             // test hook: MMA issuers wait on a barrier nothing arrives on
 };

@@ -101,15 +101,16 @@ __device__ uint32_t classify_tile(int r0, int r1, int c0, long long pl, const Ma
   return all ? kFull : kPartial;
 }
 
-// One block per (batch entry, query-tile pair).  Writes cnt[e] and the
-// compacted list of non-empty key tiles in descending key-tile order, one
-// key tile per thread, kClassifyThreads tiles at a time.
+// One block per (batch entry, group of g.tpe query tiles).  Writes cnt[e]
+// and the compacted list of key tiles that are non-empty for some query tile
+// of the group, in descending key-tile order, one key tile per thread,
+// kClassifyThreads tiles at a time.
 __global__ void __launch_bounds__(kClassifyThreads) classify_kernel(BlockMaskHeader* hdr_out,
                                                                      MaskParams mp,
                                                                      BlockMaskGeom g,
                                                                      int force_partial) {
   constexpr int kWarps = kClassifyThreads / 32;
-  const int nQ = g.nQ, nK = g.nK, nP = g.nP;
+  const int nQ = g.nQ, nK = g.nK, nP = g.nP, tpe = g.tpe;
   const int e = blockIdx.x;
   const int bb = e / nP;  // batch of this entry (0 when the mask is batch-independent)
   const int p = e % nP;
@@ -129,12 +130,13 @@ __global__ void __launch_bounds__(kClassifyThreads) classify_kernel(BlockMaskHea
   const long long pl = (mp.flags & ATTN_MASK_PREFIX_LM) ? mp.prefix_len[bb] : 0;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
-  int r0[2], r1[2];
-  Range dq[2];
-  for (int t = 0; t < 2; ++t) {
-    const int qt = 2 * p + t;
+  int r0[kTilesPerQuad], r1[kTilesPerQuad];
+  Range dq[kTilesPerQuad];
+#pragma unroll
+  for (int t = 0; t < kTilesPerQuad; ++t) {
+    const int qt = tpe * p + t;
     r0[t] = qt * kTileM;
-    r1[t] = (qt < nQ) ? min(r0[t] + kTileM - 1, mp.S_q - 1) : r0[t] - 1;
+    r1[t] = (t < tpe && qt < nQ) ? min(r0[t] + kTileM - 1, mp.S_q - 1) : r0[t] - 1;
     dq[t] = (docs && r0[t] <= r1[t]) ? Range{t_lo[qt], t_hi[qt]} : Range{0, 0};
   }
 
@@ -147,18 +149,17 @@ __global__ void __launch_bounds__(kClassifyThreads) classify_kernel(BlockMaskHea
       const int kt = nK - 1 - idx;
       const int c0 = kt * kTileN;
       const Range dk = docs ? Range{t_lo[kt], t_hi[kt]} : Range{0, 0};
-      uint32_t c_0 = block_open(mp, bb, 2 * p, kt, nQ, nK)
-                         ? classify_tile(r0[0], r1[0], c0, pl, mp, dq[0], dk)
+      entry = (uint32_t)kt;
+#pragma unroll
+      for (int t = 0; t < kTilesPerQuad; ++t) {
+        // rows past the group or past S_q: r1 < r0, classified EMPTY
+        uint32_t c = (r0[t] <= r1[t] && block_open(mp, bb, tpe * p + t, kt, nQ, nK))
+                         ? classify_tile(r0[t], r1[t], c0, pl, mp, dq[t], dk)
                          : kEmpty;
-      uint32_t c_1 = (2 * p + 1 < nQ && block_open(mp, bb, 2 * p + 1, kt, nQ, nK))
-                         ? classify_tile(r0[1], r1[1], c0, pl, mp, dq[1], dk)
-                         : kEmpty;
-      if (force_partial) {
-        if (c_0 == kFull) c_0 = kPartial;
-        if (c_1 == kFull) c_1 = kPartial;
+        if (force_partial && c == kFull) c = kPartial;
+        keep |= c != kEmpty;
+        entry |= c << (24 + 2 * t);
       }
-      keep = (c_0 != kEmpty) || (c_1 != kEmpty);
-      entry = list_entry((uint32_t)kt, c_0, c_1);
     }
     // stable compaction within the chunk: warp ballots + block prefix
     const unsigned ball = __ballot_sync(0xffffffffu, keep);
@@ -398,7 +399,7 @@ __global__ void __launch_bounds__(kBuildThreads) order_kernel(BlockMaskHeader* h
     h.total_bytes = g.total;
     h.doc_off = g.doc_off;
     h.docs_sorted = (g.flag_off != 0 && !disorder) ? 1 : 0;
-    h.pad_ = 0;
+    h.tiles_per_entry = g.tpe;
     h.blocks_ptr = reinterpret_cast<uint64_t>(mp.blocks);
     h.pad2_ = 0;
     *hdr = h;
@@ -427,8 +428,8 @@ cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, int threads, cudaStre
 }  // namespace
 
 cudaError_t launch_build_block_mask(int B, int S_q, int S_k, const MaskParams& mp,
-                                    int force_partial, void* dst, cudaStream_t stream) {
-  BlockMaskGeom g = block_mask_geom(B, S_q, S_k, mp.flags);
+                                    int force_partial, void* dst, cudaStream_t stream, int tpe) {
+  BlockMaskGeom g = block_mask_geom(B, S_q, S_k, mp.flags, tpe);
   BlockMaskHeader* hdr = reinterpret_cast<BlockMaskHeader*>(dst);
   char* base = reinterpret_cast<char*>(dst);
   cudaError_t err;

@@ -257,6 +257,19 @@ def time_workload(attn, w, inp, dev, steps, warmup):
     return total_ms / steps, statistics.mean(kern_ms), statistics.median(kern_ms)
 
 
+def time_pair(attn, w, inp, dev, steps, warmup, flops, peak):
+    """The same steps with the CTA-pair forward (option cta_pair; D = 128):
+    its step time and the pair kernel's own throughput."""
+    attn.set_option("cta_pair", 1)
+    try:
+        ms, kms, _ = time_workload(attn, w, inp, dev, steps, warmup)
+    finally:
+        attn.set_option("cta_pair", 0)
+    kt = flops / (kms * 1e-3) / 1e12
+    return {"pair_ms_per_step": ms, "pair_kernel_ms": kms, "pair_kernel_tflops": kt,
+            "pair_frac": kt / peak}
+
+
 def time_backward(attn, w, inp, dev, steps, warmup):
     """Device time of one attn_bwd call (block masks, row statistics, dQ and
     dK/dV kernels) on resident inputs, after the forward produced O and LSE."""
@@ -491,6 +504,9 @@ def main():
                              "ms_per_step": ms_step, "frac": achieved / peak}
                 bms = time_backward(attn, w, inp, dev, bsteps, 3)
                 per[name].update(bwd_ms=bms, bwd_tflops=2.5 * flops / (bms * 1e-3) / 1e12)
+                if w.D == 128:
+                    per[name].update(time_pair(attn, w, inp, dev, min(max(5, args.steps // 4), 500),
+                                               3, flops, peak))
                 continue
             ix = workloads.generate(wx)
             px = visible_pairs(wx, ix.get("doc_ids"), ix.get("prefix_len"))
@@ -505,6 +521,9 @@ def main():
             # recomputed S and dP over the visible pairs, the usual count)
             bms = time_backward(attn, wx, ix, dev, bsteps, 3)
             per[name].update(bwd_ms=bms, bwd_tflops=2.5 * fx / (bms * 1e-3) / 1e12)
+            if wx.D == 128:
+                per[name].update(time_pair(attn, wx, ix, dev, min(max(5, args.steps // 4), 500), 3,
+                                           fx, peak))
             del ix
         # the descriptor mods of the next-step row on the headline shape
         pm, fm, bmm = time_mods3(attn, w, inp, dev, min(max(5, args.steps // 4), 200), 3)

@@ -364,7 +364,19 @@ typedef enum attn_option {
      * lets its in-flight copies land, frees Tensor Memory and returns, with
      * unspecified outputs.  Lets tests exercise the timeout path without any
      * real fault or hang. */
-    ATTN_OPT_DEBUG_STALL = 6
+    ATTN_OPT_DEBUG_STALL = 6,
+    /* 1: forwards with D = 128 run on CTA pairs (thread-block clusters of
+     * two): the two CTAs of a pair issue their score and output products
+     * as single 256-row tcgen05 MMAs (cta_group::2), each CTA staging its
+     * own 128 query rows and half of every key / value tile ("FlashAttention-4
+     * explained", "TMEM and 2-CTA MMA", "2-CTA MMA mode").  Block masks built
+     * while the option is 1 group four query tiles per entry instead of two
+     * (attn_block_mask_bytes changes accordingly); a block mask must be used
+     * under the setting it was built with, else the forward records
+     * ATTN_ERR_DEVICE_CHECK.  Forwards with D = 64 use the one-CTA kernel
+     * on such masks.  Both settings meet the same accuracy bounds against
+     * exact attention.  Default 0. */
+    ATTN_OPT_CTA_PAIR = 7
 } attn_option;
 
 attn_status attn_set_option(attn_option opt, double value);

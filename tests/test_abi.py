@@ -176,3 +176,26 @@ def test_options_round_trip(attn):
     with pytest.raises(attn.AttnError):
         attn.set_option("debug_stall", 2)
     assert attn.get_option("debug_stall") == 0
+
+
+def test_cta_pair_option_sets_mask_geometry(attn):
+    # With the CTA-pair option a block-mask entry groups four query tiles
+    # instead of two: half the entries, the same key-tile rows each.
+    lib = attn.lib()
+    m = attn.ModDesc()
+    m.version = 1
+    m.mask_flags = attn.MASK_CAUSAL
+    assert attn.get_option("cta_pair") == 0
+    n2 = lib.attn_block_mask_bytes(1, 8, 8192, 8192, ctypes.byref(m))
+    try:
+        attn.set_option("cta_pair", 1)
+        assert attn.get_option("cta_pair") == 1
+        n4 = lib.attn_block_mask_bytes(1, 8, 8192, 8192, ctypes.byref(m))
+    finally:
+        attn.set_option("cta_pair", 0)
+    # 64 query tiles, 64 key tiles: 32 entries of 64 list slots vs 16
+    assert n2 - n4 >= 16 * 64 * 4
+    assert lib.attn_block_mask_bytes(1, 8, 8192, 8192, ctypes.byref(m)) == n2
+    with pytest.raises(attn.AttnError):
+        attn.set_option("cta_pair", 0.5)
+    assert attn.get_option("cta_pair") == 0
