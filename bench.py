@@ -450,6 +450,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=8.0)
+    ap.add_argument("--cta-pair", action="store_true",
+                    help="run the timed forward on CTA pairs (option cta_pair, D = 128)")
     args = ap.parse_args()
     world, rank, local = dist_init()
     if args.impl == "reference":
@@ -459,6 +461,8 @@ def main():
         raise SystemExit("--warmup must be >= 3")
 
     import attention_attn_fwd_04_gb300 as attn
+    if args.cta_pair:
+        attn.set_option("cta_pair", 1)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     peaks, peak_kind = load_peaks()
@@ -547,6 +551,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "H_kv": w.H_kv, "S": w.S_q,
                        "D": w.D, "parallelism": "replicas" if world > 1 else "single",
+                       "cta_pair": bool(args.cta_pair),
                        "l2": "inputs larger than L2 (%d MB of Q/K/V)"
                              % (algorithmic_bytes(w) // 2**20),
                        "useful_flops": flops, "visible_pairs": pairs},
