@@ -29,10 +29,18 @@
 // Neither kernel uses atomics: every output row is written once by the work
 // item that owns it, so results are deterministic.
 //
-// Warp roles (256 threads): warps 0-3 elementwise (one TMEM lane quarter
-// each), warp 4 TMA loads, warp 5 allocates Tensor Memory and issues the
-// MMAs, warps 6-7 only join the teardown.  Every wait is bounded like the
-// forward's: on expiry the kernel records ATTN_ERR_TIMEOUT and returns.
+// Warp roles (320 threads): warps 0-7 elementwise in two warpgroups, warp 8
+// TMA loads, warp 9 allocates Tensor Memory and issues the MMAs.  Warps w
+// and w + 4 share Tensor Memory lane quarter w & 3 (32 rows of the tile) and
+// split its 128 columns: warpgroup 0 takes columns [0, 64), warpgroup 1
+// [64, 128).  No elementwise step reduces along a row (P = exp(S - LSE) with
+// LSE known, dS = P (dP - Delta) with Delta known), so the halves are
+// independent, and two warps per SM sub-partition hide each other's latency.
+// Each half packs its bf16 results (P^T, dS, dS^T) over its own columns,
+// half 0 at packed columns [32, 64) and half 1 at [64, 96), so the packed
+// 128-wide operand is contiguous at column 32 for the MMA that reads it.
+// Every wait is bounded like the forward's: on expiry the kernel records
+// ATTN_ERR_TIMEOUT and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -45,9 +53,11 @@ namespace attn {
 
 namespace {
 
-constexpr int kBThreads = 256;
-constexpr int kBLoadWarp = 4;
-constexpr int kBMmaWarp = 5;
+constexpr int kBThreads = 320;
+constexpr int kBLoadWarp = 8;
+constexpr int kBMmaWarp = 9;
+constexpr int kBCols = 64;      // columns of a tile per elementwise half
+constexpr uint32_t kBPack = 32;  // packed operand: Tensor Memory columns [32, 96)
 constexpr uint32_t kBTmemCols = 512;
 constexpr float kBLog2e = 1.4426950408889634f;
 
@@ -230,19 +240,19 @@ __device__ __forceinline__ ScoreMod make_mod(const BParams& p, int h) {
   return m;
 }
 
-// Adds the relative-position bias of head h to raw scores tv[0..127] whose
+// Adds the relative-position bias of head h to raw scores tv[0..N-1] whose
 // relative positions (kpos - qpos) are pos0 + step * c, pre-divided by the
 // score scale so that score_t applies it as table * (units of t); a
 // uniform branch around its own loop keeps the other loops branch-free.
-template <bool ALIBI, bool SOFTCAP>
-__device__ __forceinline__ void add_rel_bias(float (&tv)[128], const BParams& p, int h, int pos0,
+template <bool ALIBI, bool SOFTCAP, int N>
+__device__ __forceinline__ void add_rel_bias(float (&tv)[N], const BParams& p, int h, int pos0,
                                              int step, const ScoreMod& m) {
   if constexpr (ALIBI) {
     if (p.rel_bias == nullptr) return;
     const float* row = p.rel_bias + (size_t)h * (2 * (size_t)p.rel_max + 1);
     const float rs = (SOFTCAP ? 2.0f * kBLog2e / p.softcap : kBLog2e) / m.sc;
     // beyond +-R of every position of the warp the clamped bias is one entry
-    const int lo_r = min(pos0, pos0 + step * 127), hi_r = max(pos0, pos0 + step * 127);
+    const int lo_r = min(pos0, pos0 + step * (N - 1)), hi_r = max(pos0, pos0 + step * (N - 1));
     float cst = 0.f;
     bool flat = true;
     if (__all_sync(0xffffffffu, hi_r <= -p.rel_max)) {
@@ -255,11 +265,11 @@ __device__ __forceinline__ void add_rel_bias(float (&tv)[128], const BParams& p,
     if (flat) {
       const float add = cst * rs;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) tv[c] += add;
+      for (int c = 0; c < N; ++c) tv[c] += add;
       return;
     }
 #pragma unroll
-    for (int c = 0; c < 128; ++c) {
+    for (int c = 0; c < N; ++c) {
       const int r = min(max(pos0 + step * c, -p.rel_max), p.rel_max);
       tv[c] = fmaf(__ldg(row + r + p.rel_max), rs, tv[c]);
     }
@@ -369,12 +379,13 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
       ptx::mbar_init(bar(KVF + s), 1);
       ptx::mbar_init(bar(KVE + s), 1);
     }
+    // one arrival per elementwise warp
     ptx::mbar_init(bar(SF), 1);
-    ptx::mbar_init(bar(DSF), 4);
+    ptx::mbar_init(bar(DSF), 8);
     ptx::mbar_init(bar(DQF), 1);
-    ptx::mbar_init(bar(DQE), 4);
+    ptx::mbar_init(bar(DQE), 8);
     ptx::mbar_init(bar(DPF), 1);
-    ptx::mbar_init(bar(SCON), 4);
+    ptx::mbar_init(bar(SCON), 8);
     ptx::mbar_init(bar(DRAIN), 1);
     *s_abort = 0;
     ptx::fence_mbar_init();
@@ -513,7 +524,7 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
         if (!ok) break;
         ++ds_cnt;
         ptx::tc_fence_after();
-        mma_tn<D>(tQ, tP, BDesc<D>::kMNMajor + (kaddr(u) >> 4), u > 0);  // dQ += dS K
+        mma_tn<D>(tQ, tP + kBPack, BDesc<D>::kMNMajor + (kaddr(u) >> 4), u > 0);  // dQ += dS K
         ptx::mma_commit_elect(bar(KVE + ((kv0 + u) & 1)));
         if (u + 1 < m) {
           mma_nt<D>(tP, do_desc, BDesc<D>::kKMajor + ((kaddr(u + 1) + C::kTileBytes) >> 4));
@@ -538,11 +549,17 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
       }
     }
     if (!__all_sync(0xffffffffu, drained) && lane == 0) breport(ctl, ATTN_ERR_TIMEOUT, kBSiteDrain, 0);
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ===================== elementwise: one thread per query row =========
-    const int row = warp * 32 + lane;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    const uint32_t tS = lane_base, tP = lane_base + 128u, tQ = lane_base + 256u;
+    // half 0: key columns [0, 64) of each tile, half 1: [64, 128); the dQ
+    // epilogue splits the D columns the same way
+    const int half = warp >> 2, wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const int cb = kBCols * half;
+    const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+    const uint32_t tS = lane_base + (uint32_t)cb, tP = lane_base + 128u + (uint32_t)cb,
+                   tPk = lane_base + 128u + kBPack + 32u * (uint32_t)half,
+                   tQ = lane_base + 256u + (uint32_t)(half * D / 2);
     uint32_t s_cnt = 0;
     int act = 0;
     bool ok = true;
@@ -553,12 +570,12 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
       const int i = it.qt * kTileM + row;
       const bool valid = i < p.S_q;
       const size_t bh = (size_t)it.b * p.H + it.h;
-      __nv_bfloat16* dqrow = p.dq + (bh * p.S_q + (size_t)i) * D;
+      __nv_bfloat16* dqrow = p.dq + (bh * p.S_q + (size_t)i) * D + half * (D / 2);
       if (nonempty(it) == 0) {
         if (valid) {
           const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(dqrow)[c] = z;
+          for (int c = 0; c < D / 16; ++c) reinterpret_cast<uint4*>(dqrow)[c] = z;
         }
         continue;
       }
@@ -575,7 +592,7 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
       for (int j = 0; j < it.n && ok; ++j) {
         const uint32_t cls = entry_cls(it.lst[j], it.t);
         if (cls == kEmpty) continue;
-        const int j0 = (int)entry_tile(it.lst[j]) * kTileN;
+        const int j0 = (int)entry_tile(it.lst[j]) * kTileN + cb;  // first key of this half
         {
           const bool got = bwait(bar(SF), s_cnt & 1, ctl, kBSiteElem);
           ok = __all_sync(0xffffffffu, got);
@@ -583,37 +600,34 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
         }
         ++s_cnt;
         ptx::tc_fence_after();
-        // S of the whole tile into registers, then release it for S(u+1)
-        // modified scores, 64 columns per load (fewer live registers); the
-        // mask then runs in a loop of its own (a branch per element would
-        // split the unrolled loop and serialise the exponentials)
-        float tv[kTileN];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+        // this half of S into registers, then release it for S(u+1); the
+        // modified scores, then the mask in a loop of its own (a branch per
+        // element would split the unrolled loop and serialise the
+        // exponentials)
+        float tv[kBCols];
+        {
           uint32_t ra[32], rb[32];
-          ptx::tmem_ld32(tS + (uint32_t)(64 * hh), ra);
-          ptx::tmem_ld32(tS + (uint32_t)(64 * hh + 32), rb);
+          ptx::tmem_ld32(tS, ra);
+          ptx::tmem_ld32(tS + 32u, rb);
           ptx::tmem_wait_ld();
-          if (hh == 1) {  // all of S is in registers: release it for S(u+1)
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(SCON));
-          }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bar(SCON));
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            tv[64 * hh + c] = __uint_as_float(ra[c]);
-            tv[64 * hh + 32 + c] = __uint_as_float(rb[c]);
+            tv[c] = __uint_as_float(ra[c]);
+            tv[32 + c] = __uint_as_float(rb[c]);
           }
         }
-        add_rel_bias<ALIBI, SOFTCAP>(tv, p, it.h, j0 - qpos, 1, md);
+        add_rel_bias<ALIBI, SOFTCAP, kBCols>(tv, p, it.h, j0 - qpos, 1, md);
 #pragma unroll
-        for (int c = 0; c < kTileN; ++c)
+        for (int c = 0; c < kBCols; ++c)
           tv[c] = score_t<ALIBI, SOFTCAP>(tv[c], (float)(j0 + c - qpos), md);
         if (cls == kPartial) {
           const int clo = lo - j0, chi = hi - j0;
           if (has_doc) {
 #pragma unroll
-            for (int c = 0; c < kTileN; ++c) {
+            for (int c = 0; c < kBCols; ++c) {
               const int jj = j0 + c;
               const bool vis = (c >= clo) & (c <= chi) & (jj < p.S_k) &&
                                doc_b[jj < p.S_k ? jj : 0] == doc_i;
@@ -621,12 +635,12 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
             }
           } else {
 #pragma unroll
-            for (int c = 0; c < kTileN; ++c) tv[c] = ((c >= clo) & (c <= chi)) ? tv[c] : -INFINITY;
+            for (int c = 0; c < kBCols; ++c) tv[c] = ((c >= clo) & (c <= chi)) ? tv[c] : -INFINITY;
           }
         }
         // P (times the soft cap's derivative), in place, while dP computes
 #pragma unroll
-        for (int c = 0; c < kTileN; ++c) {
+        for (int c = 0; c < kBCols; ++c) {
           float pr = ptx::ex2_approx(tv[c] - lse2);
           if constexpr (SOFTCAP) {  // masked: t = -inf, clamped so the factor is 0
             const float uu = fmaxf(tv[c], -md.capl2) / md.capl2;
@@ -640,20 +654,22 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
           if (!ok) break;
         }
         ptx::tc_fence_after();
-        // dS = P (dP - Delta), 32 columns at a time, packed over dP's columns
-#pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          uint32_t dp[32];
-          ptx::tmem_ld32(tP + (uint32_t)(32 * k4), dp);
+        // dS = P (dP - Delta): this half's 64 columns of dP, then 32 packed
+        // columns over them
+        {
+          uint32_t d0[32], d1[32], pk[32];
+          ptx::tmem_ld32(tP, d0);
+          ptx::tmem_ld32(tP + 32u, d1);
           ptx::tmem_wait_ld();
-          uint32_t pk[16];
 #pragma unroll
           for (int c2 = 0; c2 < 16; ++c2) {
-            const int c = 32 * k4 + 2 * c2;
-            pk[c2] = ptx::pack_bf16x2(tv[c] * (__uint_as_float(dp[2 * c2]) - dlt),
-                                      tv[c + 1] * (__uint_as_float(dp[2 * c2 + 1]) - dlt));
+            pk[c2] = ptx::pack_bf16x2(tv[2 * c2] * (__uint_as_float(d0[2 * c2]) - dlt),
+                                      tv[2 * c2 + 1] * (__uint_as_float(d0[2 * c2 + 1]) - dlt));
+            pk[16 + c2] =
+                ptx::pack_bf16x2(tv[32 + 2 * c2] * (__uint_as_float(d1[2 * c2]) - dlt),
+                                 tv[33 + 2 * c2] * (__uint_as_float(d1[2 * c2 + 1]) - dlt));
           }
-          ptx::tmem_st16(tP + (uint32_t)(16 * k4), pk);
+          ptx::tmem_st32(tPk, pk);
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
@@ -668,7 +684,7 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
       }
       ptx::tc_fence_after();
 #pragma unroll
-      for (int c4 = 0; c4 < D / 32; ++c4) {
+      for (int c4 = 0; c4 < D / 64; ++c4) {
         uint32_t o[32];
         ptx::tmem_ld32(tQ + (uint32_t)(c4 * 32), o);
         ptx::tmem_wait_ld();
@@ -724,12 +740,13 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
       ptx::mbar_init(bar(QF + s), 1);
       ptx::mbar_init(bar(QE + s), 1);
     }
+    // one arrival per elementwise warp
     ptx::mbar_init(bar(SF), 1);
-    ptx::mbar_init(bar(PF), 4);
+    ptx::mbar_init(bar(PF), 8);
     ptx::mbar_init(bar(AF), 1);
-    ptx::mbar_init(bar(AE), 4);
+    ptx::mbar_init(bar(AE), 8);
     ptx::mbar_init(bar(DPF), 1);
-    ptx::mbar_init(bar(DSF), 4);
+    ptx::mbar_init(bar(DSF), 8);
     ptx::mbar_init(bar(DRAIN), 1);
     *s_abort = 0;
     ptx::fence_mbar_init();
@@ -860,7 +877,8 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
         if (!ok) break;
         ++p_cnt;
         ptx::tc_fence_after();
-        mma_tn<D>(tDV, tST, BDesc<D>::kMNMajor + ((qaddr(u) + C::kTileBytes) >> 4), u > 0);  // dV
+        mma_tn<D>(tDV, tST + kBPack, BDesc<D>::kMNMajor + ((qaddr(u) + C::kTileBytes) >> 4),
+                  u > 0);  // dV += P^T dO
         if (u + 1 < units) {
           ok = q_ready(u + 1);
           if (!ok) break;
@@ -872,7 +890,7 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
         if (!ok) break;
         ++ds_cnt;
         ptx::tc_fence_after();
-        mma_tn<D>(tDK, tDPT, BDesc<D>::kMNMajor + (qaddr(u) >> 4), u > 0);  // dK += dS^T Q
+        mma_tn<D>(tDK, tDPT + kBPack, BDesc<D>::kMNMajor + (qaddr(u) >> 4), u > 0);  // dK += dS^T Q
         ptx::mma_commit_elect(bar(QE + (int)((q0 + (uint32_t)u) & 1)));
         if (u + 1 < units) {
           mma_nt<D>(tDPT, v_kmaj, BDesc<D>::kKMajor + ((qaddr(u + 1) + C::kTileBytes) >> 4));
@@ -896,12 +914,19 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
       }
     }
     if (!__all_sync(0xffffffffu, drained) && lane == 0) breport(ctl, ATTN_ERR_TIMEOUT, kBSiteDrain, 0);
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ===================== elementwise: one thread per key ================
-    const int row = warp * 32 + lane;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
-    const uint32_t tST = lane_base, tDPT = lane_base + 128u, tDV = lane_base + 256u,
-                   tDK = lane_base + 256u + D;
+    // half 0: query columns [0, 64) of each tile, half 1: [64, 128); the
+    // dK / dV epilogue splits the D columns the same way
+    const int half = warp >> 2, wq = warp & 3;
+    const int row = wq * 32 + lane;
+    const int cb = kBCols * half;
+    const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+    const uint32_t tST = lane_base + (uint32_t)cb, tDPT = lane_base + 128u + (uint32_t)cb,
+                   tPk = lane_base + kBPack + 32u * (uint32_t)half,
+                   tDSk = lane_base + 128u + kBPack + 32u * (uint32_t)half,
+                   tDV = lane_base + 256u + (uint32_t)(half * D / 2),
+                   tDK = lane_base + 256u + D + (uint32_t)(half * D / 2);
     uint32_t q_cnt = 0;
     int act = 0;
     bool ok = true;
@@ -912,13 +937,13 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
       const int j = it.kt * kTileN + row;  // this thread's key
       const bool valid = j < p.S_k;
       const size_t kvh = (size_t)it.b * p.H_kv + it.hk;
-      __nv_bfloat16* dkrow = p.dk + (kvh * p.S_k + (size_t)j) * D;
-      __nv_bfloat16* dvrow = p.dv + (kvh * p.S_k + (size_t)j) * D;
+      __nv_bfloat16* dkrow = p.dk + (kvh * p.S_k + (size_t)j) * D + half * (D / 2);
+      __nv_bfloat16* dvrow = p.dv + (kvh * p.S_k + (size_t)j) * D + half * (D / 2);
       if (it.n == 0) {
         if (valid) {
           const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) {
+          for (int c = 0; c < D / 16; ++c) {
             reinterpret_cast<uint4*>(dkrow)[c] = z;
             reinterpret_cast<uint4*>(dvrow)[c] = z;
           }
@@ -935,7 +960,7 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
         const ScoreMod md = make_mod<ALIBI, SOFTCAP>(p, h);
         for (int u = 0; u < it.n && ok; ++u) {
           const uint32_t cls = entry_cls(it.lst[u], 0);
-          const int i0 = (int)entry_tile(it.lst[u]) * kTileM;
+          const int i0 = (int)entry_tile(it.lst[u]) * kTileM + cb;  // first query of this half
           const int st = (int)(q_cnt & 1);
           {
             const bool got = bwait(bar(SF), q_cnt & 1, ctl, kBSiteElem);
@@ -945,32 +970,31 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
           ptx::tc_fence_after();
           const float* s_lse2 = reinterpret_cast<const float*>(smem + C::kKvStage0 +
                                                                st * C::kKvStageBytes +
-                                                               2 * C::kTileBytes);
+                                                               2 * C::kTileBytes) + cb;
           const float* s_delta = s_lse2 + kTileM;
-          // S^T of the whole tile (this key against 128 queries) into registers
-          float tv[kTileM];
+          // this half of S^T (this key against 64 queries) into registers
+          float tv[kBCols];
           const float jb = (float)(j - (i0 + p.q_offset));  // bias position of column 0
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
+          {
             uint32_t ra[32], rb[32];
-            ptx::tmem_ld32(tST + (uint32_t)(64 * hh), ra);
-            ptx::tmem_ld32(tST + (uint32_t)(64 * hh + 32), rb);
+            ptx::tmem_ld32(tST, ra);
+            ptx::tmem_ld32(tST + 32u, rb);
             ptx::tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-              tv[64 * hh + c] = __uint_as_float(ra[c]);
-              tv[64 * hh + 32 + c] = __uint_as_float(rb[c]);
+              tv[c] = __uint_as_float(ra[c]);
+              tv[32 + c] = __uint_as_float(rb[c]);
             }
           }
-          add_rel_bias<ALIBI, SOFTCAP>(tv, p, h, j - (i0 + p.q_offset), -1, md);
+          add_rel_bias<ALIBI, SOFTCAP, kBCols>(tv, p, h, j - (i0 + p.q_offset), -1, md);
 #pragma unroll
-          for (int c = 0; c < kTileM; ++c) tv[c] = score_t<ALIBI, SOFTCAP>(tv[c], jb - (float)c, md);
+          for (int c = 0; c < kBCols; ++c) tv[c] = score_t<ALIBI, SOFTCAP>(tv[c], jb - (float)c, md);
           // the mask in a loop of its own (rows beyond S_k see nothing)
           if (!valid || cls == kPartial) {
             const int clo = ilo - i0, chi = ihi - i0;
             if (has_doc) {
 #pragma unroll
-              for (int c = 0; c < kTileM; ++c) {
+              for (int c = 0; c < kBCols; ++c) {
                 const int qi = i0 + c;
                 const bool vis = valid & (c >= clo) & (c <= chi) & (qi < p.S_q) &&
                                  doc_b[qi < p.S_q ? qi : 0] == doc_j;
@@ -978,21 +1002,20 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
               }
             } else {
 #pragma unroll
-              for (int c = 0; c < kTileM; ++c)
+              for (int c = 0; c < kBCols; ++c)
                 tv[c] = (valid & (c >= clo) & (c <= chi)) ? tv[c] : -INFINITY;
             }
           }
-          // P^T, packed over S^T's first 64 columns for dV; kept (times the
+          // P^T, packed over this half's S^T columns for dV; kept (times the
           // soft cap's derivative) in place for dS^T
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
+          {
             uint32_t pp[32];
 #pragma unroll
             for (int c2 = 0; c2 < 32; ++c2) {
               float pr[2];
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
-                const int c = 64 * hh + 2 * c2 + e;
+                const int c = 2 * c2 + e;
                 pr[e] = ptx::ex2_approx(tv[c] - s_lse2[c]);
                 float dm = 1.0f;
                 if constexpr (SOFTCAP) {
@@ -1003,7 +1026,7 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
               }
               pp[c2] = ptx::pack_bf16x2(pr[0], pr[1]);
             }
-            ptx::tmem_st32(tST + (uint32_t)(32 * hh), pp);
+            ptx::tmem_st32(tPk, pp);
           }
           ptx::tmem_wait_st();
           ptx::tc_fence_before();
@@ -1015,20 +1038,23 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
             if (!ok) break;
           }
           ptx::tc_fence_after();
-          // dS^T = P^T (dP^T - Delta), 32 columns at a time, packed over dP^T's
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            uint32_t dp[32];
-            ptx::tmem_ld32(tDPT + (uint32_t)(32 * k4), dp);
+          // dS^T = P^T (dP^T - Delta): this half's 64 columns of dP^T, then
+          // 32 packed columns over them
+          {
+            uint32_t d0[32], d1[32], pk[32];
+            ptx::tmem_ld32(tDPT, d0);
+            ptx::tmem_ld32(tDPT + 32u, d1);
             ptx::tmem_wait_ld();
-            uint32_t pk[16];
 #pragma unroll
             for (int c2 = 0; c2 < 16; ++c2) {
-              const int c = 32 * k4 + 2 * c2;
-              pk[c2] = ptx::pack_bf16x2(tv[c] * (__uint_as_float(dp[2 * c2]) - s_delta[c]),
-                                        tv[c + 1] * (__uint_as_float(dp[2 * c2 + 1]) - s_delta[c + 1]));
+              const int c = 2 * c2;
+              pk[c2] = ptx::pack_bf16x2(tv[c] * (__uint_as_float(d0[c]) - s_delta[c]),
+                                        tv[c + 1] * (__uint_as_float(d0[c + 1]) - s_delta[c + 1]));
+              pk[16 + c2] =
+                  ptx::pack_bf16x2(tv[32 + c] * (__uint_as_float(d1[c]) - s_delta[32 + c]),
+                                   tv[33 + c] * (__uint_as_float(d1[c + 1]) - s_delta[33 + c]));
             }
-            ptx::tmem_st16(tDPT + (uint32_t)(16 * k4), pk);
+            ptx::tmem_st32(tDSk, pk);
           }
           ptx::tmem_wait_st();
           ptx::tc_fence_before();
@@ -1045,7 +1071,7 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
       }
       ptx::tc_fence_after();
 #pragma unroll
-      for (int c4 = 0; c4 < D / 32; ++c4) {
+      for (int c4 = 0; c4 < D / 64; ++c4) {
         uint32_t ov[32], ok32[32];
         ptx::tmem_ld32(tDV + (uint32_t)(c4 * 32), ov);
         ptx::tmem_ld32(tDK + (uint32_t)(c4 * 32), ok32);
