@@ -30,7 +30,10 @@
 // item that owns it, so results are deterministic.
 //
 // Warp roles (320 threads): warps 0-7 elementwise in two warpgroups, warp 8
-// TMA loads, warp 9 allocates Tensor Memory and issues the MMAs.  Warps w
+// TMA loads, warp 9 allocates Tensor Memory and issues the MMAs (168
+// registers a thread: moving registers from a third warpgroup to the
+// elementwise ones with setmaxnreg removed the last spills of the dK/dV
+// kernel but measured 3-4% slower).  Warps w
 // and w + 4 share Tensor Memory lane quarter w & 3 (32 rows of the tile) and
 // split its 128 columns: warpgroup 0 takes columns [0, 64), warpgroup 1
 // [64, 128).  No elementwise step reduces along a row (P = exp(S - LSE) with
@@ -56,6 +59,7 @@ namespace {
 constexpr int kBThreads = 320;
 constexpr int kBLoadWarp = 8;
 constexpr int kBMmaWarp = 9;
+
 constexpr int kBCols = 64;      // columns of a tile per elementwise half
 constexpr uint32_t kBPack = 32;  // packed operand: Tensor Memory columns [32, 96)
 constexpr uint32_t kBTmemCols = 512;
@@ -425,6 +429,7 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
     return m;
   };
 
+  if (warp >= 8) {
   if (warp == kBLoadWarp) {
     if (lane == 0) {
       ptx::prefetch_tmap(&p.tmap_q);
@@ -549,7 +554,8 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
       }
     }
     if (!__all_sync(0xffffffffu, drained) && lane == 0) breport(ctl, ATTN_ERR_TIMEOUT, kBSiteDrain, 0);
-  } else if (warp < 8) {
+  }
+  } else {
     // ===================== elementwise: one thread per query row =========
     // half 0: key columns [0, 64) of each tile, half 1: [64, 128); the dQ
     // epilogue splits the D columns the same way
@@ -781,6 +787,7 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
   };
   auto stage_addr = [&](int st) { return sbase + (uint32_t)(C::kKvStage0 + st * C::kKvStageBytes); };
 
+  if (warp >= 8) {
   if (warp == kBLoadWarp) {
     if (lane == 0) {
       ptx::prefetch_tmap(&p.tmap_q);
@@ -914,7 +921,8 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
       }
     }
     if (!__all_sync(0xffffffffu, drained) && lane == 0) breport(ctl, ATTN_ERR_TIMEOUT, kBSiteDrain, 0);
-  } else if (warp < 8) {
+  }
+  } else {
     // ===================== elementwise: one thread per key ================
     // half 0: query columns [0, 64) of each tile, half 1: [64, 128); the
     // dK / dV epilogue splits the D columns the same way
@@ -1008,15 +1016,20 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
           }
           // P^T, packed over this half's S^T columns for dV; kept (times the
           // soft cap's derivative) in place for dS^T
+          // (LSE and Delta of the 64 queries: 16-byte shared-memory loads,
+          // the same address for every lane)
           {
             uint32_t pp[32];
+            const float4* l4 = reinterpret_cast<const float4*>(s_lse2);
 #pragma unroll
-            for (int c2 = 0; c2 < 32; ++c2) {
-              float pr[2];
+            for (int c4 = 0; c4 < kBCols / 4; ++c4) {
+              const float4 lv = l4[c4];
+              const float lq[4] = {lv.x, lv.y, lv.z, lv.w};
+              float pr[4];
 #pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int c = 2 * c2 + e;
-                pr[e] = ptx::ex2_approx(tv[c] - s_lse2[c]);
+              for (int e = 0; e < 4; ++e) {
+                const int c = 4 * c4 + e;
+                pr[e] = ptx::ex2_approx(tv[c] - lq[e]);
                 float dm = 1.0f;
                 if constexpr (SOFTCAP) {
                   const float uu = fmaxf(tv[c], -md.capl2) / md.capl2;
@@ -1024,7 +1037,8 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
                 }
                 tv[c] = pr[e] * dm;
               }
-              pp[c2] = ptx::pack_bf16x2(pr[0], pr[1]);
+              pp[2 * c4] = ptx::pack_bf16x2(pr[0], pr[1]);
+              pp[2 * c4 + 1] = ptx::pack_bf16x2(pr[2], pr[3]);
             }
             ptx::tmem_st32(tPk, pp);
           }
@@ -1045,14 +1059,21 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
             ptx::tmem_ld32(tDPT, d0);
             ptx::tmem_ld32(tDPT + 32u, d1);
             ptx::tmem_wait_ld();
+            const float4* dl4 = reinterpret_cast<const float4*>(s_delta);
 #pragma unroll
-            for (int c2 = 0; c2 < 16; ++c2) {
-              const int c = 2 * c2;
-              pk[c2] = ptx::pack_bf16x2(tv[c] * (__uint_as_float(d0[c]) - s_delta[c]),
-                                        tv[c + 1] * (__uint_as_float(d0[c + 1]) - s_delta[c + 1]));
-              pk[16 + c2] =
-                  ptx::pack_bf16x2(tv[32 + c] * (__uint_as_float(d1[c]) - s_delta[32 + c]),
-                                   tv[33 + c] * (__uint_as_float(d1[c + 1]) - s_delta[33 + c]));
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const float4 a = dl4[c4], b = dl4[8 + c4];
+              const int c = 4 * c4;
+              pk[2 * c4] = ptx::pack_bf16x2(tv[c] * (__uint_as_float(d0[c]) - a.x),
+                                            tv[c + 1] * (__uint_as_float(d0[c + 1]) - a.y));
+              pk[2 * c4 + 1] = ptx::pack_bf16x2(tv[c + 2] * (__uint_as_float(d0[c + 2]) - a.z),
+                                                tv[c + 3] * (__uint_as_float(d0[c + 3]) - a.w));
+              pk[16 + 2 * c4] =
+                  ptx::pack_bf16x2(tv[32 + c] * (__uint_as_float(d1[c]) - b.x),
+                                   tv[33 + c] * (__uint_as_float(d1[c + 1]) - b.y));
+              pk[17 + 2 * c4] =
+                  ptx::pack_bf16x2(tv[34 + c] * (__uint_as_float(d1[c + 2]) - b.z),
+                                   tv[35 + c] * (__uint_as_float(d1[c + 3]) - b.w));
             }
             ptx::tmem_st32(tDSk, pk);
           }
