@@ -322,7 +322,11 @@ __device__ __forceinline__ void key_rows(const BParams& p, int b, int j, bool do
 
 // ---------------------------------------------------------------- prep ----
 // lse2[r] = LSE * log2(e) (+inf where the row has no visible key or r is
-// padding); delta[r] = dO_r . O_r (0 for padding).  One warp per row.
+// padding); delta[r] = dO_r . O_r (0 for padding).  Four threads per row,
+// each with D/4 elements of O and of dO in flight as 16-byte loads (the
+// kernel only streams O and dO once, so it is bound by HBM).
+constexpr int kPrepTpr = 4;                     // threads per row
+constexpr int kPrepRows = 256 / kPrepTpr;       // rows per 256-thread block
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* out,
                                                        const __nv_bfloat16* dout,
@@ -330,25 +334,41 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* out,
                                                        float* delta, int BH, int S_q, int nQ) {
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
-  const long long rows = (long long)BH * nQ * kTileM;
-  const long long r = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (r >= rows) return;
-  const long long bh = r / ((long long)nQ * kTileM);
-  const int i = (int)(r % ((long long)nQ * kTileM));
+  constexpr int kVec = D / (8 * kPrepTpr);  // 16-byte vectors per thread and tensor
+  const long long per = (long long)nQ * kTileM;
+  const long long rows = (long long)BH * per;
+  const long long r = (long long)blockIdx.x * kPrepRows + (threadIdx.x / kPrepTpr);
+  const int q = threadIdx.x % kPrepTpr;
+  const bool in = r < rows;
+  const long long bh = in ? r / per : 0;
+  const int i = in ? (int)(r % per) : S_q;
   float acc = 0.f;
   if (i < S_q) {
-    const size_t base = ((size_t)bh * S_q + (size_t)i) * D;
-    for (int d = lane * 2; d < D; d += 64) {
-      const __nv_bfloat162 o2 = *reinterpret_cast<const __nv_bfloat162*>(out + base + d);
-      const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(dout + base + d);
-      acc = fmaf(__bfloat162float(o2.x), __bfloat162float(g2.x), acc);
-      acc = fmaf(__bfloat162float(o2.y), __bfloat162float(g2.y), acc);
+    const size_t base = ((size_t)bh * S_q + (size_t)i) * D + (size_t)q * (D / kPrepTpr);
+    const uint4* o4 = reinterpret_cast<const uint4*>(out + base);
+    const uint4* g4 = reinterpret_cast<const uint4*>(dout + base);
+    uint4 ov[kVec], gv[kVec];
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) {
+      ov[v] = __ldg(o4 + v);
+      gv[v] = __ldg(g4 + v);
+    }
+#pragma unroll
+    for (int v = 0; v < kVec; ++v) {
+      const __nv_bfloat162* a = reinterpret_cast<const __nv_bfloat162*>(&ov[v]);
+      const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&gv[v]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 fa = __bfloat1622float2(a[e]), fb = __bfloat1622float2(b[e]);
+        acc = fmaf(fa.x, fb.x, acc);
+        acc = fmaf(fa.y, fb.y, acc);
+      }
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) {
+  // the row's four partial sums (lanes 4k .. 4k+3 of the warp)
+  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+  if (in && q == 0) {
     float l2 = INFINITY;
     if (i < S_q) {
       const float l = lse[(size_t)bh * S_q + (size_t)i];
@@ -1261,7 +1281,7 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
   // row statistics, then the two gradient kernels
   const int BH = a.B * a.H;
   const long long rows = (long long)padded;
-  const unsigned blocks = (unsigned)((rows + 7) / 8);
+  const unsigned blocks = (unsigned)((rows + kPrepRows - 1) / kPrepRows);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(blocks, 1, 1);
   cfg.blockDim = dim3(256, 1, 1);
