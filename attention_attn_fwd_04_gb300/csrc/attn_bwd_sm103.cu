@@ -78,18 +78,23 @@ struct BCfg {
   static constexpr int kHalfBytes = kTileM * 64 * 2;  // 128 rows x 64 bf16, 128-byte swizzle
   static constexpr int kHalves = D / 64;
   static constexpr int kTileBytes = kHalves * kHalfBytes;
-  // bwd_dq_kernel: Q, dO, then two stages of (K, V)
+  // bwd_dq_kernel: Q, dO, a ring of K tiles, a ring of V tiles (K is read
+  // by S and dQ, V only by dP, so V tiles are released earlier and need
+  // fewer stages)
   static constexpr int kDqQ = 0;
   static constexpr int kDqDo = kTileBytes;
-  static constexpr int kDqKV = 2 * kTileBytes;
-  static constexpr int kDqBar = kDqKV + 2 * 2 * kTileBytes;
+  static constexpr int kDqKStages = 3;
+  static constexpr int kDqVStages = 2;
+  static constexpr int kDqK = 2 * kTileBytes;
+  static constexpr int kDqV = kDqK + kDqKStages * kTileBytes;
+  static constexpr int kDqBar = kDqV + kDqVStages * kTileBytes;
   // bwd_dkdv_kernel: K, V, then two stages of (Q, dO, LSE2[128], Delta[128])
   static constexpr int kKvK = 0;
   static constexpr int kKvV = kTileBytes;
   static constexpr int kKvStage0 = 2 * kTileBytes;
   static constexpr int kKvStageBytes = 2 * kTileBytes + 1024;
   static constexpr int kKvBar = kKvStage0 + 2 * kKvStageBytes;
-  static constexpr int kNumBars = 16;
+  static constexpr int kNumBars = 24;
   static constexpr int kSmemDq = kDqBar + 8 * kNumBars + 16;
   static constexpr int kSmemKv = kKvBar + 8 * kNumBars + 16;
   static constexpr int kSmemAllocDq = kSmemDq + 1024;
@@ -392,16 +397,23 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
   const int docs_sorted = p.hdr->docs_sorted;
 
   auto bar = [&](int i) { return sbase + (uint32_t)(C::kDqBar + 8 * i); };
-  enum { QF = 0, QE = 1, KVF = 2, KVE = 4, SF = 6, DSF = 7, DQF = 8, DQE = 9, DRAIN = 10,
-         DPF = 11, SCON = 12 };
+  constexpr int KS = C::kDqKStages, VS = C::kDqVStages;
+  // KF/KE: K ring (KS each), VF/VE: V ring (VS each), DPF: one per dP buffer
+  enum { QF = 0, QE = 1, SF = 2, DSF = 3, DQF = 4, DQE = 5, DRAIN = 6, SCON = 7, DPF = 8,
+         KF = 10, KE = KF + KS, VF = KE + KS, VE = VF + VS };
+  static_assert(VE + VS <= C::kNumBars, "barrier slots");
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kDqBar + 8 * C::kNumBars);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kDqBar + 8 * C::kNumBars + 4);
   if (threadIdx.x == 0) {
     ptx::mbar_init(bar(QF), 1);
     ptx::mbar_init(bar(QE), 1);
-    for (int s = 0; s < 2; ++s) {
-      ptx::mbar_init(bar(KVF + s), 1);
-      ptx::mbar_init(bar(KVE + s), 1);
+    for (int s = 0; s < KS; ++s) {
+      ptx::mbar_init(bar(KF + s), 1);
+      ptx::mbar_init(bar(KE + s), 1);
+    }
+    for (int s = 0; s < VS; ++s) {
+      ptx::mbar_init(bar(VF + s), 1);
+      ptx::mbar_init(bar(VE + s), 1);
     }
     // one arrival per elementwise warp
     ptx::mbar_init(bar(SF), 1);
@@ -409,6 +421,7 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
     ptx::mbar_init(bar(DQF), 1);
     ptx::mbar_init(bar(DQE), 8);
     ptx::mbar_init(bar(DPF), 1);
+    ptx::mbar_init(bar(DPF + 1), 1);
     ptx::mbar_init(bar(SCON), 8);
     ptx::mbar_init(bar(DRAIN), 1);
     *s_abort = 0;
@@ -457,7 +470,7 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
       ptx::prefetch_tmap(&p.tmap_k);
       ptx::prefetch_tmap(&p.tmap_v);
       const uint64_t pol = ptx::policy_evict_last();
-      uint32_t kv_cnt = 0, q_issued = 0;
+      uint32_t kv_cnt = 0, q_issued = 0, v_issued = 0;
       int act = 0;
       bool ok = true;
       for (int r = 0; ok; ++r) {
@@ -478,29 +491,45 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
         const int kvz = it.b * p.H_kv + it.h / p.group;
         for (int j = 0; j < it.n && ok; ++j) {
           if (entry_cls(it.lst[j], it.t) == kEmpty) continue;
-          const int st = (int)(kv_cnt & 1);
-          if (kv_cnt >= 2) ok = bwait(bar(KVE + st), ((kv_cnt >> 1) - 1) & 1, ctl, kBSiteLoad);
-          if (!ok) break;
           const int row0 = (int)entry_tile(it.lst[j]) * kTileN;
-          const uint32_t kdst = sbase + C::kDqKV + st * 2 * C::kTileBytes;
-          ptx::mbar_arrive_expect_tx(bar(KVF + st), 2 * C::kTileBytes);
-          for (int hx = 0; hx < C::kHalves; ++hx) {
-            ptx::tma_load_3d(kdst + hx * C::kHalfBytes, &p.tmap_k, bar(KVF + st), hx * 64, row0,
+          // tile g = kv_cnt: K into slot g % KS, V into slot g % VS
+          const int ks = (int)(kv_cnt % KS), vs = (int)(kv_cnt % VS);
+          if (kv_cnt >= (uint32_t)KS)
+            ok = bwait(bar(KE + ks), ((kv_cnt / KS) - 1) & 1, ctl, kBSiteLoad);
+          if (!ok) break;
+          const uint32_t kdst = sbase + C::kDqK + ks * C::kTileBytes;
+          ptx::mbar_arrive_expect_tx(bar(KF + ks), C::kTileBytes);
+          for (int hx = 0; hx < C::kHalves; ++hx)
+            ptx::tma_load_3d(kdst + hx * C::kHalfBytes, &p.tmap_k, bar(KF + ks), hx * 64, row0,
                              kvz, pol);
-            ptx::tma_load_3d(kdst + C::kTileBytes + hx * C::kHalfBytes, &p.tmap_v, bar(KVF + st),
-                             hx * 64, row0, kvz, pol);
+          if (kv_cnt >= (uint32_t)VS)
+            ok = bwait(bar(VE + vs), ((kv_cnt / VS) - 1) & 1, ctl, kBSiteLoad);
+          if (!ok) {
+            ++kv_cnt;  // K of this tile is in flight (drained below)
+            break;
           }
+          const uint32_t vdst = sbase + C::kDqV + vs * C::kTileBytes;
+          ptx::mbar_arrive_expect_tx(bar(VF + vs), C::kTileBytes);
+          for (int hx = 0; hx < C::kHalves; ++hx)
+            ptx::tma_load_3d(vdst + hx * C::kHalfBytes, &p.tmap_v, bar(VF + vs), hx * 64, row0,
+                             kvz, pol);
           ++kv_cnt;
+          ++v_issued;
         }
         ++act;
       }
       if (!ok) {
         drain_loads(bar(QF), 1, q_issued, p.budget_ns);
-        drain_loads(bar(KVF), 2, kv_cnt, p.budget_ns);
+        drain_loads(bar(KF), KS, kv_cnt, p.budget_ns);
+        drain_loads(bar(VF), VS, v_issued, p.budget_ns);
       }
     }
   } else if (warp == kBMmaWarp) {
-    const uint32_t tS = tmem, tP = tmem + 128u, tQ = tmem + 256u;
+    // Tensor Memory: S [0, 128), dP in two buffers [128, 256) and
+    // [256, 384) (tile g of the CTA's sequence uses buffer g & 1), dQ
+    // [384, 384 + D)
+    const uint32_t tS = tmem, tQ = tmem + 384u;
+    auto tPb = [&](uint32_t g) { return tmem + 128u + 128u * (g & 1u); };
     const uint64_t q_desc = BDesc<D>::kKMajor + ((sbase + C::kDqQ) >> 4);
     const uint64_t do_desc = BDesc<D>::kKMajor + ((sbase + C::kDqDo) >> 4);
     auto waitw = [&](uint32_t b, uint32_t par) {
@@ -515,25 +544,44 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
       const It it = item(w);
       if (nonempty(it) == 0) continue;
       ok = waitw(bar(QF), act & 1);
-      if (ok && act > 0) ok = waitw(bar(DQE), (act - 1) & 1);
       if (!ok) break;
-      // Software pipeline over the item's key tiles u: S(u+1) is issued as
-      // soon as the elementwise warps have read S(u), so their next tile is
-      // ready while dQ(u) and dP(u+1) run.  dS(u) is written over dP(u)'s
-      // columns, which dP(u+1) overwrites only after dQ(u) read them.
+      // Software pipeline over the item's key tiles u (tile g = kv0 + u of
+      // the CTA's sequence): S(u+1) and dP(u+1) are issued as soon as the
+      // elementwise warps have read S(u), dP(u+1) into the other buffer, so
+      // both are ready when the elementwise warps finish tile u; dQ(u)
+      // follows once dS(u) is written over dP(u)'s buffer (which dP(u+2)
+      // overwrites only after dQ(u), in issue order).  V(u) is released
+      // after dP(u), K(u) after dQ(u); the K ring is one stage deeper, since
+      // S(u+2) follows dQ(u) directly.  Q and dO are released after the
+      // item's last S and dP, so the next item's Q loads under this item's
+      // last dQ products, and the previous item's dQ must be read out only
+      // before this item's first dQ.
       const int m = nonempty(it);
       const uint32_t kv0 = kv_cnt;
-      auto kaddr = [&](int u) { return sbase + C::kDqKV + ((kv0 + u) & 1) * 2 * C::kTileBytes; };
+      auto kaddr = [&](int u) {
+        return sbase + C::kDqK + (uint32_t)(((kv0 + (uint32_t)u) % KS) * C::kTileBytes);
+      };
+      auto vaddr = [&](int u) {
+        return sbase + C::kDqV + (uint32_t)(((kv0 + (uint32_t)u) % VS) * C::kTileBytes);
+      };
       auto kv_ready = [&](int u) {
-        return waitw(bar(KVF + ((kv0 + u) & 1)), ((kv0 + u) >> 1) & 1);
+        const uint32_t g = kv0 + (uint32_t)u;
+        return waitw(bar(KF + (int)(g % KS)), (g / KS) & 1) &&
+               waitw(bar(VF + (int)(g % VS)), (g / VS) & 1);
+      };
+      auto issue_s_dp = [&](int u) {
+        const uint32_t g = kv0 + (uint32_t)u;
+        mma_nt<D>(tS, q_desc, BDesc<D>::kKMajor + (kaddr(u) >> 4));  // S = Q K^T
+        ptx::mma_commit_elect(bar(SF));
+        mma_nt<D>(tPb(g), do_desc, BDesc<D>::kKMajor + (vaddr(u) >> 4));  // dP = dO V^T
+        ptx::mma_commit_elect(bar(DPF + (int)(g & 1u)));
+        ptx::mma_commit_elect(bar(VE + (int)(g % VS)));
+        if (u + 1 == m) ptx::mma_commit_elect(bar(QE));
       };
       ok = kv_ready(0);
       if (!ok) break;
       ptx::tc_fence_after();
-      mma_nt<D>(tS, q_desc, BDesc<D>::kKMajor + (kaddr(0) >> 4));  // S = Q K^T
-      ptx::mma_commit_elect(bar(SF));
-      mma_nt<D>(tP, do_desc, BDesc<D>::kKMajor + ((kaddr(0) + C::kTileBytes) >> 4));  // dP
-      ptx::mma_commit_elect(bar(DPF));
+      issue_s_dp(0);
       for (int u = 0; u < m && ok; ++u) {
         ok = waitw(bar(SCON), scon_cnt & 1);
         if (!ok) break;
@@ -542,24 +590,20 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
           ok = kv_ready(u + 1);
           if (!ok) break;
           ptx::tc_fence_after();
-          mma_nt<D>(tS, q_desc, BDesc<D>::kKMajor + (kaddr(u + 1) >> 4));
-          ptx::mma_commit_elect(bar(SF));
+          issue_s_dp(u + 1);
         }
         ok = waitw(bar(DSF), ds_cnt & 1);
+        if (ok && u == 0 && act > 0) ok = waitw(bar(DQE), (act - 1) & 1);
         if (!ok) break;
         ++ds_cnt;
         ptx::tc_fence_after();
-        mma_tn<D>(tQ, tP + kBPack, BDesc<D>::kMNMajor + (kaddr(u) >> 4), u > 0);  // dQ += dS K
-        ptx::mma_commit_elect(bar(KVE + ((kv0 + u) & 1)));
-        if (u + 1 < m) {
-          mma_nt<D>(tP, do_desc, BDesc<D>::kKMajor + ((kaddr(u + 1) + C::kTileBytes) >> 4));
-          ptx::mma_commit_elect(bar(DPF));
-        }
+        const uint32_t g = kv0 + (uint32_t)u;
+        mma_tn<D>(tQ, tPb(g) + kBPack, BDesc<D>::kMNMajor + (kaddr(u) >> 4), u > 0);  // dQ += dS K
+        ptx::mma_commit_elect(bar(KE + (int)(g % KS)));
       }
       kv_cnt = kv0 + (uint32_t)m;
       if (!ok) break;
       ptx::mma_commit_elect(bar(DQF));
-      ptx::mma_commit_elect(bar(QE));
       ++act;
     }
     // every MMA done before Tensor Memory is freed
@@ -583,9 +627,7 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
     const int row = wq * 32 + lane;
     const int cb = kBCols * half;
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
-    const uint32_t tS = lane_base + (uint32_t)cb, tP = lane_base + 128u + (uint32_t)cb,
-                   tPk = lane_base + 128u + kBPack + 32u * (uint32_t)half,
-                   tQ = lane_base + 256u + (uint32_t)(half * D / 2);
+    const uint32_t tS = lane_base + (uint32_t)cb, tQ = lane_base + 384u + (uint32_t)(half * D / 2);
     uint32_t s_cnt = 0;
     int act = 0;
     bool ok = true;
@@ -619,6 +661,10 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
         const uint32_t cls = entry_cls(it.lst[j], it.t);
         if (cls == kEmpty) continue;
         const int j0 = (int)entry_tile(it.lst[j]) * kTileN + cb;  // first key of this half
+        const uint32_t g = s_cnt;  // this tile's place in the CTA's sequence
+        // its dP buffer: this half's columns, and where dS is packed
+        const uint32_t tP = lane_base + 128u + 128u * (g & 1u) + (uint32_t)cb,
+                       tPk = lane_base + 128u + 128u * (g & 1u) + kBPack + 32u * (uint32_t)half;
         {
           const bool got = bwait(bar(SF), s_cnt & 1, ctl, kBSiteElem);
           ok = __all_sync(0xffffffffu, got);
@@ -675,7 +721,7 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
           tv[c] = pr;
         }
         {
-          const bool got = bwait(bar(DPF), (s_cnt & 1) ^ 1, ctl, kBSiteElem);
+          const bool got = bwait(bar(DPF + (int)(g & 1u)), (g >> 1) & 1u, ctl, kBSiteElem);
           ok = __all_sync(0xffffffffu, got);
           if (!ok) break;
         }
