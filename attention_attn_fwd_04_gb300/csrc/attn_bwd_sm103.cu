@@ -1042,10 +1042,10 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
             if (!ok) break;
           }
           ptx::tc_fence_after();
-          const float* s_lse2 = reinterpret_cast<const float*>(smem + C::kKvStage0 +
-                                                               st * C::kKvStageBytes +
-                                                               2 * C::kTileBytes) + cb;
-          const float* s_delta = s_lse2 + kTileM;
+          // LSE (log2 units) and Delta of this half's 64 queries in shared memory
+          const uint32_t s_lse2 = sbase + (uint32_t)(C::kKvStage0 + st * C::kKvStageBytes +
+                                                     2 * C::kTileBytes + 4 * cb);
+          const uint32_t s_delta = s_lse2 + 4u * kTileM;
           // this half of S^T (this key against 64 queries) into registers
           float tv[kBCols];
           const float jb = (float)(j - (i0 + p.q_offset));  // bias position of column 0
@@ -1082,14 +1082,13 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
           }
           // P^T, packed over this half's S^T columns for dV; kept (times the
           // soft cap's derivative) in place for dS^T
-          // (LSE and Delta of the 64 queries: 16-byte shared-memory loads,
-          // the same address for every lane)
+          // (LSE of the 64 queries: 16-byte shared-memory loads, the same
+          // address for every lane)
           {
             uint32_t pp[32];
-            const float4* l4 = reinterpret_cast<const float4*>(s_lse2);
 #pragma unroll
             for (int c4 = 0; c4 < kBCols / 4; ++c4) {
-              const float4 lv = l4[c4];
+              const float4 lv = ptx::lds_v4(s_lse2 + 16u * (uint32_t)c4);
               const float lq[4] = {lv.x, lv.y, lv.z, lv.w};
               float pr[4];
 #pragma unroll
@@ -1125,10 +1124,10 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
             ptx::tmem_ld32(tDPT, d0);
             ptx::tmem_ld32(tDPT + 32u, d1);
             ptx::tmem_wait_ld();
-            const float4* dl4 = reinterpret_cast<const float4*>(s_delta);
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4) {
-              const float4 a = dl4[c4], b = dl4[8 + c4];
+              const float4 a = ptx::lds_v4(s_delta + 16u * (uint32_t)c4),
+                           b = ptx::lds_v4(s_delta + 16u * (uint32_t)(8 + c4));
               const int c = 4 * c4;
               pk[2 * c4] = ptx::pack_bf16x2(tv[c] * (__uint_as_float(d0[c]) - a.x),
                                             tv[c + 1] * (__uint_as_float(d0[c + 1]) - a.y));

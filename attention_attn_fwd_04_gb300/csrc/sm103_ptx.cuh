@@ -82,6 +82,17 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity
   return done != 0;
 }
 
+// 16-byte load from shared memory by shared-window address (an explicit
+// ld.shared: through a generic pointer the compiler may emit a generic load,
+// which takes the slower global-memory path).
+__device__ __forceinline__ float4 lds_v4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+
 __device__ __forceinline__ int ld_volatile_shared(uint32_t addr) {
   int v;
   asm volatile("ld.volatile.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
