@@ -13,9 +13,11 @@
 // goes to HBM.)
 //
 // Three kernels:
-//   bwd_prep_kernel   per query row: LSE in log2 units and dO . O, padded to
-//                     whole 128-row tiles (padding rows get +inf / 0, so
-//                     they contribute P = 0 without a mask)
+//   bwd_prep_kernel   per query row: -LSE in log2 units and -(dO . O),
+//                     padded to whole 128-row tiles (padding rows get
+//                     -inf / 0, so they contribute P = 0 without a mask);
+//                     negated so that the elementwise steps are additions
+//                     (paired fp32 instructions)
 //   bwd_dq_kernel     one 128-row query tile per work item: for each key tile
 //                     of its block-mask list, S = Q K^T and dP = dO V^T into
 //                     Tensor Memory, dS by the elementwise warpgroup (one
@@ -109,8 +111,8 @@ struct BParams {
   __nv_bfloat16* dq;
   __nv_bfloat16* dk;
   __nv_bfloat16* dv;
-  const float* lse2;   // [B*H][nQ*128]
-  const float* delta;  // [B*H][nQ*128]
+  const float* nlse2;   // [B*H][nQ*128] -LSE * log2(e)
+  const float* ndelta;  // [B*H][nQ*128] -(dO . O)
   int B, H, H_kv, S_q, S_k, group, nQ, nK, nP, bm;
   float scale, scale_log2, softcap;
   uint32_t mask_flags;
@@ -326,8 +328,8 @@ __device__ __forceinline__ void key_rows(const BParams& p, int b, int j, bool do
 }
 
 // ---------------------------------------------------------------- prep ----
-// lse2[r] = LSE * log2(e) (+inf where the row has no visible key or r is
-// padding); delta[r] = dO_r . O_r (0 for padding).  Four threads per row,
+// nlse2[r] = -LSE * log2(e) (-inf where the row has no visible key or r is
+// padding); ndelta[r] = -(dO_r . O_r) (0 for padding).  Four threads per row,
 // each with D/4 elements of O and of dO in flight as 16-byte loads (the
 // kernel only streams O and dO once, so it is bound by HBM).
 constexpr int kPrepTpr = 4;                     // threads per row
@@ -335,8 +337,8 @@ constexpr int kPrepRows = 256 / kPrepTpr;       // rows per 256-thread block
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* out,
                                                        const __nv_bfloat16* dout,
-                                                       const float* lse, float* lse2,
-                                                       float* delta, int BH, int S_q, int nQ) {
+                                                       const float* lse, float* nlse2,
+                                                       float* ndelta, int BH, int S_q, int nQ) {
   ptx::griddep_wait();
   ptx::griddep_launch_dependents();
   constexpr int kVec = D / (8 * kPrepTpr);  // 16-byte vectors per thread and tensor
@@ -374,13 +376,13 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* out,
   acc += __shfl_xor_sync(0xffffffffu, acc, 1);
   acc += __shfl_xor_sync(0xffffffffu, acc, 2);
   if (in && q == 0) {
-    float l2 = INFINITY;
+    float nl2 = -INFINITY;
     if (i < S_q) {
       const float l = lse[(size_t)bh * S_q + (size_t)i];
-      if (l != -INFINITY) l2 = l * kBLog2e;
+      if (l != -INFINITY) nl2 = -(l * kBLog2e);
     }
-    lse2[r] = l2;
-    delta[r] = acc;
+    nlse2[r] = nl2;
+    ndelta[r] = -acc;
   }
 }
 
@@ -648,8 +650,8 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
         continue;
       }
       const size_t si = bh * (size_t)p.nQ * kTileM + (size_t)it.qt * kTileM + row;
-      const float lse2 = p.lse2[si];
-      const float dlt = p.delta[si];
+      const float nlse2 = p.nlse2[si];
+      const float ndlt = p.ndelta[si];
       int lo, hi;
       row_keys(p, it.b, i, docs_sorted != 0, lo, hi);
       const bool has_doc = (p.mask_flags & ATTN_MASK_DOCUMENT) != 0 && !docs_sorted;
@@ -691,10 +693,14 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
             tv[32 + c] = __uint_as_float(rb[c]);
           }
         }
+        // the plain score (a scale) is folded into the exponential below
+        constexpr bool kPlain = !ALIBI && !SOFTCAP;
         add_rel_bias<ALIBI, SOFTCAP, kBCols>(tv, p, it.h, j0 - qpos, 1, md);
+        if constexpr (!kPlain) {
 #pragma unroll
-        for (int c = 0; c < kBCols; ++c)
-          tv[c] = score_t<ALIBI, SOFTCAP>(tv[c], (float)(j0 + c - qpos), md);
+          for (int c = 0; c < kBCols; ++c)
+            tv[c] = score_t<ALIBI, SOFTCAP>(tv[c], (float)(j0 + c - qpos), md);
+        }
         if (cls == kPartial) {
           const int clo = lo - j0, chi = hi - j0;
           if (has_doc) {
@@ -710,15 +716,26 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
             for (int c = 0; c < kBCols; ++c) tv[c] = ((c >= clo) & (c <= chi)) ? tv[c] : -INFINITY;
           }
         }
-        // P (times the soft cap's derivative), in place, while dP computes
+        // P (times the soft cap's derivative), in place, while dP computes;
+        // two columns per paired fp32 instruction (a masked -inf stays -inf:
+        // the scale is positive)
+        {
+          const uint64_t sc2 = ptx::f2(kPlain ? md.sc : 1.0f, kPlain ? md.sc : 1.0f),
+                         nl2 = ptx::f2(nlse2, nlse2);
 #pragma unroll
-        for (int c = 0; c < kBCols; ++c) {
-          float pr = ptx::ex2_approx(tv[c] - lse2);
-          if constexpr (SOFTCAP) {  // masked: t = -inf, clamped so the factor is 0
-            const float uu = fmaxf(tv[c], -md.capl2) / md.capl2;
-            pr *= 1.0f - uu * uu;
+          for (int c = 0; c < kBCols; c += 2) {
+            float xa, xb;
+            ptx::f2_split(ptx::ffma2(ptx::f2(tv[c], tv[c + 1]), sc2, nl2), xa, xb);
+            float pa = ptx::ex2_approx(xa), pb = ptx::ex2_approx(xb);
+            if constexpr (SOFTCAP) {  // masked: t = -inf, clamped so the factor is 0
+              const float ua = fmaxf(tv[c], -md.capl2) / md.capl2;
+              const float ub = fmaxf(tv[c + 1], -md.capl2) / md.capl2;
+              pa *= 1.0f - ua * ua;
+              pb *= 1.0f - ub * ub;
+            }
+            tv[c] = pa;
+            tv[c + 1] = pb;
           }
-          tv[c] = pr;
         }
         {
           const bool got = bwait(bar(DPF + (int)(g & 1u)), (g >> 1) & 1u, ctl, kBSiteElem);
@@ -727,19 +744,25 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
         }
         ptx::tc_fence_after();
         // dS = P (dP - Delta): this half's 64 columns of dP, then 32 packed
-        // columns over them
+        // columns over them (paired fp32: dP + (-Delta), then times P)
         {
           uint32_t d0[32], d1[32], pk[32];
           ptx::tmem_ld32(tP, d0);
           ptx::tmem_ld32(tP + 32u, d1);
           ptx::tmem_wait_ld();
+          const uint64_t nd2 = ptx::f2(ndlt, ndlt);
+          auto ds2 = [&](uint32_t a, uint32_t b, int c) {
+            float x, y;
+            ptx::f2_split(ptx::fmul2(ptx::fadd2(ptx::f2(__uint_as_float(a), __uint_as_float(b)),
+                                                nd2),
+                                     ptx::f2(tv[c], tv[c + 1])),
+                          x, y);
+            return ptx::pack_bf16x2(x, y);
+          };
 #pragma unroll
           for (int c2 = 0; c2 < 16; ++c2) {
-            pk[c2] = ptx::pack_bf16x2(tv[2 * c2] * (__uint_as_float(d0[2 * c2]) - dlt),
-                                      tv[2 * c2 + 1] * (__uint_as_float(d0[2 * c2 + 1]) - dlt));
-            pk[16 + c2] =
-                ptx::pack_bf16x2(tv[32 + 2 * c2] * (__uint_as_float(d1[2 * c2]) - dlt),
-                                 tv[33 + 2 * c2] * (__uint_as_float(d1[2 * c2 + 1]) - dlt));
+            pk[c2] = ds2(d0[2 * c2], d0[2 * c2 + 1], 2 * c2);
+            pk[16 + c2] = ds2(d1[2 * c2], d1[2 * c2 + 1], 32 + 2 * c2);
           }
           ptx::tmem_st32(tPk, pk);
         }
@@ -897,8 +920,8 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
                                hx * 64, qt * kTileM, (int)bh, pol);
             }
             const size_t so = bh * (size_t)p.nQ * kTileM + (size_t)qt * kTileM;
-            ptx::bulk_load(dst + 2 * C::kTileBytes, p.lse2 + so, kTileM * 4, bar(QF + st));
-            ptx::bulk_load(dst + 2 * C::kTileBytes + kTileM * 4, p.delta + so, kTileM * 4,
+            ptx::bulk_load(dst + 2 * C::kTileBytes, p.nlse2 + so, kTileM * 4, bar(QF + st));
+            ptx::bulk_load(dst + 2 * C::kTileBytes + kTileM * 4, p.ndelta + so, kTileM * 4,
                            bar(QF + st));
             ++q_cnt;
           }
@@ -1042,10 +1065,11 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
             if (!ok) break;
           }
           ptx::tc_fence_after();
-          // LSE (log2 units) and Delta of this half's 64 queries in shared memory
-          const uint32_t s_lse2 = sbase + (uint32_t)(C::kKvStage0 + st * C::kKvStageBytes +
-                                                     2 * C::kTileBytes + 4 * cb);
-          const uint32_t s_delta = s_lse2 + 4u * kTileM;
+          // -LSE (log2 units) and -Delta of this half's 64 queries in shared
+          // memory
+          const uint32_t s_nlse2 = sbase + (uint32_t)(C::kKvStage0 + st * C::kKvStageBytes +
+                                                      2 * C::kTileBytes + 4 * cb);
+          const uint32_t s_ndelta = s_nlse2 + 4u * kTileM;
           // this half of S^T (this key against 64 queries) into registers
           float tv[kBCols];
           const float jb = (float)(j - (i0 + p.q_offset));  // bias position of column 0
@@ -1060,9 +1084,14 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
               tv[32 + c] = __uint_as_float(rb[c]);
             }
           }
+          // the plain score (a scale) is folded into the exponential below
+          constexpr bool kPlain = !ALIBI && !SOFTCAP;
           add_rel_bias<ALIBI, SOFTCAP, kBCols>(tv, p, h, j - (i0 + p.q_offset), -1, md);
+          if constexpr (!kPlain) {
 #pragma unroll
-          for (int c = 0; c < kBCols; ++c) tv[c] = score_t<ALIBI, SOFTCAP>(tv[c], jb - (float)c, md);
+            for (int c = 0; c < kBCols; ++c)
+              tv[c] = score_t<ALIBI, SOFTCAP>(tv[c], jb - (float)c, md);
+          }
           // the mask in a loop of its own (rows beyond S_k see nothing)
           if (!valid || cls == kPartial) {
             const int clo = ilo - i0, chi = ihi - i0;
@@ -1081,29 +1110,35 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
             }
           }
           // P^T, packed over this half's S^T columns for dV; kept (times the
-          // soft cap's derivative) in place for dS^T
-          // (LSE of the 64 queries: 16-byte shared-memory loads, the same
-          // address for every lane)
+          // soft cap's derivative) in place for dS^T.  -LSE of the 64 queries
+          // comes in 16-byte shared-memory loads (the same address for every
+          // lane); two columns per paired fp32 instruction (a masked -inf
+          // stays -inf: the scale is positive).
           {
             uint32_t pp[32];
+            const uint64_t sc2 = ptx::f2(kPlain ? md.sc : 1.0f, kPlain ? md.sc : 1.0f);
 #pragma unroll
             for (int c4 = 0; c4 < kBCols / 4; ++c4) {
-              const float4 lv = ptx::lds_v4(s_lse2 + 16u * (uint32_t)c4);
+              const float4 lv = ptx::lds_v4(s_nlse2 + 16u * (uint32_t)c4);
               const float lq[4] = {lv.x, lv.y, lv.z, lv.w};
-              float pr[4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
+              for (int e = 0; e < 4; e += 2) {
                 const int c = 4 * c4 + e;
-                pr[e] = ptx::ex2_approx(tv[c] - lq[e]);
-                float dm = 1.0f;
+                float xa, xb;
+                ptx::f2_split(ptx::ffma2(ptx::f2(tv[c], tv[c + 1]), sc2, ptx::f2(lq[e], lq[e + 1])),
+                              xa, xb);
+                const float pa = ptx::ex2_approx(xa), pb = ptx::ex2_approx(xb);
+                float da = 1.0f, db = 1.0f;
                 if constexpr (SOFTCAP) {
-                  const float uu = fmaxf(tv[c], -md.capl2) / md.capl2;
-                  dm = 1.0f - uu * uu;
+                  const float ua = fmaxf(tv[c], -md.capl2) / md.capl2;
+                  const float ub = fmaxf(tv[c + 1], -md.capl2) / md.capl2;
+                  da = 1.0f - ua * ua;
+                  db = 1.0f - ub * ub;
                 }
-                tv[c] = pr[e] * dm;
+                tv[c] = pa * da;
+                tv[c + 1] = pb * db;
+                pp[2 * c4 + e / 2] = ptx::pack_bf16x2(pa, pb);
               }
-              pp[2 * c4] = ptx::pack_bf16x2(pr[0], pr[1]);
-              pp[2 * c4 + 1] = ptx::pack_bf16x2(pr[2], pr[3]);
             }
             ptx::tmem_st32(tPk, pp);
           }
@@ -1124,21 +1159,25 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
             ptx::tmem_ld32(tDPT, d0);
             ptx::tmem_ld32(tDPT + 32u, d1);
             ptx::tmem_wait_ld();
+            // paired fp32: dP^T + (-Delta), then times P^T
+            auto ds2 = [&](uint32_t x0, uint32_t x1, float n0, float n1, int c) {
+              float x, y;
+              ptx::f2_split(
+                  ptx::fmul2(ptx::fadd2(ptx::f2(__uint_as_float(x0), __uint_as_float(x1)),
+                                        ptx::f2(n0, n1)),
+                             ptx::f2(tv[c], tv[c + 1])),
+                  x, y);
+              return ptx::pack_bf16x2(x, y);
+            };
 #pragma unroll
             for (int c4 = 0; c4 < 8; ++c4) {
-              const float4 a = ptx::lds_v4(s_delta + 16u * (uint32_t)c4),
-                           b = ptx::lds_v4(s_delta + 16u * (uint32_t)(8 + c4));
+              const float4 a = ptx::lds_v4(s_ndelta + 16u * (uint32_t)c4),
+                           b = ptx::lds_v4(s_ndelta + 16u * (uint32_t)(8 + c4));
               const int c = 4 * c4;
-              pk[2 * c4] = ptx::pack_bf16x2(tv[c] * (__uint_as_float(d0[c]) - a.x),
-                                            tv[c + 1] * (__uint_as_float(d0[c + 1]) - a.y));
-              pk[2 * c4 + 1] = ptx::pack_bf16x2(tv[c + 2] * (__uint_as_float(d0[c + 2]) - a.z),
-                                                tv[c + 3] * (__uint_as_float(d0[c + 3]) - a.w));
-              pk[16 + 2 * c4] =
-                  ptx::pack_bf16x2(tv[32 + c] * (__uint_as_float(d1[c]) - b.x),
-                                   tv[33 + c] * (__uint_as_float(d1[c + 1]) - b.y));
-              pk[17 + 2 * c4] =
-                  ptx::pack_bf16x2(tv[34 + c] * (__uint_as_float(d1[c + 2]) - b.z),
-                                   tv[35 + c] * (__uint_as_float(d1[c + 3]) - b.w));
+              pk[2 * c4] = ds2(d0[c], d0[c + 1], a.x, a.y, c);
+              pk[2 * c4 + 1] = ds2(d0[c + 2], d0[c + 3], a.z, a.w, c + 2);
+              pk[16 + 2 * c4] = ds2(d1[c], d1[c + 1], b.x, b.y, 32 + c);
+              pk[17 + 2 * c4] = ds2(d1[c + 2], d1[c + 3], b.z, b.w, 34 + c);
             }
             ptx::tmem_st32(tDSk, pk);
           }
@@ -1284,8 +1323,8 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
   bp.dk = reinterpret_cast<__nv_bfloat16*>(a.dk);
   bp.dv = reinterpret_cast<__nv_bfloat16*>(a.dv);
   const size_t padded = (size_t)a.B * a.H * (size_t)g.nQ * kTileM;
-  bp.lse2 = a.rowstat;
-  bp.delta = a.rowstat + padded;
+  bp.nlse2 = a.rowstat;
+  bp.ndelta = a.rowstat + padded;
   bp.B = a.B;
   bp.H = a.H;
   bp.H_kv = a.H_kv;

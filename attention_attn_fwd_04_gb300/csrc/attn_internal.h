@@ -213,7 +213,7 @@ struct BwdArgs {
   int rel_max;
   const void* block_mask;    // forward block mask, built for this call
   const void* block_mask_t;  // transposed block mask, built for this call
-  float* rowstat;            // scratch: [2][B*H][nQ*128] (LSE in log2 units, dO . O)
+  float* rowstat;            // scratch: [2][B*H][nQ*128] (-LSE in log2 units, -(dO . O))
   DeviceStatus* status;
   double wait_budget_ms;
   int force_partial;
