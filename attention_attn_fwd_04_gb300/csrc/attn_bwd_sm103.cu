@@ -223,7 +223,7 @@ __device__ __forceinline__ int bitem_of(int r) {
 
 // The score transform in log2 units, as in the forward kernel.
 struct ScoreMod {
-  float sc, slope2, capl2;
+  float sc, slope2, capl2, inv_capl2;
 };
 template <bool ALIBI, bool SOFTCAP>
 __device__ __forceinline__ float score_t(float s, float bias_pos, const ScoreMod& m) {
@@ -240,6 +240,7 @@ __device__ __forceinline__ ScoreMod make_mod(const BParams& p, int h) {
   ScoreMod m;
   m.sc = SOFTCAP ? p.scale * (2.0f * kBLog2e / p.softcap) : p.scale_log2;
   m.capl2 = p.softcap * kBLog2e;
+  m.inv_capl2 = SOFTCAP ? 1.0f / m.capl2 : 0.f;
   m.slope2 = 0.f;
   if constexpr (ALIBI) {
     if (p.alibi_on) {
@@ -728,8 +729,8 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
             ptx::f2_split(ptx::ffma2(ptx::f2(tv[c], tv[c + 1]), sc2, nl2), xa, xb);
             float pa = ptx::ex2_approx(xa), pb = ptx::ex2_approx(xb);
             if constexpr (SOFTCAP) {  // masked: t = -inf, clamped so the factor is 0
-              const float ua = fmaxf(tv[c], -md.capl2) / md.capl2;
-              const float ub = fmaxf(tv[c + 1], -md.capl2) / md.capl2;
+              const float ua = fmaxf(tv[c], -md.capl2) * md.inv_capl2;
+              const float ub = fmaxf(tv[c + 1], -md.capl2) * md.inv_capl2;
               pa *= 1.0f - ua * ua;
               pb *= 1.0f - ub * ub;
             }
@@ -1130,8 +1131,8 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
                 const float pa = ptx::ex2_approx(xa), pb = ptx::ex2_approx(xb);
                 float da = 1.0f, db = 1.0f;
                 if constexpr (SOFTCAP) {
-                  const float ua = fmaxf(tv[c], -md.capl2) / md.capl2;
-                  const float ub = fmaxf(tv[c + 1], -md.capl2) / md.capl2;
+                  const float ua = fmaxf(tv[c], -md.capl2) * md.inv_capl2;
+                  const float ub = fmaxf(tv[c + 1], -md.capl2) * md.inv_capl2;
                   da = 1.0f - ua * ua;
                   db = 1.0f - ub * ub;
                 }
