@@ -178,3 +178,34 @@ def test_pair_workload_parity(pair, name):
     msg, _, _ = tp.run_and_compare(pair, inp["q"], inp["k"], inp["v"], w.scale,
                                    rows=rows.numpy(), **kw)
     print(name, msg)
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_pair_host_entry_matches_device(pair, D):
+    # attn_fwd_host builds its per-chunk block masks under the option too
+    B, H, Hkv, S = 2, 4, 2, 900
+    q, k, v = tp.rand_inputs(B, H, Hkv, S, S, D, seed=25)
+    o_h, l_h = pair.attn_fwd_host(q, k, v, causal=True, alibi=True)
+    torch.cuda.synchronize(DEV)
+    assert pair.get_device_status(device=DEV) == 0
+    o_d, l_d = pair.attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=True, alibi=True)
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(l_h, l_d.cpu())
+
+
+def test_backward_does_not_depend_on_the_option(attn):
+    # attn_bwd builds its own two-tile masks whatever the option says
+    B, H, S, D = 1, 4, 700, 128
+    q, k, v = tp.rand_inputs(B, H, H, S, S, D, seed=26)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    o, lse = attn.attn_fwd(qd, kd, vd, causal=True)
+    g = torch.Generator(device=DEV).manual_seed(5)
+    do = torch.randn(o.shape, device=DEV, generator=g).to(torch.bfloat16)
+    ref = attn.attn_bwd(qd, kd, vd, o, lse, do, causal=True)
+    attn.set_option("cta_pair", 1)
+    try:
+        got = attn.attn_bwd(qd, kd, vd, o, lse, do, causal=True)
+        assert attn.get_device_status(device=DEV) == 0
+    finally:
+        attn.set_option("cta_pair", 0)
+    for a, b in zip(got, ref):
+        assert torch.equal(a, b)

@@ -120,3 +120,21 @@ def test_noalloc_rejects_what_it_cannot_serve(api):
     st = fn(P["q"], P["k"], P["v"], P["out"], None, 1, 1, 1, 256, 256, 128, 0.1,
             ctypes.byref(m), None)
     assert st == 1  # ATTN_ERR_INVALID_ARG
+
+
+def test_noalloc_under_cta_pair(api):
+    # With the CTA-pair option the fixed scratch holds a four-tile block mask;
+    # the results equal attn_fwd's under the same option bit for bit.
+    attn, fn = api
+    case = make_case(attn, 0)
+    q, k, v, B, H, Hkv, S, D, mods = case
+    attn.set_option("cta_pair", 1)
+    try:
+        ro, rl = attn.attn_fwd(q, k, v, scale=1.0 / math.sqrt(D), **mods)
+        o, l = torch.empty_like(q), torch.empty(q.shape[:3], device=DEV)
+        assert call_noalloc(attn, fn, case, o, l) == 0
+        torch.cuda.synchronize(DEV)
+        assert attn.get_device_status(device=DEV) == 0
+    finally:
+        attn.set_option("cta_pair", 0)
+    assert torch.equal(o, ro) and torch.equal(l, rl)
