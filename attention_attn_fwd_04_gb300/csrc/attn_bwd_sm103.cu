@@ -569,22 +569,26 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
       };
       auto kv_ready = [&](int u) {
         const uint32_t g = kv0 + (uint32_t)u;
-        return waitw(bar(KF + (int)(g % KS)), (g / KS) & 1) &&
-               waitw(bar(VF + (int)(g % VS)), (g / VS) & 1);
+        return waitw(bar(KF + (int)(g % KS)), (g / KS) & 1);
       };
-      auto issue_s_dp = [&](int u) {
+      auto issue_s_dp = [&](int u) -> bool {
         const uint32_t g = kv0 + (uint32_t)u;
         mma_nt<D>(tS, q_desc, BDesc<D>::kKMajor + (kaddr(u) >> 4));  // S = Q K^T
         ptx::mma_commit_elect(bar(SF));
+        // V is waited for only now: S does not need it
+        if (!waitw(bar(VF + (int)(g % VS)), (g / VS) & 1)) return false;
+        ptx::tc_fence_after();
         mma_nt<D>(tPb(g), do_desc, BDesc<D>::kKMajor + (vaddr(u) >> 4));  // dP = dO V^T
         ptx::mma_commit_elect(bar(DPF + (int)(g & 1u)));
         ptx::mma_commit_elect(bar(VE + (int)(g % VS)));
         if (u + 1 == m) ptx::mma_commit_elect(bar(QE));
+        return true;
       };
       ok = kv_ready(0);
       if (!ok) break;
       ptx::tc_fence_after();
-      issue_s_dp(0);
+      ok = issue_s_dp(0);
+      if (!ok) break;
       for (int u = 0; u < m && ok; ++u) {
         ok = waitw(bar(SCON), scon_cnt & 1);
         if (!ok) break;
@@ -593,7 +597,8 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
           ok = kv_ready(u + 1);
           if (!ok) break;
           ptx::tc_fence_after();
-          issue_s_dp(u + 1);
+          ok = issue_s_dp(u + 1);
+          if (!ok) break;
         }
         ok = waitw(bar(DSF), ds_cnt & 1);
         if (ok && u == 0 && act > 0) ok = waitw(bar(DQE), (act - 1) & 1);
