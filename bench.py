@@ -216,9 +216,22 @@ def mods_of(w, inp, dev):
     return kw
 
 
-def time_workload(attn, w, inp, dev, steps, warmup):
+def quantile(xs, f):
+    """The f-quantile of xs by linear interpolation between order statistics."""
+    ys = sorted(xs)
+    x = f * (len(ys) - 1)
+    i = int(x)
+    return ys[i] if i + 1 >= len(ys) else ys[i] + (x - i) * (ys[i + 1] - ys[i])
+
+
+def time_workload(attn, w, inp, dev, steps, warmup, flush_l2=False):
     """Device timing of `steps` whole steps (block mask + forward) on resident
-    inputs, plus the forward kernel's own average duration."""
+    inputs, with the forward kernel's and the block-mask rebuild's own
+    durations per step (CUDA events on the launching stream).
+
+    flush_l2 writes a 256 MB buffer (larger than the 129 MB L2) before each
+    step, outside the events, so every forward starts from cold L2; the
+    step total then counts only the events' spans."""
     q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
     kw = mods_of(w, inp, dev)
     mask_kw = {n: kw[n] for n in ("causal", "window", "doc_ids", "prefix_len", "q_offset") if n in kw}
@@ -227,34 +240,45 @@ def time_workload(attn, w, inp, dev, steps, warmup):
     lse = torch.empty((w.B, w.H, w.S_q), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     bm = attn.build_block_mask(w.B, w.H, w.S_q, w.S_k, device=dev, **mask_kw)
+    scrub = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if flush_l2 else None
 
-    def step(ev_a=None, ev_b=None):
+    def step(ev=None):
+        if scrub is not None:
+            scrub.fill_(1)
+        if ev is not None:
+            ev[0].record(stream)
         bm.rebuild(stream)  # a1: tile classes + work order, into the same buffer
-        if ev_a is not None:
-            ev_a.record(stream)
+        if ev is not None:
+            ev[1].record(stream)
         attn.attn_fwd_into(q, k, v, o, lse, scale=w.scale, block_mask=bm, stream=stream,
                            **mask_kw, **score_kw)
-        if ev_b is not None:
-            ev_b.record(stream)
+        if ev is not None:
+            ev[2].record(stream)
 
     for _ in range(warmup):
         step()
     torch.cuda.synchronize(dev)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(steps)]
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
     start.record(stream)
-    for a, b in evs:
-        step(a, b)
+    for e in evs:
+        step(e)
     end.record(stream)
     torch.cuda.synchronize(dev)
-    total_ms = start.elapsed_time(end)
-    kern_ms = [a.elapsed_time(b) for a, b in evs]
+    kern_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    mask_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    if flush_l2:
+        total_ms = sum(e[0].elapsed_time(e[2]) for e in evs)
+    else:
+        total_ms = start.elapsed_time(end)
     st = attn.get_device_status(device=dev)
     if st != 0:
         raise RuntimeError("device status %s" % attn.status_string(st))
-    return total_ms / steps, statistics.mean(kern_ms), statistics.median(kern_ms)
+    return {"ms_step": total_ms / steps, "kernel_ms_mean": statistics.mean(kern_ms),
+            "kernel_ms_median": statistics.median(kern_ms),
+            "kernel_ms_p10": quantile(kern_ms, 0.1), "kernel_ms_p90": quantile(kern_ms, 0.9),
+            "mask_build_ms": statistics.mean(mask_ms)}
 
 
 def time_pair(attn, w, inp, dev, steps, warmup, flops, peak):
@@ -262,7 +286,8 @@ def time_pair(attn, w, inp, dev, steps, warmup, flops, peak):
     its step time and the pair kernel's own throughput."""
     attn.set_option("cta_pair", 1)
     try:
-        ms, kms, _ = time_workload(attn, w, inp, dev, steps, warmup)
+        t = time_workload(attn, w, inp, dev, steps, warmup)
+        ms, kms = t["ms_step"], t["kernel_ms_mean"]
     finally:
         attn.set_option("cta_pair", 0)
     kt = flops / (kms * 1e-3) / 1e12
@@ -474,8 +499,8 @@ def main():
 
     barrier(world)
     with ClockSampler(local) as clk:
-        ms_step, kern_ms_mean, kern_ms_med = time_workload(attn, w, inp, dev, args.steps,
-                                                           args.warmup)
+        tw = time_workload(attn, w, inp, dev, args.steps, args.warmup)
+    ms_step, kern_ms_mean = tw["ms_step"], tw["kernel_ms_mean"]
     clocks = clk.summary()
     ms_step_max = max_over_ranks(ms_step, world)
     value = world * flops / (ms_step_max * 1e-3) / 1e12
@@ -488,7 +513,8 @@ def main():
                 "frac": achieved / peak, "traffic": profiled_traffic(w.name),
                 "algorithmic_bytes": algorithmic_bytes(w),
                 "kernel": "attn_fwd_kernel", "kernel_ms_mean": kern_ms_mean,
-                "kernel_ms_median": kern_ms_med,
+                "kernel_ms_median": tw["kernel_ms_median"],
+                "kernel_ms_p10": tw["kernel_ms_p10"], "kernel_ms_p90": tw["kernel_ms_p90"],
                 "peak_kind": "%s burst bf16 (cuBLAS)" % peak_kind}
 
     e2e = None
@@ -505,7 +531,11 @@ def main():
             bsteps = min(max(3, args.steps // 100), 20)
             if name == w.name:
                 per[name] = {"tflops": value / world, "kernel_tflops": achieved,
-                             "ms_per_step": ms_step, "frac": achieved / peak}
+                             "ms_per_step": ms_step, "frac": achieved / peak,
+                             "kernel_ms_median": tw["kernel_ms_median"],
+                             "kernel_ms_p10": tw["kernel_ms_p10"],
+                             "kernel_ms_p90": tw["kernel_ms_p90"],
+                             "mask_build_ms": tw["mask_build_ms"]}
                 bms = time_backward(attn, w, inp, dev, bsteps, 3)
                 per[name].update(bwd_ms=bms, bwd_tflops=2.5 * flops / (bms * 1e-3) / 1e12)
                 if w.D == 128:
@@ -515,12 +545,23 @@ def main():
             ix = workloads.generate(wx)
             px = visible_pairs(wx, ix.get("doc_ids"), ix.get("prefix_len"))
             fx = useful_flops(wx, px)
-            msx, kx, _ = time_workload(attn, wx, ix, dev, min(max(5, args.steps // 4), 500), 3)
+            tx = time_workload(attn, wx, ix, dev, min(max(5, args.steps // 4), 500), 3)
+            msx, kx = tx["ms_step"], tx["kernel_ms_mean"]
             per[name] = {"tflops": fx / (msx * 1e-3) / 1e12,
                          "kernel_tflops": fx / (kx * 1e-3) / 1e12,
                          "ms_per_step": msx, "kernel_ms": kx,
+                         "kernel_ms_median": tx["kernel_ms_median"],
+                         "kernel_ms_p10": tx["kernel_ms_p10"],
+                         "kernel_ms_p90": tx["kernel_ms_p90"],
+                         "mask_build_ms": tx["mask_build_ms"],
                          "frac": fx / (kx * 1e-3) / 1e12 / peak,
                          "hbm_gbs": algorithmic_bytes(wx) / (kx * 1e-3) / 1e9}
+            if wx.S_q * wx.B * wx.H <= 4096:
+                # the launch-bound tiny case, again from cold L2 each step
+                tc = time_workload(attn, wx, ix, dev, min(max(5, args.steps // 20), 100), 3,
+                                   flush_l2=True)
+                per[name].update(kernel_ms_l2_flushed=tc["kernel_ms_median"],
+                                 ms_per_step_l2_flushed=tc["ms_step"])
             # backward: 2.5x the forward's useful FLOPs (dQ, dK, dV and the
             # recomputed S and dP over the visible pairs, the usual count)
             bms = time_backward(attn, wx, ix, dev, bsteps, 3)
