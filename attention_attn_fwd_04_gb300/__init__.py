@@ -363,11 +363,14 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, *, return_lse: b
 
 def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor,
              lse: torch.Tensor, dout: torch.Tensor, *, scale: Optional[float] = None,
-             stream: Optional[torch.cuda.Stream] = None, **mods):
+             stream: Optional[torch.cuda.Stream] = None, dq: Optional[torch.Tensor] = None,
+             dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None, **mods):
     """Gradients of :func:`attn_fwd`: returns ``(dQ, dK, dV)`` (bf16, shapes
     of q, k, v) for the upstream gradient ``dout`` of ``out``.  ``out`` and
     ``lse`` are the forward's results for the same inputs, scale and mods
-    (keywords as for :func:`attn_fwd`, without ``block_mask``)."""
+    (keywords as for :func:`attn_fwd`, without ``block_mask``).  ``dq``,
+    ``dk``, ``dv``: caller-provided outputs (contiguous bf16, the shapes of
+    q, k, v), written and returned instead of new tensors."""
     B, H, S_q, D = q.shape
     _, H_kv, S_k, _ = k.shape
     dev = q.device
@@ -386,9 +389,14 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tenso
         raise ValueError("attn_bwd builds its own block masks")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    dq = torch.empty_like(q)
-    dk = torch.empty_like(k)
-    dv = torch.empty_like(v)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t, shape in (("dq", dq, (B, H, S_q, D)), ("dk", dk, (B, H_kv, S_k, D)),
+                           ("dv", dv, (B, H_kv, S_k, D))):
+        if (t.device != dev or t.dtype != torch.bfloat16 or not t.is_contiguous()
+                or tuple(t.shape) != shape):
+            raise ValueError("%s must be a contiguous bfloat16 %s tensor on %s" % (name, shape, dev))
     m, keep = _mod_desc(**mods)
     with torch.cuda.device(dev):
         st = _lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),

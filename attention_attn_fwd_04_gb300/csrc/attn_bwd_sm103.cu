@@ -201,6 +201,27 @@ __device__ __forceinline__ void mma_tn(uint32_t tmem_c, uint32_t tmem_a, uint64_
                       idesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
+// 32-byte global store (one full sector per lane); addr 32-byte aligned.
+__device__ __forceinline__ void stg_v8(void* addr, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(addr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+// 32 bf16 values (16 packed words) to a row: whole 32-byte sectors when the
+// tensor is 32-byte aligned (rows are), 16-byte stores otherwise.
+__device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&pk)[16],
+                                            bool al32) {
+  if (al32) {
+    stg_v8(dst, pk);
+    stg_v8(dst + 16, pk + 8);
+  } else {
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) d4[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+  }
+}
+
 // After an abort, let a loader's copies in flight land before the CTA
 // exits: wait (bounded) for the last phase issued on each of n_stages
 // barriers that saw `issued` loads in total (round-robin).
@@ -784,26 +805,29 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
         if (!ok) break;
       }
       ptx::tc_fence_after();
+      {
+        // every load in flight before one wait; dQ's columns are free for the
+        // next item as soon as they have landed
+        uint32_t o[D / 64][32];
 #pragma unroll
-      for (int c4 = 0; c4 < D / 64; ++c4) {
-        uint32_t o[32];
-        ptx::tmem_ld32(tQ + (uint32_t)(c4 * 32), o);
+        for (int c4 = 0; c4 < D / 64; ++c4) ptx::tmem_ld32(tQ + (uint32_t)(c4 * 32), o[c4]);
         ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(DQE));
         if (valid) {
-          uint32_t pk[16];
+          const bool al32 = (reinterpret_cast<uintptr_t>(p.dq) & 31u) == 0;
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
-            pk[c] = ptx::pack_bf16x2(__uint_as_float(o[2 * c]) * p.scale,
-                                     __uint_as_float(o[2 * c + 1]) * p.scale);
-          uint4* dst = reinterpret_cast<uint4*>(dqrow + c4 * 32);
+          for (int c4 = 0; c4 < D / 64; ++c4) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            for (int c = 0; c < 16; ++c)
+              pk[c] = ptx::pack_bf16x2(__uint_as_float(o[c4][2 * c]) * p.scale,
+                                       __uint_as_float(o[c4][2 * c + 1]) * p.scale);
+            store_row32(dqrow + c4 * 32, pk, al32);
+          }
         }
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(DQE));
       ++act;
     }
   }
@@ -1201,32 +1225,37 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
         if (!ok) break;
       }
       ptx::tc_fence_after();
+      {
+        // every load in flight before one wait; the accumulators are free
+        // for the next item as soon as they have landed
+        uint32_t ov[D / 64][32], ok32[D / 64][32];
 #pragma unroll
-      for (int c4 = 0; c4 < D / 64; ++c4) {
-        uint32_t ov[32], ok32[32];
-        ptx::tmem_ld32(tDV + (uint32_t)(c4 * 32), ov);
-        ptx::tmem_ld32(tDK + (uint32_t)(c4 * 32), ok32);
+        for (int c4 = 0; c4 < D / 64; ++c4) {
+          ptx::tmem_ld32(tDV + (uint32_t)(c4 * 32), ov[c4]);
+          ptx::tmem_ld32(tDK + (uint32_t)(c4 * 32), ok32[c4]);
+        }
         ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(AE));
         if (valid) {
-          uint32_t pv[16], pkk[16];
+          const bool al32 = ((reinterpret_cast<uintptr_t>(p.dk) | reinterpret_cast<uintptr_t>(p.dv)) &
+                             31u) == 0;
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            pv[c] = ptx::pack_bf16x2(__uint_as_float(ov[2 * c]), __uint_as_float(ov[2 * c + 1]));
-            pkk[c] = ptx::pack_bf16x2(__uint_as_float(ok32[2 * c]) * p.scale,
-                                      __uint_as_float(ok32[2 * c + 1]) * p.scale);
-          }
-          uint4* dv4 = reinterpret_cast<uint4*>(dvrow + c4 * 32);
-          uint4* dk4 = reinterpret_cast<uint4*>(dkrow + c4 * 32);
+          for (int c4 = 0; c4 < D / 64; ++c4) {
+            uint32_t pv[16], pkk[16];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            dv4[c] = make_uint4(pv[4 * c], pv[4 * c + 1], pv[4 * c + 2], pv[4 * c + 3]);
-            dk4[c] = make_uint4(pkk[4 * c], pkk[4 * c + 1], pkk[4 * c + 2], pkk[4 * c + 3]);
+            for (int c = 0; c < 16; ++c) {
+              pv[c] = ptx::pack_bf16x2(__uint_as_float(ov[c4][2 * c]),
+                                       __uint_as_float(ov[c4][2 * c + 1]));
+              pkk[c] = ptx::pack_bf16x2(__uint_as_float(ok32[c4][2 * c]) * p.scale,
+                                        __uint_as_float(ok32[c4][2 * c + 1]) * p.scale);
+            }
+            store_row32(dvrow + c4 * 32, pv, al32);
+            store_row32(dkrow + c4 * 32, pkk, al32);
           }
         }
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(AE));
       ++act;
     }
   }

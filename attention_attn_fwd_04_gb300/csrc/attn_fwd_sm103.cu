@@ -116,6 +116,14 @@ struct Cfg {
   static constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
 };
 
+
+// 32-byte global store (one full sector per lane); addr 32-byte aligned.
+__device__ __forceinline__ void stg_v8(void* addr, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(addr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 struct KParams {
   CUtensorMap tmap_q;
   CUtensorMap tmap_k;
@@ -999,26 +1007,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // LSE = -inf (l itself may hold the polynomial's tiny values).
       const bool seen = m_ref != -INFINITY && l > 0.f;
       const float inv_l = seen ? 1.0f / l : 0.f;
+      {
+        // all of O's loads in flight before one wait; Tensor Memory is free
+        // for the next item's first PV as soon as they have landed
+        uint32_t o[D / 32][32];
 #pragma unroll
-      for (int c4 = 0; c4 < D / 32; ++c4) {
-        uint32_t o[32];
-        ptx::tmem_ld32(tO + (uint32_t)(c4 * 32), o);
+        for (int c4 = 0; c4 < D / 32; ++c4) ptx::tmem_ld32(tO + (uint32_t)(c4 * 32), o[c4]);
         ptx::tmem_wait_ld();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive(B_OE + t);
+        const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
         if (valid) {
-          uint32_t pk[16];
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
-            pk[c] = ptx::pack_bf16x2(__uint_as_float(o[2 * c]) * inv_l,
-                                     __uint_as_float(o[2 * c + 1]) * inv_l);
-          uint4* dst = reinterpret_cast<uint4*>(orow + c4 * 32);
+          for (int c4 = 0; c4 < D / 32; ++c4) {
+            uint32_t pk[16];
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
-            dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            for (int c = 0; c < 16; ++c)
+              pk[c] = ptx::pack_bf16x2(__uint_as_float(o[c4][2 * c]) * inv_l,
+                                       __uint_as_float(o[c4][2 * c + 1]) * inv_l);
+            if (out32) {  // rows start 32-byte aligned: whole sectors per lane
+              stg_v8(orow + c4 * 32, pk);
+              stg_v8(orow + c4 * 32 + 16, pk + 8);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c4 * 32);
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+            }
+          }
         }
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) arrive(B_OE + t);
       if (valid && p.lse) p.lse[row_id] = seen ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
       ++act;
     }

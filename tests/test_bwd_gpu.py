@@ -125,6 +125,29 @@ def test_backward_sampled_at_size(attn):
     check("dV", dv.reshape(-1, D)[torch.from_numpy(keys)], ref_dv)
 
 
+def test_backward_outputs_aligned_to_16_bytes_only(attn):
+    # dQ, dK, dV 16- but not 32-byte aligned take the epilogues' 16-byte
+    # stores (32-byte aligned outputs take 32-byte stores): identical results
+    B, H, Hkv, S, D = 1, 4, 2, 500, 128
+    q, k, v, do = inputs(B, H, Hkv, S, S, D, seed=510)
+    qd, kd, vd, dod = (t.to(DEV) for t in (q, k, v, do))
+    o, lse = attn.attn_fwd(qd, kd, vd, causal=True)
+    ref = attn.attn_bwd(qd, kd, vd, o, lse, dod, causal=True)
+
+    def off16(shape):
+        n = math.prod(shape)
+        t = torch.empty(n + 16, dtype=torch.bfloat16, device=DEV)[8:8 + n].view(shape)
+        assert t.data_ptr() % 32 == 16
+        return t
+
+    bufs = (off16(q.shape), off16(k.shape), off16(v.shape))
+    got = attn.attn_bwd(qd, kd, vd, o, lse, dod, causal=True, dq=bufs[0], dk=bufs[1], dv=bufs[2])
+    torch.cuda.synchronize()
+    assert attn.get_device_status(device=DEV) == 0
+    for g, b, r in zip(got, bufs, ref):
+        assert g is b and torch.equal(g, r)
+
+
 MODS3 = [
     (1, 2, 2, 300, 128, {"rel": 6, "causal": True}),
     (2, 2, 2, 400, 64, {"blocks": "batched", "rel": 3, "softcap": 8.0}),

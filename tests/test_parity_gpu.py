@@ -427,6 +427,25 @@ def test_wait_timeout_is_reported_and_context_survives(attn):
     run_and_compare(attn, q, k, v, 1 / math.sqrt(D), causal=True)
 
 
+@pytest.mark.parametrize("D", [128, 64])
+def test_output_aligned_to_16_bytes_only(attn, D):
+    # out 16- but not 32-byte aligned takes the epilogue's 16-byte stores
+    # (32-byte aligned outputs take 32-byte stores): identical results
+    B, H, S = 1, 2, 700
+    q, k, v = rand_inputs(B, H, H, S, S, D, seed=31)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    o_ref, l_ref = attn.attn_fwd(qd, kd, vd, causal=True)
+    assert o_ref.data_ptr() % 32 == 0
+    n = o_ref.numel()
+    flat = torch.empty(n + 16, dtype=torch.bfloat16, device=DEV)
+    out = flat[8:8 + n].view(B, H, S, D)
+    assert out.data_ptr() % 32 == 16
+    lse = torch.empty_like(l_ref)
+    attn.attn_fwd_into(qd, kd, vd, out, lse, causal=True)
+    assert attn.get_device_status(device=DEV) == 0
+    assert torch.equal(out, o_ref) and torch.equal(lse, l_ref)
+
+
 def test_gqa_equals_repeated_kv(attn):
     B, H, Hkv, S, D = 1, 8, 2, 333, 128
     q, k, v = rand_inputs(B, H, Hkv, S, S, D, seed=15)
