@@ -201,20 +201,13 @@ __device__ __forceinline__ void mma_tn(uint32_t tmem_c, uint32_t tmem_a, uint64_
                       idesc, (accumulate || kk > 0) ? 1u : 0u);
 }
 
-// 32-byte global store (one full sector per lane); addr 32-byte aligned.
-__device__ __forceinline__ void stg_v8(void* addr, const uint32_t* v) {
-  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(addr), "r"(v[0]),
-               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-               : "memory");
-}
-
 // 32 bf16 values (16 packed words) to a row: whole 32-byte sectors when the
 // tensor is 32-byte aligned (rows are), 16-byte stores otherwise.
 __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (&pk)[16],
                                             bool al32) {
   if (al32) {
-    stg_v8(dst, pk);
-    stg_v8(dst + 16, pk + 8);
+    ptx::stg_v8(dst, pk);
+    ptx::stg_v8(dst + 16, pk + 8);
   } else {
     uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll

@@ -117,13 +117,6 @@ struct Cfg {
 };
 
 
-// 32-byte global store (one full sector per lane); addr 32-byte aligned.
-__device__ __forceinline__ void stg_v8(void* addr, const uint32_t* v) {
-  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(addr), "r"(v[0]),
-               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
-               : "memory");
-}
-
 struct KParams {
   CUtensorMap tmap_q;
   CUtensorMap tmap_k;
@@ -1027,8 +1020,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               pk[c] = ptx::pack_bf16x2(__uint_as_float(o[c4][2 * c]) * inv_l,
                                        __uint_as_float(o[c4][2 * c + 1]) * inv_l);
             if (out32) {  // rows start 32-byte aligned: whole sectors per lane
-              stg_v8(orow + c4 * 32, pk);
-              stg_v8(orow + c4 * 32 + 16, pk + 8);
+              ptx::stg_v8(orow + c4 * 32, pk);
+              ptx::stg_v8(orow + c4 * 32 + 16, pk + 8);
             } else {
               uint4* dst = reinterpret_cast<uint4*>(orow + c4 * 32);
 #pragma unroll

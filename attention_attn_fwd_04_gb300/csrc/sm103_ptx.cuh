@@ -99,6 +99,14 @@ __device__ __forceinline__ int ld_volatile_shared(uint32_t addr) {
   return v;
 }
 
+// 32-byte global store of eight words (one full 32-byte sector per lane);
+// addr must be 32-byte aligned.
+__device__ __forceinline__ void stg_v8(void* addr, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(addr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
 // ----------------------------------------------------------------- TMA ----
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
