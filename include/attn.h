@@ -154,7 +154,8 @@ typedef struct attn_mod_desc {
  *
  *  q, k, v  device, bf16, layouts above, 16-byte aligned
  *  out      device, bf16 [B][H][S_q][D], 16-byte aligned, must not overlap
- *           the inputs
+ *           the inputs; 32-byte aligned is faster (each row is written in
+ *           32-byte stores, else in 16-byte ones; the results are the same)
  *  lse      device, fp32 [B][H][S_q], 4-byte aligned, or NULL to skip it
  *  B, H, H_kv, S_q, S_k  > 0, H % H_kv == 0, S_q and S_k < 2^30
  *  D        head dimension, 64 or 128 (others: ATTN_ERR_UNSUPPORTED)
@@ -324,7 +325,8 @@ attn_status attn_fwd_host(const void *q, const void *k, const void *v,
  *                      are rebuilt, forward and transposed, into a
  *                      library-owned per-device buffer)
  *
- * All tensors 16-byte aligned (lse 4-byte), outputs overlapping nothing.
+ * All tensors 16-byte aligned (lse 4-byte), outputs overlapping nothing;
+ * dq, dk and dv 32-byte aligned take 32-byte stores (same results).
  * Deterministic: no atomics, every output row is written once.  Errors as
  * for attn_fwd; device-side failures are read with attn_get_device_status.
  * Calls that share the library's buffer must not run concurrently on
