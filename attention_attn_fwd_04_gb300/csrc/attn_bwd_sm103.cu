@@ -46,6 +46,7 @@
 // 128-wide operand is contiguous at column 32 for the MMA that reads it.
 // Every wait is bounded like the forward's: on expiry the kernel records
 // ATTN_ERR_TIMEOUT and returns.
+#include <atomic>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -211,7 +212,8 @@ __device__ __forceinline__ void store_row32(__nv_bfloat16* dst, const uint32_t (
   } else {
     uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) d4[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+    for (int c = 0; c < 4; ++c)
+      d4[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
   }
 }
 
@@ -1232,8 +1234,9 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar(AE));
         if (valid) {
-          const bool al32 = ((reinterpret_cast<uintptr_t>(p.dk) | reinterpret_cast<uintptr_t>(p.dv)) &
-                             31u) == 0;
+          const uintptr_t kv_bits =
+              reinterpret_cast<uintptr_t>(p.dk) | reinterpret_cast<uintptr_t>(p.dv);
+          const bool al32 = (kv_bits & 31u) == 0;
 #pragma unroll
           for (int c4 = 0; c4 < D / 64; ++c4) {
             uint32_t pv[16], pkk[16];
@@ -1297,10 +1300,21 @@ bool bmake_map(CUtensorMap* map, const void* ptr, int D, int S, int outer) {
   return r == CUDA_SUCCESS;
 }
 
+// The opt-in shared memory size is a function attribute: it is set once per
+// device and kernel (attr_set: that kernel's flag for this device, or null
+// to set it on every call).  A concurrent first call repeats the same
+// idempotent call.
+constexpr int kBLaunchCacheDevices = 64;
+
 template <typename K>
-cudaError_t launch_ex(K kern, int grid, int smem, cudaStream_t stream, const BParams& bp) {
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (err != cudaSuccess) return err;
+cudaError_t launch_ex(K kern, int grid, int smem, cudaStream_t stream, const BParams& bp,
+                      std::atomic<bool>* attr_set) {
+  if (attr_set == nullptr || !attr_set->load(std::memory_order_relaxed)) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (attr_set != nullptr) attr_set->store(true, std::memory_order_relaxed);
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3(kBThreads, 1, 1);
@@ -1315,24 +1329,28 @@ cudaError_t launch_ex(K kern, int grid, int smem, cudaStream_t stream, const BPa
 }
 
 template <int D, bool ALIBI, bool SOFTCAP>
-cudaError_t launch_bwd_variant(BParams bp, int sms, cudaStream_t s) {
+cudaError_t launch_bwd_variant(BParams bp, int sms, cudaStream_t s, int dev) {
   using C = BCfg<D>;
+  static std::atomic<bool> set_dq[kBLaunchCacheDevices], set_kv[kBLaunchCacheDevices];
+  const bool cache = dev >= 0 && dev < kBLaunchCacheDevices;
   bp.n_items = bp.B * bp.H * bp.nQ;
   const int g1 = bp.n_items < sms ? bp.n_items : sms;
-  cudaError_t err =
-      launch_ex(bwd_dq_kernel<D, ALIBI, SOFTCAP>, g1 > 0 ? g1 : 1, C::kSmemAllocDq, s, bp);
+  cudaError_t err = launch_ex(bwd_dq_kernel<D, ALIBI, SOFTCAP>, g1 > 0 ? g1 : 1, C::kSmemAllocDq,
+                              s, bp, cache ? &set_dq[dev] : nullptr);
   if (err != cudaSuccess) return err;
   bp.n_items = bp.B * bp.H_kv * bp.nK;
   const int g2 = bp.n_items < sms ? bp.n_items : sms;
-  return launch_ex(bwd_dkdv_kernel<D, ALIBI, SOFTCAP>, g2 > 0 ? g2 : 1, C::kSmemAllocKv, s, bp);
+  return launch_ex(bwd_dkdv_kernel<D, ALIBI, SOFTCAP>, g2 > 0 ? g2 : 1, C::kSmemAllocKv, s, bp,
+                   cache ? &set_kv[dev] : nullptr);
 }
 
 template <int D>
-cudaError_t launch_bwd_d(const BParams& bp, bool alibi, bool softcap, int sms, cudaStream_t s) {
-  if (alibi && softcap) return launch_bwd_variant<D, true, true>(bp, sms, s);
-  if (alibi) return launch_bwd_variant<D, true, false>(bp, sms, s);
-  if (softcap) return launch_bwd_variant<D, false, true>(bp, sms, s);
-  return launch_bwd_variant<D, false, false>(bp, sms, s);
+cudaError_t launch_bwd_d(const BParams& bp, bool alibi, bool softcap, int sms, cudaStream_t s,
+                         int dev) {
+  if (alibi && softcap) return launch_bwd_variant<D, true, true>(bp, sms, s, dev);
+  if (alibi) return launch_bwd_variant<D, true, false>(bp, sms, s, dev);
+  if (softcap) return launch_bwd_variant<D, false, true>(bp, sms, s, dev);
+  return launch_bwd_variant<D, false, false>(bp, sms, s, dev);
 }
 
 }  // namespace
@@ -1412,13 +1430,19 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
                                              a.rowstat, a.rowstat + padded, BH, a.S_q, g.nQ);
   if (err != cudaSuccess) return err;
   int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return cudaErrorUnknown;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorUnknown;
+  static std::atomic<int> sm_count[kBLaunchCacheDevices];
+  const bool cache = dev >= 0 && dev < kBLaunchCacheDevices;
+  if (cache) sms = sm_count[dev].load(std::memory_order_relaxed);
+  if (sms == 0) {
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return cudaErrorUnknown;
+    if (cache) sm_count[dev].store(sms, std::memory_order_relaxed);
+  }
   const bool alibi = (a.score_flags & (ATTN_SCORE_ALIBI | ATTN_SCORE_RELBIAS)) != 0;
   const bool softcap = (a.score_flags & ATTN_SCORE_SOFTCAP) != 0;
-  if (a.D == 64) return launch_bwd_d<64>(bp, alibi, softcap, sms, stream);
-  return launch_bwd_d<128>(bp, alibi, softcap, sms, stream);
+  if (a.D == 64) return launch_bwd_d<64>(bp, alibi, softcap, sms, stream, dev);
+  return launch_bwd_d<128>(bp, alibi, softcap, sms, stream, dev);
 }
 
 }  // namespace attn

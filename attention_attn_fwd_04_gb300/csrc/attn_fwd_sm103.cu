@@ -44,6 +44,7 @@
 // records ATTN_ERR_TIMEOUT in the device status word (and raises the abort
 // flag of both CTAs of a pair), drains its own in-flight copies and MMAs,
 // frees Tensor Memory and returns.
+#include <atomic>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -1094,12 +1095,25 @@ bool make_map(CUtensorMap* map, const void* ptr, int D, int S, int outer,
 // grid: CTAs wanted (a CTA pair counts two); PAIR launches clusters of two
 // and caps the grid at the pairs that fit on the GPU at once, so that every
 // pair of the persistent schedule is resident.
+// Launch-time queries that do not change for a device are made once per
+// device and kernel instantiation: the opt-in shared memory size (a function
+// attribute) and, for CTA pairs, how many clusters fit.  A concurrent first
+// call only repeats the same idempotent query.
+constexpr int kLaunchCacheDevices = 64;
+
 template <int D, bool ALIBI, bool SOFTCAP, bool PAIR, bool QUAD>
-cudaError_t launch_variant(const KParams& kp, int grid, cudaStream_t stream) {
+cudaError_t launch_variant(const KParams& kp, int grid, cudaStream_t stream, int dev) {
   auto kern = attn_fwd_kernel<D, ALIBI, SOFTCAP, PAIR, QUAD>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<D, PAIR>::kSmemAlloc);
-  if (err != cudaSuccess) return err;
+  static std::atomic<bool> attr_set[kLaunchCacheDevices];
+  static std::atomic<int> clusters[kLaunchCacheDevices];
+  const bool cache = dev >= 0 && dev < kLaunchCacheDevices;
+  cudaError_t err = cudaSuccess;
+  if (!cache || !attr_set[dev].load(std::memory_order_relaxed)) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Cfg<D, PAIR>::kSmemAlloc);
+    if (err != cudaSuccess) return err;
+    if (cache) attr_set[dev].store(true, std::memory_order_relaxed);
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = Cfg<D, PAIR>::kSmemAlloc;
@@ -1117,10 +1131,13 @@ cudaError_t launch_variant(const KParams& kp, int grid, cudaStream_t stream) {
     cfg.numAttrs = 2;
     int pairs = (grid + 1) / 2;
     cfg.gridDim = dim3(2u * (unsigned)pairs, 1, 1);
-    int resident = 0;
-    err = cudaOccupancyMaxActiveClusters(&resident, kern, &cfg);
-    if (err != cudaSuccess) return err;
-    if (resident < 1) return cudaErrorInvalidConfiguration;
+    int resident = cache ? clusters[dev].load(std::memory_order_relaxed) : 0;
+    if (resident == 0) {
+      err = cudaOccupancyMaxActiveClusters(&resident, kern, &cfg);
+      if (err != cudaSuccess) return err;
+      if (resident < 1) return cudaErrorInvalidConfiguration;
+      if (cache) clusters[dev].store(resident, std::memory_order_relaxed);
+    }
     if (pairs > resident) pairs = resident;
     cfg.gridDim = dim3(2u * (unsigned)pairs, 1, 1);
   } else {
@@ -1130,11 +1147,12 @@ cudaError_t launch_variant(const KParams& kp, int grid, cudaStream_t stream) {
 }
 
 template <int D, bool PAIR, bool QUAD>
-cudaError_t launch_d(const KParams& kp, bool alibi, bool softcap, int grid, cudaStream_t s) {
-  if (alibi && softcap) return launch_variant<D, true, true, PAIR, QUAD>(kp, grid, s);
-  if (alibi) return launch_variant<D, true, false, PAIR, QUAD>(kp, grid, s);
-  if (softcap) return launch_variant<D, false, true, PAIR, QUAD>(kp, grid, s);
-  return launch_variant<D, false, false, PAIR, QUAD>(kp, grid, s);
+cudaError_t launch_d(const KParams& kp, bool alibi, bool softcap, int grid, cudaStream_t s,
+                     int dev) {
+  if (alibi && softcap) return launch_variant<D, true, true, PAIR, QUAD>(kp, grid, s, dev);
+  if (alibi) return launch_variant<D, true, false, PAIR, QUAD>(kp, grid, s, dev);
+  if (softcap) return launch_variant<D, false, true, PAIR, QUAD>(kp, grid, s, dev);
+  return launch_variant<D, false, false, PAIR, QUAD>(kp, grid, s, dev);
 }
 
 }  // namespace
@@ -1161,7 +1179,7 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
   if (!make_map(&kp.tmap_q, a.q, a.D, a.S_q, a.B * a.H) ||
       !make_map(&kp.tmap_k, a.k, a.D, a.S_k, a.B * a.H_kv) ||
       !make_map(&kp.tmap_v, a.v, a.D, a.S_k, a.B * a.H_kv) ||
-      !make_map(&kp.tmap_kh, a.k, a.D, a.S_k, a.B * a.H_kv, kTileN / 2))
+      (pair && !make_map(&kp.tmap_kh, a.k, a.D, a.S_k, a.B * a.H_kv, kTileN / 2)))
     return cudaErrorInvalidValue;
   BlockMaskGeom g = block_mask_geom(a.B, a.S_q, a.S_k, a.mask.flags, a.tpe);
   kp.out = reinterpret_cast<__nv_bfloat16*>(a.out);
@@ -1211,8 +1229,13 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
   int dev = 0, sms = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
-  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (err != cudaSuccess) return err;
+  static std::atomic<int> sm_count[kLaunchCacheDevices];
+  if (dev >= 0 && dev < kLaunchCacheDevices) sms = sm_count[dev].load(std::memory_order_relaxed);
+  if (sms == 0) {
+    err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    if (dev >= 0 && dev < kLaunchCacheDevices) sm_count[dev].store(sms, std::memory_order_relaxed);
+  }
   int grid = a.num_ctas > 0 ? a.num_ctas : sms;
   const int per_unit = pair ? 2 : 1;  // CTAs per work unit
   if (grid > kp.n_items * per_unit) grid = kp.n_items * per_unit;
@@ -1222,10 +1245,12 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
   const bool alibi = (a.score_flags & (ATTN_SCORE_ALIBI | ATTN_SCORE_RELBIAS)) != 0;
   const bool softcap = (a.score_flags & ATTN_SCORE_SOFTCAP) != 0;
   const bool quad = g.tpe == kTilesPerQuad;
-  if (a.D == 128 && pair) return launch_d<128, true, true>(kp, alibi, softcap, grid, stream);
-  if (a.D == 128 && !quad) return launch_d<128, false, false>(kp, alibi, softcap, grid, stream);
-  if (a.D == 64 && quad) return launch_d<64, false, true>(kp, alibi, softcap, grid, stream);
-  if (a.D == 64) return launch_d<64, false, false>(kp, alibi, softcap, grid, stream);
+  if (a.D == 128 && pair)
+    return launch_d<128, true, true>(kp, alibi, softcap, grid, stream, dev);
+  if (a.D == 128 && !quad)
+    return launch_d<128, false, false>(kp, alibi, softcap, grid, stream, dev);
+  if (a.D == 64 && quad) return launch_d<64, false, true>(kp, alibi, softcap, grid, stream, dev);
+  if (a.D == 64) return launch_d<64, false, false>(kp, alibi, softcap, grid, stream, dev);
   return cudaErrorInvalidValue;  // four-tile masks at D = 128 run on CTA pairs
 }
 

@@ -281,6 +281,49 @@ def time_workload(attn, w, inp, dev, steps, warmup, flush_l2=False):
             "mask_build_ms": statistics.mean(mask_ms)}
 
 
+def time_graph(attn, w, inp, dev, steps, warmup):
+    """A launch-bound workload's step (block-mask rebuild + forward, the
+    same C ABI calls) captured once in a CUDA graph and replayed: the
+    device-side cost of the step once host and Python launch overhead no
+    longer paces the GPU.  CUDA events around every replay."""
+    q, k, v = (inp[n].to(dev) for n in ("q", "k", "v"))
+    kw = mods_of(w, inp, dev)
+    mask_kw = {n: kw[n] for n in ("causal", "window", "doc_ids", "prefix_len", "q_offset") if n in kw}
+    score_kw = {n: kw[n] for n in ("alibi", "softcap") if n in kw}
+    o = torch.empty((w.B, w.H, w.S_q, w.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.H, w.S_q), dtype=torch.float32, device=dev)
+    bm = attn.build_block_mask(w.B, w.H, w.S_q, w.S_k, device=dev, **mask_kw)
+
+    def step(stream):
+        bm.rebuild(stream)
+        attn.attn_fwd_into(q, k, v, o, lse, scale=w.scale, block_mask=bm, stream=stream,
+                           **mask_kw, **score_kw)
+
+    for _ in range(warmup):
+        step(torch.cuda.current_stream(dev))
+    torch.cuda.synchronize(dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="thread_local"):
+        step(torch.cuda.current_stream(dev))
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, b in evs:
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    st = attn.get_device_status(device=dev)
+    if st != 0:
+        raise RuntimeError("device status %s" % attn.status_string(st))
+    ms = [a.elapsed_time(b) for a, b in evs]
+    return {"ms_per_step_graph": statistics.median(ms), "ms_per_step_graph_p10": quantile(ms, 0.1),
+            "ms_per_step_graph_p90": quantile(ms, 0.9)}
+
+
 def time_pair(attn, w, inp, dev, steps, warmup, flops, peak):
     """The same steps with the CTA-pair forward (option cta_pair; D = 128):
     its step time and the pair kernel's own throughput."""
@@ -577,6 +620,18 @@ def main():
             "tflops": fm_flops / (fm * 1e-3) / 1e12, "ms_per_step": fm,
             "frac": fm_flops / (fm * 1e-3) / 1e12 / peak, "visible_pairs": pm,
             "bwd_ms": bmm, "bwd_tflops": 2.5 * fm_flops / (bmm * 1e-3) / 1e12}
+
+    # last, so that a failed capture cannot disturb the numbers above: the
+    # launch-bound tiny workload replayed from a CUDA graph
+    if not args.no_per_workload:
+        for name, wx in workloads.WORKLOADS.items():
+            if wx.S_q * wx.B * wx.H > 4096 or name not in per:
+                continue
+            try:
+                per[name].update(time_graph(attn, wx, workloads.generate(wx), dev,
+                                            min(max(20, args.steps // 10), 200), 5))
+            except Exception as e:  # reported, not fatal
+                per[name]["graph_error"] = str(e)[:200]
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
