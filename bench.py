@@ -12,7 +12,10 @@ Metric: useful TFLOPS = 4 * D * (visible (query, key) pairs) / time, so the
 two GEMMs are counted only on unmasked pairs; softmax work is not counted.
 The headline workload is dense B=4 H=16 S=4096 D=128; the other named
 workloads are reported per mask type under "per_workload", each with the
-backward's time (attn_bwd) and its TFLOPS at 2.5x the forward's FLOPs.
+forward kernel's median / p10 / p90 duration, the block-mask rebuild's time,
+the backward's time (attn_bwd) and its TFLOPS at 2.5x the forward's FLOPs,
+and the CTA-pair forward for D = 128.  The launch-bound tiny workload is
+also timed from cold L2 and replayed from a CUDA graph.
 
 One JSON line is printed by rank 0.  With N > 1 (torchrun, one process per
 GPU) every rank runs an independent replica of the workload ("scaling":
@@ -22,7 +25,6 @@ from __future__ import annotations
 
 import argparse
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -37,9 +39,6 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 import workloads  # noqa: E402
-
-L2_BYTES = 129 * 1024 * 1024
-
 
 def visible_pairs(w: workloads.Workload, doc_ids=None, prefix_len=None) -> int:
     """Exact number of visible (query, key) pairs summed over batch and heads."""
