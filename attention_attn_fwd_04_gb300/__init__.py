@@ -19,7 +19,7 @@ from __future__ import annotations
 import ctypes
 import math
 import os
-from typing import Optional, Sequence, Tuple
+from typing import Optional, Tuple
 
 import torch
 
