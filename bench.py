@@ -435,7 +435,8 @@ def time_e2e(attn, w, inp, dev, steps, warmup):
 
 
 def oracle_sample(w, inp, target_s=15.0, seed=5):
-    """Time the fp64 oracle on a bounded row sample; returns (TFLOPS, rows, secs, cores)."""
+    """Time the fp64 oracle on a bounded row sample; returns (TFLOPS, rows,
+    secs, cores, visible pairs in the sample)."""
     import oracle
     cores = oracle.num_threads()
     g = torch.Generator().manual_seed(seed)
@@ -453,7 +454,7 @@ def oracle_sample(w, inp, target_s=15.0, seed=5):
     # useful pairs in the sample: each sampled row contributes its visible keys
     pairs_per_row = visible_pairs(w, inp.get("doc_ids"), inp.get("prefix_len")) / N
     flops = useful_flops(w, pairs_per_row * n)
-    return flops / secs / 1e12, n, secs, cores
+    return flops / secs / 1e12, n, secs, cores, pairs_per_row * n
 
 
 def run_reference(args, world, rank):
@@ -634,9 +635,12 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        tf, n, secs, cores = oracle_sample(w, inp, target_s=15.0)
+        tf, n, secs, cores, spairs = oracle_sample(w, inp, target_s=15.0)
         cpu = {"value": tf, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
-               "sample": "%d seeded query rows of %s (%.1f s)" % (n, w.name, secs)}
+               "sample": "%d seeded query rows of %s (%.1f s)" % (n, w.name, secs),
+               "rows_per_s": n / secs, "visible_pairs_per_s": spairs / secs,
+               # labelled extrapolation: the sample's rate over every visible pair
+               "extrapolated_full_workload_s": secs * pairs / spairs}
 
     if rank == 0:
         line = {
