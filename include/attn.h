@@ -64,7 +64,7 @@ typedef struct CUstream_st *attn_stream_t;
 typedef enum attn_status {
     ATTN_OK = 0,
     ATTN_ERR_INVALID_ARG = 1,  /* bad pointer, size, flag or descriptor     */
-    ATTN_ERR_UNSUPPORTED = 2,  /* valid request this build does not serve    */
+    ATTN_ERR_UNSUPPORTED = 2,  /* valid request the library does not serve  */
     ATTN_ERR_CUDA = 3,         /* a CUDA runtime/driver call failed          */
     ATTN_ERR_TIMEOUT = 4,      /* a device pipeline wait ran out of time     */
     ATTN_ERR_DEVICE_CHECK = 5  /* a device-side consistency check failed     */
