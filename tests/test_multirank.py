@@ -46,6 +46,7 @@ def test_two_gloo_ranks_take_the_max_step_time():
         pytest.skip("checks the CPU (gloo) path")
     world = 2
     port = _free_port()
-    out = mp.Manager().dict()
+    # spawn, not fork: the process may already run OpenMP threads (the oracle)
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
     assert out[0] == out[1] == 2.5
