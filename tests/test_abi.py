@@ -164,6 +164,47 @@ def test_block_mask_bytes_is_host_only(attn):
     assert lib.attn_block_mask_bytes(0, 1, 8, 8, None) == 0
 
 
+def test_block_mask_bytes_matches_the_documented_layout(attn):
+    # A 144-byte header, order[n] and cnt[n] (int32), list[n][nK] (uint32),
+    # each region 16-byte aligned, with n = (B if the mask depends on the
+    # batch, else 1) * ceil(S_q / 256); document masks add per-token key
+    # ranges [2][B][S_k], per-tile id ranges [2][B][nK] and one flag per
+    # 1024 tokens (int32 each).
+    lib = attn.lib()
+
+    def a16(x):
+        return (x + 15) // 16 * 16
+
+    def want(B, S_q, S_k, per_batch, docs):
+        nK = -(-S_k // 128)
+        n = (B if per_batch else 1) * -(-S_q // 256)
+        total = a16(a16(a16(a16(144) + 4 * n) + 4 * n) + 4 * n * nK)
+        if docs:
+            bm = B
+            total = a16(a16(a16(total + 8 * bm * S_k) + 8 * bm * nK) + 4 * bm * -(-S_k // 1024))
+        return total
+
+    m = attn.ModDesc()
+    m.version = 1
+    for B, S_q, S_k in ((4, 4096, 4096), (2, 300, 1000), (1, 1, 2 ** 21), (3, 5000, 5000)):
+        m.mask_flags = 0
+        assert lib.attn_block_mask_bytes(B, 8, S_q, S_k, ctypes.byref(m)) == want(B, S_q, S_k, 0, 0)
+        m.mask_flags = attn.MASK_CAUSAL
+        assert lib.attn_block_mask_bytes(B, 8, S_q, S_k, ctypes.byref(m)) == want(B, S_q, S_k, 0, 0)
+    # prefix-LM depends on the batch; documents need S_q == S_k.  The size
+    # query only checks that the mask arrays are given (host arrays here;
+    # it never reads them).
+    prefix = (ctypes.c_int32 * 3)(0, 100, 200)
+    docs = (ctypes.c_int32 * (2 * 3000))()
+    m.prefix_len = ctypes.cast(prefix, ctypes.c_void_p)
+    m.mask_flags = attn.MASK_PREFIX_LM
+    assert lib.attn_block_mask_bytes(3, 8, 700, 700, ctypes.byref(m)) == want(3, 700, 700, 1, 0)
+    m.prefix_len = None
+    m.doc_ids = ctypes.cast(docs, ctypes.c_void_p)
+    m.mask_flags = attn.MASK_CAUSAL | attn.MASK_DOCUMENT
+    assert lib.attn_block_mask_bytes(2, 8, 3000, 3000, ctypes.byref(m)) == want(2, 3000, 3000, 1, 1)
+
+
 def test_options_round_trip(attn):
     old = attn.get_option("rescale_threshold")
     attn.set_option("rescale_threshold", 0.0)
