@@ -65,3 +65,23 @@ def test_block_maps_one_per_batch_or_shared():
     for shared in (torch.ones((1, 2, 4), dtype=torch.uint8), torch.ones((2, 4), dtype=torch.uint8)):
         m, _ = a._mod_desc(blocks=shared)
         assert m.mask_flags == a.MASK_BLOCKS and m.blocks_batched == 0
+
+
+def test_missing_library_fails_loudly():
+    # no fallback: without the compiled library the first call raises
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = (
+        "import attention_attn_fwd_04_gb300 as a\n"
+        "a._LIB_PATH = '/nonexistent/libattn_gb300.so'\n"
+        "try:\n"
+        "    a.status_string(0)\n"
+        "except ImportError as e:\n"
+        "    print('raised', 'not built' in str(e))\n"
+        "else:\n"
+        "    print('no error')\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                       timeout=300)
+    assert "raised True" in r.stdout, r.stdout + r.stderr
