@@ -70,3 +70,22 @@ def test_quantile_interpolates_between_order_statistics():
     assert bench.quantile(xs, 0.1) == pytest.approx(1.4)
     assert bench.quantile(xs, 0.9) == pytest.approx(4.6)
     assert bench.quantile([7.0], 0.9) == 7.0
+
+
+def test_clock_record_parses_the_sampler_output():
+    c = bench.ClockSampler(0)
+    c.out = "\n".join([
+        "0, 2032, 2070, 910.5, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 2070, 2070, 1011.0, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "0, 1995, 2070, 1390.2, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, [N/A], 2070, 1390.2, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "garbage",
+    ])
+    got = c.summary()
+    assert got == {"sm_mhz": 2032.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"],
+                   "samples": 3}
+    c.out = "0, 1500, 2070, 700, 0x8, Active, Not Active, Active, Not Active"
+    assert c.summary()["reasons"] == ["hw_slowdown", "sw_thermal_slowdown"]
+    c.out = ""
+    assert c.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"],
+                           "samples": 0}
