@@ -108,12 +108,19 @@ def profiled_traffic(workload: str):
 
 
 def load_peaks():
+    """The measured peaks (the generated MEASURED_PEAKS.json), else the
+    fallback figures of an earlier GB300 measurement; says which."""
+    fallback = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
-        with open(path) as f:
-            d = json.load(f)
-        return d, "measured"
-    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+        try:
+            with open(path) as f:
+                d = json.load(f)
+            if float(d["bf16_tflops"]) > 0:
+                return d, "measured"
+        except (OSError, ValueError, KeyError, TypeError):
+            pass
+    return fallback, "fallback"
 
 
 class ClockSampler:

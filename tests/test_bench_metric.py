@@ -89,3 +89,16 @@ def test_clock_record_parses_the_sampler_output():
     c.out = ""
     assert c.summary() == {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"],
                            "samples": 0}
+
+
+def test_peaks_come_from_the_measured_file_else_the_fallback(tmp_path, monkeypatch):
+    peaks, kind = bench.load_peaks()
+    if kind == "measured":
+        assert peaks["bf16_tflops"] > 0
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.load_peaks() == ({"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                                   "bf16_tflops_sustained": 1700.0}, "fallback")
+    (tmp_path / "MEASURED_PEAKS.json").write_text('{"hbm_gbs": 7000}')
+    assert bench.load_peaks()[1] == "fallback"
+    (tmp_path / "MEASURED_PEAKS.json").write_text('{"bf16_tflops": 1850.5}')
+    assert bench.load_peaks() == ({"bf16_tflops": 1850.5}, "measured")
