@@ -34,6 +34,7 @@ __all__ = [
     "block_mask_bytes",
     "block_mask_stats",
     "get_device_status",
+    "get_noalloc_status",
     "set_option",
     "get_option",
     "status_string",
@@ -133,6 +134,8 @@ def _load() -> ctypes.CDLL:
         [ctypes.POINTER(ctypes.c_int64)] * 4
     lib.attn_get_device_status.restype = I
     lib.attn_get_device_status.argtypes = [P]
+    lib.attn_get_noalloc_status.restype = I
+    lib.attn_get_noalloc_status.argtypes = [P]
     lib.attn_set_option.restype = I
     lib.attn_set_option.argtypes = [I, ctypes.c_double]
     lib.attn_get_option.restype = I
@@ -464,6 +467,14 @@ def get_device_status(stream: Optional[torch.cuda.Stream] = None, device=None) -
     device = torch.device(device if device is not None else "cuda")
     with torch.cuda.device(device):
         return int(_lib.attn_get_device_status(_stream_ptr(stream, device)))
+
+
+def get_noalloc_status(stream: Optional[torch.cuda.Stream] = None, device=None) -> int:
+    """Synchronise and return (then clear) the status word of the
+    allocation-free entry point's fixed scratch array."""
+    device = torch.device(device if device is not None else "cuda")
+    with torch.cuda.device(device):
+        return int(_lib.attn_get_noalloc_status(_stream_ptr(stream, device)))
 
 
 def set_option(name: str, value: float) -> None:

@@ -302,7 +302,7 @@ attn_status enqueue_forward(const void* q, const void* k, const void* v, void* o
 // host it names a stand-in, not device memory); the device address comes
 // from cudaGetSymbolAddress, once per device.
 namespace {
-constexpr size_t kNoAllocStatusBytes = 256;
+constexpr size_t kNoAllocStatusBytes = ATTN_NOALLOC_STATUS_BYTES;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
 constexpr int kNoAllocMaxDevices = 64;
 std::mutex g_noalloc_mu;
@@ -476,7 +476,7 @@ attn_status attn_set_option(attn_option opt, double value) {
       g_opts.poly_fraction = value;
       return ATTN_OK;
     case ATTN_OPT_DEBUG_STALL:
-      if (value != 0.0 && value != 1.0) return ATTN_ERR_INVALID_ARG;
+      if (value != 0.0 && value != 1.0 && value != 2.0) return ATTN_ERR_INVALID_ARG;
       g_opts.debug_stall = value;
       return ATTN_OK;
     case ATTN_OPT_CTA_PAIR:
@@ -669,6 +669,22 @@ attn_status attn_fwd_noalloc(const void* q, const void* k, const void* v, void* 
   if (cudaMemsetAsync(status, 0, sizeof(DeviceStatus), s) != cudaSuccess) return ATTN_ERR_CUDA;
   return enqueue_forward(q, k, v, out, lse, B, H, H_kv, S_q, S_k, D, scale, mod, nullptr, bmask,
                          status, o, s);
+}
+
+attn_status attn_get_noalloc_status(attn_stream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ERR_CUDA;
+  void* scratch = nullptr;
+  attn_status st = noalloc_scratch(dev, &scratch);
+  if (st != ATTN_OK) return st;
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  DeviceStatus h;
+  if (cudaMemcpy(&h, scratch, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (h.code != 0 && cudaMemset(scratch, 0, sizeof(DeviceStatus)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return static_cast<attn_status>(h.code);
 }
 
 attn_status attn_fwd_host(const void* q, const void* k, const void* v, void* out, float* lse,
@@ -901,6 +917,7 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* ou
   a.status = scr->status;
   a.wait_budget_ms = o.wait_budget_ms;
   a.force_partial = fp;
+  a.debug_stall = (o.debug_stall == 1.0 || o.debug_stall == 2.0) ? (int)o.debug_stall : 0;
   return launch_attn_bwd(a, s) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -74,6 +74,7 @@ enum BSite : int {
   kBSiteMma = 120,
   kBSiteElem = 130,
   kBSiteDrain = 140,
+  kBSiteDebugStall = 150,  // + 1 in the dQ kernel, + 2 in the dK/dV kernel
 };
 
 template <int D>
@@ -134,6 +135,7 @@ struct BParams {
   int n_items;
   DeviceStatus* status;
   uint64_t budget_ns;
+  int debug_stall;  // test hook: 1 = the dQ kernel, 2 = the dK/dV kernel
 };
 
 struct BCtl {
@@ -419,8 +421,8 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
   constexpr int KS = C::kDqKStages, VS = C::kDqVStages;
   // KF/KE: K ring (KS each), VF/VE: V ring (VS each), DPF: one per dP buffer
   enum { QF = 0, QE = 1, SF = 2, DSF = 3, DQF = 4, DQE = 5, DRAIN = 6, SCON = 7, DPF = 8,
-         KF = 10, KE = KF + KS, VF = KE + KS, VE = VF + VS };
-  static_assert(VE + VS <= C::kNumBars, "barrier slots");
+         KF = 10, KE = KF + KS, VF = KE + KS, VE = VF + VS, NEVER = VE + VS };
+  static_assert(NEVER < C::kNumBars, "barrier slots");
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kDqBar + 8 * C::kNumBars);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kDqBar + 8 * C::kNumBars + 4);
   if (threadIdx.x == 0) {
@@ -443,6 +445,7 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
     ptx::mbar_init(bar(DPF + 1), 1);
     ptx::mbar_init(bar(SCON), 8);
     ptx::mbar_init(bar(DRAIN), 1);
+    ptx::mbar_init(bar(NEVER), 1);  // the test hook's: nothing arrives on it
     *s_abort = 0;
     ptx::fence_mbar_init();
   }
@@ -562,6 +565,10 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
       if (w >= p.n_items) break;
       const It it = item(w);
       if (nonempty(it) == 0) continue;
+      if (p.debug_stall == 1) {  // test hook: a wait nothing ever completes
+        ok = __all_sync(0xffffffffu, bwait(bar(NEVER), 0, ctl, kBSiteDebugStall + 1));
+        if (!ok) break;
+      }
       ok = waitw(bar(QF), act & 1);
       if (!ok) break;
       // Software pipeline over the item's key tiles u (tile g = kv0 + u of
@@ -850,7 +857,8 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
 
   auto bar = [&](int i) { return sbase + (uint32_t)(C::kKvBar + 8 * i); };
   enum { KF = 0, KE = 1, QF = 2, QE = 4, SF = 6, PF = 7, AF = 8, AE = 9, DRAIN = 10, DPF = 11,
-         DSF = 12 };
+         DSF = 12, NEVER = 13 };
+  static_assert(NEVER < C::kNumBars, "barrier slots");
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kKvBar + 8 * C::kNumBars);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kKvBar + 8 * C::kNumBars + 4);
   if (threadIdx.x == 0) {
@@ -868,6 +876,7 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
     ptx::mbar_init(bar(DPF), 1);
     ptx::mbar_init(bar(DSF), 8);
     ptx::mbar_init(bar(DRAIN), 1);
+    ptx::mbar_init(bar(NEVER), 1);  // the test hook's: nothing arrives on it
     *s_abort = 0;
     ptx::fence_mbar_init();
   }
@@ -973,6 +982,10 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
       if (w >= p.n_items) break;
       const It it = item(w);
       if (it.n == 0) continue;
+      if (p.debug_stall == 2) {  // test hook: a wait nothing ever completes
+        ok = __all_sync(0xffffffffu, bwait(bar(NEVER), 0, ctl, kBSiteDebugStall + 2));
+        if (!ok) break;
+      }
       ok = waitw(bar(KF), act & 1);
       if (ok && act > 0) ok = waitw(bar(AE), (act - 1) & 1);
       if (!ok) break;
@@ -1407,6 +1420,7 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
   bp.status = a.status;
   const double ms = a.wait_budget_ms > 0 ? a.wait_budget_ms : 2000.0;
   bp.budget_ns = (uint64_t)(ms * 1e6);
+  bp.debug_stall = a.debug_stall;
 
   // row statistics, then the two gradient kernels
   const int BH = a.B * a.H;

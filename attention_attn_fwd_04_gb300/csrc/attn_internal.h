@@ -217,6 +217,7 @@ struct BwdArgs {
   DeviceStatus* status;
   double wait_budget_ms;
   int force_partial;
+  int debug_stall;  // test hook: 1 stalls the dQ kernel's MMA issuer, 2 the dK/dV kernel's
 };
 
 // Bytes of the row-statistics scratch of a backward.

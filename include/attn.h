@@ -248,11 +248,20 @@ attn_status attn_get_device_status(attn_stream_t stream);
  *    call), else ATTN_ERR_INVALID_ARG;
  *  - its scratch (status word and block mask) lives in one fixed array of
  *    ATTN_NOALLOC_SCRATCH_BYTES bytes in the library, which every GPU that
- *    loads the library holds until the process exits.  A problem whose
- *    block mask needs more (about 4 * nP * nK bytes per mask batch, with
- *    nK = ceil(S_k / 128) and nP = ceil(S_q / 256); e.g. S_q = S_k = 131072
- *    needs 2 MiB) is rejected with ATTN_ERR_UNSUPPORTED before anything is
- *    enqueued;
+ *    loads the library holds until the process exits.  The first
+ *    ATTN_NOALLOC_STATUS_BYTES hold the status word, the rest the block
+ *    mask.  A problem is served when attn_block_mask_bytes() for the same
+ *    arguments, asked under the same options, is at most
+ *    ATTN_NOALLOC_SCRATCH_BYTES - ATTN_NOALLOC_STATUS_BYTES; anything
+ *    larger is rejected with ATTN_ERR_UNSUPPORTED before anything is
+ *    enqueued.  For orientation: the tile lists take 4 * nP * nK bytes per
+ *    mask batch (nK = ceil(S_k / 128), nP = ceil(S_q / 256), or
+ *    ceil(S_q / 512) under the CTA-pair option), and document masks add
+ *    8 * S_k + 8 * nK + 4 * ceil(S_k / 1024) bytes per batch entry; a mask
+ *    batch is the whole batch for document, prefix-LM and per-batch block
+ *    maps, else one.  So causal S_q = S_k = 131072 needs 2 MiB, and
+ *    documents over B = 3 sequences of 131072 tokens need about 9 MiB and
+ *    are rejected;
  *  - the first call on a device looks up the array's device address
  *    (cudaGetSymbolAddress, which may load the library's device code);
  *    make that first call before any stream capture begins;
@@ -261,15 +270,29 @@ attn_status attn_get_device_status(attn_stream_t stream);
  *    before its forward kernel runs), so calls whose work overlaps on the
  *    GPU -- on different streams, or from different threads without
  *    ordering -- race and may produce wrong results;
- *  - device-side failures (a pipeline wait that ran out of time) are
- *    recorded in that array's status word, which attn_get_device_status
- *    does not read; the outputs of such a call are unspecified.
+ *  - device-side failures (a pipeline wait that ran out of time, a failed
+ *    device check) are recorded in that array's status word, which
+ *    attn_get_noalloc_status reads and clears (attn_get_device_status reads
+ *    attn_fwd's word, not this one); the outputs of such a call are
+ *    unspecified.  Each call clears the word before its kernels run, so it
+ *    reports on the latest attn_fwd_noalloc call on the device.
  */
 #define ATTN_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+#define ATTN_NOALLOC_STATUS_BYTES 256u
 attn_status attn_fwd_noalloc(const void *q, const void *k, const void *v,
                              void *out, float *lse, int B, int H, int H_kv,
                              int S_q, int S_k, int D, float scale,
                              const attn_mod_desc *mod, attn_stream_t stream);
+
+/*
+ * attn_get_noalloc_status -- synchronise `stream`, then return and clear the
+ * status word of attn_fwd_noalloc's fixed array on the current device
+ * (ATTN_OK when the latest attn_fwd_noalloc call recorded nothing).  Like
+ * that entry point it has no counterpart on the pages and allocates no
+ * device memory: it copies the word out of the array and, when it is set,
+ * zeroes it, both synchronously.  Not for use while `stream` is captured.
+ */
+attn_status attn_get_noalloc_status(attn_stream_t stream);
 
 /*
  * attn_fwd_host -- attn_fwd on tensors in host memory.  The pages define
@@ -360,11 +383,13 @@ typedef enum attn_option {
      * "FlashAttention-4 explained", "Forward pass fixes",
      * "Software-emulated exponentials". */
     ATTN_OPT_EXP_POLY_FRACTION = 5,
-    /* Test hook, default 0.  1: the forward kernel's MMA issuers wait on a
-     * barrier that nothing ever arrives on, so their bounded wait runs out
-     * after ATTN_OPT_WAIT_BUDGET_MS: the kernel records ATTN_ERR_TIMEOUT,
+    /* Test hook, default 0.  Nonzero: the forward kernel's MMA issuers wait
+     * on a barrier that nothing ever arrives on, so their bounded wait runs
+     * out after ATTN_OPT_WAIT_BUDGET_MS: the kernel records ATTN_ERR_TIMEOUT,
      * lets its in-flight copies land, frees Tensor Memory and returns, with
-     * unspecified outputs.  Lets tests exercise the timeout path without any
+     * unspecified outputs.  In attn_bwd, 1 does the same to the dQ kernel's
+     * MMA issuer and 2 to the dK/dV kernel's.  Values other than 0, 1 and
+     * 2 are rejected.  Lets tests exercise the timeout paths without any
      * real fault or hang. */
     ATTN_OPT_DEBUG_STALL = 6,
     /* 1: forwards with D = 128 run on CTA pairs (thread-block clusters of

@@ -215,7 +215,9 @@ def test_options_round_trip(attn):
     with pytest.raises(attn.AttnError):
         attn.set_option("force_partial", 0.5)
     with pytest.raises(attn.AttnError):
-        attn.set_option("debug_stall", 2)
+        attn.set_option("debug_stall", 3)
+    with pytest.raises(attn.AttnError):
+        attn.set_option("debug_stall", 0.5)
     assert attn.get_option("debug_stall") == 0
 
 

@@ -168,3 +168,32 @@ def test_backward_rel_bias_and_block_map(attn, case):
         Bb = B if mods["blocks"] == "batched" else 1
         mods["blocks"] = (torch.rand((Bb, nb, nb), generator=g) < 0.6).to(torch.uint8)
     run_case(attn, B, H, Hkv, S, D, mods, seed=700 + case)
+
+
+@pytest.mark.parametrize("kernel", [1, 2])
+def test_backward_wait_timeout_is_reported_and_context_survives(attn, kernel):
+    # The test hook makes the MMA issuer of one backward kernel (1: dQ,
+    # 2: dK/dV) wait on a barrier nothing arrives on: with a 20 ms budget the
+    # wait runs out, the kernel records ATTN_ERR_TIMEOUT and returns (its
+    # loaders let their copies land, Tensor Memory is freed; no trap, no
+    # hang), and the next backward on the same context gives the same
+    # gradients, bit for bit, as the one before the stall.
+    B, H, S, D = 1, 2, 600, 128
+    q, k, v, do = (t.to(DEV) for t in inputs(B, H, H, S, S, D, seed=90 + kernel))
+    o, lse = attn.attn_fwd(q, k, v, causal=True)
+    ref = attn.attn_bwd(q, k, v, o, lse, do, causal=True)
+    assert attn.get_device_status(device=DEV) == 0
+    old_budget = attn.get_option("wait_budget_ms")
+    try:
+        attn.set_option("wait_budget_ms", 20)
+        attn.set_option("debug_stall", kernel)
+        attn.attn_bwd(q, k, v, o, lse, do, causal=True)
+        assert attn.get_device_status(device=DEV) == 4  # ATTN_ERR_TIMEOUT
+    finally:
+        attn.set_option("debug_stall", 0)
+        attn.set_option("wait_budget_ms", old_budget)
+    assert attn.get_device_status(device=DEV) == 0
+    got = attn.attn_bwd(q, k, v, o, lse, do, causal=True)
+    assert attn.get_device_status(device=DEV) == 0
+    for g, r in zip(got, ref):
+        assert torch.equal(g, r)
