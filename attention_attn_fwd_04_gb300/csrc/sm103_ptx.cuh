@@ -435,20 +435,21 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // 2^x on the FMA/ALU pipes instead of the hardware exp2 unit: n = round(x)
 // by adding 1.5 * 2^23 (the sum's low mantissa bits hold n), f = x - n in
 // [-1/2, 1/2], 2^f from the fitted degree-3 polynomial of exp2_poly.h, and
-// 2^n applied by adding n to the exponent field.  x is clamped to >= -126 so
-// the exponent add never wraps: 2^-126 and below come out as at most
-// 2^-126 (masked entries, whose x is -inf, give that tiny value, not 0).
-// Relative error: the polynomial's (ATTN_EXP2_POLY_MAX_REL_ERR) plus float32
-// rounding.
+// 2^n applied by adding n to the exponent field.  The reduction works on x
+// clamped to >= -126, so the exponent add never wraps; inputs below -126
+// (masked entries, whose x is -inf, among them) then give exactly 0, so a
+// hidden key adds nothing to the row sum or to P V.  Relative error: the
+// polynomial's (ATTN_EXP2_POLY_MAX_REL_ERR) plus float32 rounding.
 __device__ __forceinline__ float exp2_poly(float x) {
-  x = fmaxf(x, -126.0f);
+  const float xc = fmaxf(x, -126.0f);
   const float magic = 12582912.0f;  // 1.5 * 2^23
-  const float y = __fadd_rn(x, magic);
-  const float f = __fsub_rn(x, __fsub_rn(y, magic));
+  const float y = __fadd_rn(xc, magic);
+  const float f = __fsub_rn(xc, __fsub_rn(y, magic));
   float r = fmaf(ATTN_EXP2_POLY_C3, f, ATTN_EXP2_POLY_C2);
   r = fmaf(r, f, ATTN_EXP2_POLY_C1);
   r = fmaf(r, f, ATTN_EXP2_POLY_C0);
-  return __int_as_float(__float_as_int(r) + (__float_as_int(y) << 23));
+  const float e = __int_as_float(__float_as_int(r) + (__float_as_int(y) << 23));
+  return x >= -126.0f ? e : 0.0f;
 }
 
 // Paired fp32 arithmetic (sm_100 family): two lanes of work per instruction.

@@ -36,7 +36,8 @@ def fma32(a, b, c):
 def kernel_exp2(x):
     """float32 emulation of ptx::exp2_poly."""
     c = [np.float32(v) for v in coeffs()[0]]
-    x = np.maximum(f32(x), np.float32(-126.0))
+    x_in = f32(x)
+    x = np.maximum(x_in, np.float32(-126.0))
     magic = np.float32(12582912.0)
     y = f32(x.astype(np.float64) + magic)
     f = f32(x.astype(np.float64) - f32(y.astype(np.float64) - magic))
@@ -44,7 +45,8 @@ def kernel_exp2(x):
     r = fma32(r, f, np.full_like(f, c[1]))
     r = fma32(r, f, np.full_like(f, c[0]))
     bits = r.view(np.int32).astype(np.int64) + (y.view(np.int32).astype(np.int64) << 23)
-    return (bits & 0xFFFFFFFF).astype(np.uint32).view(np.float32)
+    e = (bits & 0xFFFFFFFF).astype(np.uint32).view(np.float32)
+    return np.where(x_in >= np.float32(-126.0), e, np.float32(0.0)).astype(np.float32)
 
 
 def test_coefficients_reproduce_from_the_fit():
@@ -75,8 +77,10 @@ def test_full_range_with_float32_reduction():
     assert rel.max() <= 2e-4, rel.max()
 
 
-def test_very_negative_and_masked_inputs_stay_tiny_and_finite():
-    x = np.array([-126.0, -126.7, -127.0, -300.0, -1e30, -np.inf], dtype=np.float32)
-    y = kernel_exp2(x)
-    assert np.all(np.isfinite(y)) and np.all(y >= 0)
-    assert np.all(y <= 2.0 ** -125)
+def test_masked_and_very_negative_inputs_give_exactly_zero():
+    # a hidden key (x = -inf) must add nothing to the row sum or to P V
+    x = np.array([-126.7, -127.0, -300.0, -1e30, -np.inf], dtype=np.float32)
+    assert np.all(kernel_exp2(x) == 0.0)
+    # the smallest input still reduced: 2^-126, the smallest normal float32
+    y = kernel_exp2(np.array([-126.0], dtype=np.float32))[0]
+    assert abs(float(y) / 2.0 ** -126 - 1.0) <= 2e-4
