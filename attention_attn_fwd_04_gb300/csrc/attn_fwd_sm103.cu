@@ -50,8 +50,14 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <float.h>
+#include <math.h>
+
+#include <type_traits>
+
 #include "attn_internal.h"
 #include "sm103_ptx.cuh"
+#include "tanh_poly.h"
 
 namespace attn {
 
@@ -151,6 +157,12 @@ struct KParams {
   uint64_t budget_ns;
   int poly_chunks;  // 16-column chunks per row (of 8) whose exp2 uses the polynomial
   int debug_stall;  // test hook (see ATTN_OPT_DEBUG_STALL)
+  // soft cap on the FMA pipes: t = v Q(v^2) with Q's coefficients tq (the
+  // fit of tanh_poly.h scaled by cap log2(e) and powers of u / v) while
+  // |v| <= tlim; else y = v ty and the exp2 / reciprocal formula
+  float tq[4];
+  float tlim;
+  float ty;
 };
 
 struct Ctl {
@@ -626,19 +638,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           ok = wait_all(bar(B_NEVER), 0, kSiteMmaDebugStall);
           if (!ok) break;
         }
+        // Key tiles EMPTY for this query tile (the entry lists the union of
+        // both tiles' key tiles) get no S and no PV here, and the softmax
+        // skips them: the waits on the K/V stages, the turn and the stage
+        // releases stay exactly as for a computed tile, so the hand-over
+        // order of the two issuers and the loader does not change.  A CTA
+        // pair's MMAs span both CTAs' tiles and compute every listed tile.
+        const uint32_t* lst = p.list + (size_t)it.e * p.nK;
+        const int tc = ci(it, t);
+        auto live = [&](int j) { return PAIR || entry_cls(lst[j], tc) != kEmpty; };
+        bool live_j = live(0);
+        bool any_pv = false;  // a PV of this item has written O
         ok = wait_all(bar(B_QF + t), act & 1, kSiteMmaQFull) &&
              wait_all(kv_full(k0), kv_par(k0), kSiteMmaKvFull) && take_turn();
         if (!ok) break;
         ptx::tc_fence_after();
-        issue_s<D, PAIR>(tS, q_desc, k_desc(k0));
+        if (live_j) issue_s<D, PAIR>(tS, q_desc, k_desc(k0));
         pass_turn();
-        commit(bar(B_SF + t));
+        if (live_j) commit(bar(B_SF + t));
         if (n == 1) commit(bar(B_QE + t));
         commit(kv_empty(k0));
         for (int j = 0; j < n && ok; ++j) {
           const uint32_t vi = k0 + 2 * j + 1;  // V_j
           const uint32_t ki = k0 + 2 * j + 2;  // K_{j+1}
           const bool has_next = j + 1 < n;
+          const bool live_next = has_next && live(j + 1);
           // Each mbarrier check costs a few hundred cycles even when the phase
           // has long completed, so the checks that are normally satisfied
           // early (K/V landed, O free) come first and P -- normally the last
@@ -646,22 +670,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           ok = wait_all(kv_full(vi), kv_par(vi), kSiteMmaKvFull);
           if (ok && has_next) ok = wait_all(kv_full(ki), kv_par(ki), kSiteMmaKvFull);
           if (ok && j == 0 && act > 0) ok = wait_all(bar(B_OE + t), (act - 1) & 1, kSiteMmaOEmpty);
-          if (ok) ok = wait_all(bar(B_PF + t), p_cnt & 1, kSiteMmaPFull);
+          if (ok && live_j) ok = wait_all(bar(B_PF + t), p_cnt & 1, kSiteMmaPFull);
           if (ok) ok = take_turn();
           if (!ok) break;
-          ++p_cnt;
           ptx::tc_fence_after();
-          issue_pv<D, PAIR>(tO, tS, v_desc(vi), j > 0);
-          if (has_next) issue_s<D, PAIR>(tS, q_desc, k_desc(ki));
+          if (live_j) {
+            ++p_cnt;
+            issue_pv<D, PAIR>(tO, tS, v_desc(vi), any_pv);
+            any_pv = true;
+          }
+          if (live_next) issue_s<D, PAIR>(tS, q_desc, k_desc(ki));
           pass_turn();
           commit(kv_empty(vi));
           if (has_next) {
-            commit(bar(B_SF + t));
+            if (live_next) commit(bar(B_SF + t));
             if (j + 2 == n) commit(bar(B_QE + t));
             commit(kv_empty(ki));
           } else {
             commit(bar(B_OF + t));
           }
+          live_j = live_next;
         }
         kv_cnt = k0 + 2 * (uint32_t)n;
         ++act;
@@ -758,11 +786,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const float* relrow =
           p.rel_bias ? p.rel_bias + (size_t)it.h * (2 * (size_t)p.rel_max + 1) : nullptr;
       const float rel_scale = SOFTCAP ? 2.0f * kLog2e / p.softcap : kLog2e;
-      // Score transform coefficients.
+      // Score transform coefficients (t: the exponent, log2 units).
       //   plain:   t = s * scale * log2(e)             (folded into the exp)
       //   ALiBi:   t = s * scale * log2(e) + slope2 * (j - qpos)
       //   softcap: y = (s * scale + bias) * 2 log2(e) / cap,
-      //            t = cap log2(e) * (1 - 2 / (2^y + 1))
+      //            t = cap log2(e) tanh(y / (2 log2(e)))
+      //              = cap log2(e) * (1 - 2 / (2^y + 1))
+      //            (the pre-cap value v is s itself without biases)
       const float sc = SOFTCAP ? p.scale * (2.0f * kLog2e / p.softcap) : p.scale_log2;
       const float capl2 = p.softcap * kLog2e;
 
@@ -774,6 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const int kt = (int)entry_tile(entry);
         const uint32_t cls = entry_cls(entry, tc);
         const int j0 = kt * kTileN;
+        if (!PAIR && cls == kEmpty) continue;  // no S, no P: skipped by the issuer too
         bool got = wait_bar<PAIR>(bar(B_SF + t), s_cnt & 1, ctl, kSiteSmxSFull);
         ok = __all_sync(0xffffffffu, got);
         if (!ok) break;
@@ -788,7 +819,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           ptx::named_bar_sync(1 + t, 128);
         }
 
-        if (cls == kEmpty) {
+        if (cls == kEmpty) {  // CTA pair: the peer's rows need this tile
           uint32_t z[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) z[c] = 0u;
@@ -839,33 +870,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 }
               }
             }
-          }
-          if constexpr (ALIBI || SOFTCAP) {
-            // paired fp32 instructions, two columns at a time
-            const float b0 = ALIBI ? fmaf(slope2, (float)(j0 - qpos), rel_const) : 0.f;
+            // additive position biases, paired fp32 instructions: the
+            // exponent's log2 units, or with the soft cap the units of
+            // y = 2 log2(e) x / cap, the cap itself following below
+            const float b0 = fmaf(slope2, (float)(j0 - qpos), rel_const);
             const uint64_t sc2 = ptx::f2(sc, sc), sl2 = ptx::f2(slope2, slope2),
-                           b02 = ptx::f2(b0, b0), one2 = ptx::f2(1.0f, 1.0f),
-                           m2c2 = ptx::f2(-2.0f * capl2, -2.0f * capl2),
-                           c2 = ptx::f2(capl2, capl2);
+                           b02 = ptx::f2(b0, b0);
 #pragma unroll
             for (int c = 0; c < kTileN; c += 2) {
-              const uint64_t bias2 =
-                  ALIBI ? ptx::ffma2(sl2, ptx::f2((float)c, (float)(c + 1)), b02) : 0ull;
-              uint64_t x2 = ptx::ffma2(ptx::f2(tv[c], tv[c + 1]), sc2, bias2);
-              if constexpr (SOFTCAP) {
-                float ea, eb;
-                ptx::f2_split(x2, ea, eb);
-                ea = ptx::ex2_approx(ea);
-                eb = ptx::ex2_approx(eb);
-                float da, db;
-                ptx::f2_split(ptx::fadd2(ptx::f2(ea, eb), one2), da, db);
-                x2 = ptx::ffma2(m2c2, ptx::f2(ptx::rcp_approx(da), ptx::rcp_approx(db)), c2);
-              }
-              ptx::f2_split(x2, tv[c], tv[c + 1]);
+              const uint64_t bias2 = ptx::ffma2(sl2, ptx::f2((float)c, (float)(c + 1)), b02);
+              ptx::f2_split(ptx::ffma2(ptx::f2(tv[c], tv[c + 1]), sc2, bias2), tv[c], tv[c + 1]);
             }
           }
-          // mask (partial tiles only)
-          if (cls == kPartial) {
+          // mask (partial tiles only), as an interval per row or by doc ids
+          auto apply_mask = [&]() {
             const int clo = lo - j0, chi = hi - j0;
             if (has_doc) {
 #pragma unroll
@@ -880,52 +898,213 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 tv[c] = vis ? tv[c] : -INFINITY;
               }
             }
-          }
+          };
           // row max: eight independent chains (measured faster on GB300 than
           // the three-input max)
-          float mxa[8];
+          auto row_max = [&]() {
+            float mxa[8];
 #pragma unroll
-          for (int a = 0; a < 8; ++a) mxa[a] = tv[a];
+            for (int a = 0; a < 8; ++a) mxa[a] = tv[a];
 #pragma unroll
-          for (int c = 8; c < kTileN; c += 16) {
+            for (int c = 8; c < kTileN; c += 16) {
 #pragma unroll
-            for (int a = 0; a < 8; ++a) mxa[a] = fmaxf(fmaxf(mxa[a], tv[c + a]), tv[c + 8 + a]);
-          }
-          float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
-                           fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
-          constexpr bool kPlain = !ALIBI && !SOFTCAP;
+              for (int a = 0; a < 8; ++a) mxa[a] = fmaxf(fmaxf(mxa[a], tv[c + a]), tv[c + 8 + a]);
+            }
+            return fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
+                         fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
+          };
+          auto row_min = [&]() {
+            float mna[8];
+#pragma unroll
+            for (int a = 0; a < 8; ++a) mna[a] = tv[a];
+#pragma unroll
+            for (int c = 8; c < kTileN; c += 16) {
+#pragma unroll
+              for (int a = 0; a < 8; ++a) mna[a] = fminf(fminf(mna[a], tv[c + a]), tv[c + 8 + a]);
+            }
+            return fminf(fminf(fminf(mna[0], mna[1]), fminf(mna[2], mna[3])),
+                         fminf(fminf(mna[4], mna[5]), fminf(mna[6], mna[7])));
+          };
+          // conditional rescale: the row's reference max moves only when the
+          // tile's max exceeds it by more than tau; returns the max to
+          // subtract in the exponent
+          auto update_max = [&](float mx) -> float {
+            const float m_new = fmaxf(m_ref, mx);
+            const bool need = m_new > m_ref + tau;
+            const bool had = m_ref != -INFINITY;
+            float factor = 1.0f;
+            if (need) {
+              factor = ptx::ex2_approx(m_ref - m_new);
+              l *= factor;
+              m_ref = m_new;
+            }
+            const bool resc = need && had;
+            if (__any_sync(0xffffffffu, resc)) {
+              const float f = resc ? factor : 1.0f;
+#pragma unroll
+              for (int c4 = 0; c4 < D / 32; ++c4) {
+                uint32_t o[32];
+                ptx::tmem_ld32(tO + (uint32_t)(c4 * 32), o);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
+                ptx::tmem_st32(tO + (uint32_t)(c4 * 32), o);
+              }
+            }
+            return (m_ref == -INFINITY) ? 0.f : m_ref;
+          };
+          float la[4] = {0.f, 0.f, 0.f, 0.f};
+          if constexpr (SOFTCAP) {
+            // Soft cap t = cap log2(e) tanh(u) of the pre-cap value v (the raw
+            // score, or y with position biases; u = kk v).  tanh is monotone,
+            // so the row max is taken on v and capped once.  Where every
+            // visible v of the warp's rows lies within |u| <= U0 -- always,
+            // for scores of ordinary size -- tanh comes from the odd
+            // polynomial of tanh_poly.h on the FMA pipes (pre-scaled:
+            // t = v Q(v^2)); other tiles take t = C (1 - 2 / (2^y + 1)) on the
+            // exp2 and reciprocal units ("FlashAttention-4 explained",
+            // "Forward pass fixes": moving transcendental work off the MUFU
+            // unit, whose reciprocal runs at half the exp2 rate on GB300).
+            // On a PARTIAL tile the hidden v become NaN, which the min / max
+            // instructions skip, so the range and the max cover the visible
+            // scores only; their exponent argument is NaN too and becomes -inf
+            // through fmaxf(NaN, -inf) = -inf, so their exponential is exactly
+            // 0.  The two tile classes run separate straight-line copies of
+            // this body.
+            auto softcap_tile = [&](auto partial_tag) {
+              constexpr bool kPart = decltype(partial_tag)::value;
+              if constexpr (kPart) {
+                const int clo = lo - j0, chi = hi - j0;
+                const float qnan = __int_as_float(0x7fc00000);
+                if (has_doc) {
+#pragma unroll
+                  for (int c = 0; c < kTileN; ++c) {
+                    const bool vis = (c >= clo) & (c <= chi) & (sdoc[c] == doc_i);
+                    tv[c] = vis ? tv[c] : qnan;
+                  }
+                } else {
+#pragma unroll
+                  for (int c = 0; c < kTileN; ++c) {
+                    const bool vis = (c >= clo) & (c <= chi);
+                    tv[c] = vis ? tv[c] : qnan;
+                  }
+                }
+              }
+              // row max and min, three-input instructions over four chains
+              float vmax, vmin;
+              {
+                float mxa[4], mna[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                  mxa[a] = ptx::fmax3(tv[2 * a], tv[2 * a + 1], tv[8 + 2 * a]);
+                  mna[a] = ptx::fmin3(tv[2 * a], tv[2 * a + 1], tv[8 + 2 * a]);
+                }
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {  // columns 9, 11, 13, 15
+                  mxa[a] = fmaxf(mxa[a], tv[9 + 2 * a]);
+                  mna[a] = fminf(mna[a], tv[9 + 2 * a]);
+                }
+#pragma unroll
+                for (int c = 16; c < kTileN; c += 8) {
+#pragma unroll
+                  for (int a = 0; a < 4; ++a) {
+                    mxa[a] = ptx::fmax3(mxa[a], tv[c + 2 * a], tv[c + 2 * a + 1]);
+                    mna[a] = ptx::fmin3(mna[a], tv[c + 2 * a], tv[c + 2 * a + 1]);
+                  }
+                }
+                vmax = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
+                vmin = fminf(fminf(mna[0], mna[1]), fminf(mna[2], mna[3]));
+              }
+              // NaN comparisons are false: a row with no visible score in
+              // the tile (vmax NaN or -inf) counts as in range
+              const bool poly = __all_sync(0xffffffffu, !(vmax > p.tlim) && !(vmin < -p.tlim));
+              float mx;
+              if (!(vmax > -INFINITY)) {
+                mx = -INFINITY;
+              } else if (poly) {
+                const float w = vmax * vmax;
+                float q = fmaf(p.tq[3], w, p.tq[2]);
+                q = fmaf(q, w, p.tq[1]);
+                q = fmaf(q, w, p.tq[0]);
+                mx = vmax * q;
+              } else {
+                const float e = ptx::ex2_approx(vmax * p.ty);
+                mx = fmaf(ptx::rcp_approx(e + 1.0f), -2.0f * capl2, capl2);
+              }
+              const float m_use = update_max(mx);
+              uint64_t acc2[2] = {0ull, 0ull};
+              // the exponent argument of a hidden score (NaN) becomes -inf
+              auto hide = [](float a) { return kPart ? fmaxf(a, -INFINITY) : a; };
+              if (poly) {
+                const uint64_t q3 = ptx::f2(p.tq[3], p.tq[3]), q2 = ptx::f2(p.tq[2], p.tq[2]),
+                               q1 = ptx::f2(p.tq[1], p.tq[1]), q0 = ptx::f2(p.tq[0], p.tq[0]),
+                               nm2 = ptx::f2(-m_use, -m_use);
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                  uint32_t pk[32];
+#pragma unroll
+                  for (int c = 0; c < 32; ++c) {
+                    const uint64_t v2 = ptx::f2(tv[h2 * 64 + 2 * c], tv[h2 * 64 + 2 * c + 1]);
+                    const uint64_t w2 = ptx::fmul2(v2, v2);
+                    uint64_t r2 = ptx::ffma2(w2, q3, q2);
+                    r2 = ptx::ffma2(r2, w2, q1);
+                    r2 = ptx::ffma2(r2, w2, q0);
+                    float pa, pb;
+                    ptx::f2_split(ptx::ffma2(v2, r2, nm2), pa, pb);
+                    pa = ptx::ex2_approx(hide(pa));
+                    pb = ptx::ex2_approx(hide(pb));
+                    acc2[c & 1] = ptx::fadd2(acc2[c & 1], ptx::f2(pa, pb));
+                    pk[c] = ptx::pack_bf16x2(pa, pb);
+                  }
+                  ptx::tmem_st32(tS + (uint32_t)(h2 * 32), pk);
+                }
+              } else {
+                const uint64_t ty2 = ptx::f2(p.ty, p.ty), one2 = ptx::f2(1.0f, 1.0f),
+                               m2c2 = ptx::f2(-2.0f * capl2, -2.0f * capl2),
+                               cm2 = ptx::f2(capl2 - m_use, capl2 - m_use);
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                  uint32_t pk[32];
+#pragma unroll
+                  for (int c = 0; c < 32; ++c) {
+                    const uint64_t v2 = ptx::f2(tv[h2 * 64 + 2 * c], tv[h2 * 64 + 2 * c + 1]);
+                    float ea, eb;
+                    ptx::f2_split(ptx::fmul2(v2, ty2), ea, eb);
+                    ea = ptx::ex2_approx(ea);
+                    eb = ptx::ex2_approx(eb);
+                    float da, db;
+                    ptx::f2_split(ptx::fadd2(ptx::f2(ea, eb), one2), da, db);
+                    float pa, pb;
+                    ptx::f2_split(ptx::ffma2(ptx::f2(ptx::rcp_approx(da), ptx::rcp_approx(db)), m2c2,
+                                             cm2),
+                                  pa, pb);
+                    pa = ptx::ex2_approx(hide(pa));
+                    pb = ptx::ex2_approx(hide(pb));
+                    acc2[c & 1] = ptx::fadd2(acc2[c & 1], ptx::f2(pa, pb));
+                    pk[c] = ptx::pack_bf16x2(pa, pb);
+                  }
+                  ptx::tmem_st32(tS + (uint32_t)(h2 * 32), pk);
+                }
+              }
+              ptx::f2_split(acc2[0], la[0], la[1]);
+              ptx::f2_split(acc2[1], la[2], la[3]);
+            };
+            if (cls == kPartial)
+              softcap_tile(std::true_type{});
+            else
+              softcap_tile(std::false_type{});
+          } else {
+          if (cls == kPartial) apply_mask();
+          float mx = row_max();
+          constexpr bool kPlain = !ALIBI;
           const float xs = kPlain ? p.scale_log2 : 1.0f;  // raw scores still need the scale
           mx = kPlain ? mx * xs : mx;
-          // conditional rescale
-          const float m_new = fmaxf(m_ref, mx);
-          const bool need = m_new > m_ref + tau;
-          const bool had = m_ref != -INFINITY;
-          float factor = 1.0f;
-          if (need) {
-            factor = ptx::ex2_approx(m_ref - m_new);
-            l *= factor;
-            m_ref = m_new;
-          }
-          const bool resc = need && had;
-          if (__any_sync(0xffffffffu, resc)) {
-            const float f = resc ? factor : 1.0f;
-#pragma unroll
-            for (int c4 = 0; c4 < D / 32; ++c4) {
-              uint32_t o[32];
-              ptx::tmem_ld32(tO + (uint32_t)(c4 * 32), o);
-              ptx::tmem_wait_ld();
-#pragma unroll
-              for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
-              ptx::tmem_st32(tO + (uint32_t)(c4 * 32), o);
-            }
-          }
-          const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+          const float m_use = update_max(mx);
           // exponentials, row sum, bf16 P written over S.  The first
           // poly_chunks 16-column chunks of the row evaluate exp2 with the
           // FMA polynomial, the rest with the hardware unit ("FlashAttention-4
           // explained", "Forward pass fixes", "Software-emulated
           // exponentials"); the choice is uniform across the warp.
-          float la[4] = {0.f, 0.f, 0.f, 0.f};
           const int npc = p.poly_chunks;
           if (npc == 0) {
             // hardware exp2 only: one straight-line loop (the chunked form
@@ -981,6 +1160,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             ptx::tmem_st32(tS + (uint32_t)(h2 * 32), pk);
           }
           }
+          }
           ptx::tmem_wait_st();
           ptx::tc_fence_before();
           __syncwarp();
@@ -998,7 +1178,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       }
       ptx::tc_fence_after();
       // A row that never saw a visible key keeps m_ref = -inf: O = 0 and
-      // LSE = -inf (l itself may hold the polynomial's tiny values).
+      // LSE = -inf.
       const bool seen = m_ref != -INFINITY && l > 0.f;
       const float inv_l = seen ? 1.0f / l : 0.f;
       {
@@ -1013,6 +1193,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (lane == 0) arrive(B_OE + t);
         const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
         if (valid) {
+          // a tile whose every key tile was EMPTY had no PV: its O columns
+          // still hold the previous item's accumulator, so write zeros
+          if (!seen) {
+#pragma unroll
+            for (int c4 = 0; c4 < D / 32; ++c4)
+#pragma unroll
+              for (int c = 0; c < 32; ++c) o[c4][c] = 0u;
+          }
 #pragma unroll
           for (int c4 = 0; c4 < D / 32; ++c4) {
             uint32_t pk[16];
@@ -1222,6 +1410,27 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
   kp.tau = a.rescale_threshold;
   kp.budget_ns = (uint64_t)(a.wait_budget_ms * 1.0e6);
   kp.debug_stall = a.debug_stall;
+  if (kp.softcap > 0.f) {
+    // u = kk v: the raw score (kk = scale / cap), or y with position biases
+    // (the bias variant's pre-cap value, kk = 1 / (2 log2 e))
+    const bool biased = (a.score_flags & (ATTN_SCORE_ALIBI | ATTN_SCORE_RELBIAS)) != 0;
+    const double l2e = 1.4426950408889634;
+    const double kk = biased ? 1.0 / (2.0 * l2e) : (double)a.scale / (double)kp.softcap;
+    const double C = (double)kp.softcap * l2e;
+    const double r[4] = {ATTN_TANH_POLY_R0, ATTN_TANH_POLY_R1, ATTN_TANH_POLY_R2,
+                         ATTN_TANH_POLY_R3};
+    double kpow = kk;
+    bool normal = true;
+    for (int i = 0; i < 4; ++i) {
+      kp.tq[i] = (float)(C * r[i] * kpow);
+      normal = normal && fabsf(kp.tq[i]) >= FLT_MIN && isfinite(kp.tq[i]);
+      kpow *= kk * kk;
+    }
+    // the polynomial path needs normal coefficients; otherwise every tile
+    // takes the exp2 / reciprocal formula
+    kp.tlim = normal ? (float)(ATTN_TANH_POLY_U0 / kk) : -1.0f;
+    kp.ty = biased ? 1.0f : (float)(2.0 * l2e * kk);
+  }
   kp.poly_chunks = (int)lrintf(a.poly_fraction * 8.0f);
   if (kp.poly_chunks < 0) kp.poly_chunks = 0;
   if (kp.poly_chunks > 8) kp.poly_chunks = 8;
