@@ -638,31 +638,19 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           ok = wait_all(bar(B_NEVER), 0, kSiteMmaDebugStall);
           if (!ok) break;
         }
-        // Key tiles EMPTY for this query tile (the entry lists the union of
-        // both tiles' key tiles) get no S and no PV here, and the softmax
-        // skips them: the waits on the K/V stages, the turn and the stage
-        // releases stay exactly as for a computed tile, so the hand-over
-        // order of the two issuers and the loader does not change.  A CTA
-        // pair's MMAs span both CTAs' tiles and compute every listed tile.
-        const uint32_t* lst = p.list + (size_t)it.e * p.nK;
-        const int tc = ci(it, t);
-        auto live = [&](int j) { return PAIR || entry_cls(lst[j], tc) != kEmpty; };
-        bool live_j = live(0);
-        bool any_pv = false;  // a PV of this item has written O
         ok = wait_all(bar(B_QF + t), act & 1, kSiteMmaQFull) &&
              wait_all(kv_full(k0), kv_par(k0), kSiteMmaKvFull) && take_turn();
         if (!ok) break;
         ptx::tc_fence_after();
-        if (live_j) issue_s<D, PAIR>(tS, q_desc, k_desc(k0));
+        issue_s<D, PAIR>(tS, q_desc, k_desc(k0));
         pass_turn();
-        if (live_j) commit(bar(B_SF + t));
+        commit(bar(B_SF + t));
         if (n == 1) commit(bar(B_QE + t));
         commit(kv_empty(k0));
         for (int j = 0; j < n && ok; ++j) {
           const uint32_t vi = k0 + 2 * j + 1;  // V_j
           const uint32_t ki = k0 + 2 * j + 2;  // K_{j+1}
           const bool has_next = j + 1 < n;
-          const bool live_next = has_next && live(j + 1);
           // Each mbarrier check costs a few hundred cycles even when the phase
           // has long completed, so the checks that are normally satisfied
           // early (K/V landed, O free) come first and P -- normally the last
@@ -670,26 +658,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           ok = wait_all(kv_full(vi), kv_par(vi), kSiteMmaKvFull);
           if (ok && has_next) ok = wait_all(kv_full(ki), kv_par(ki), kSiteMmaKvFull);
           if (ok && j == 0 && act > 0) ok = wait_all(bar(B_OE + t), (act - 1) & 1, kSiteMmaOEmpty);
-          if (ok && live_j) ok = wait_all(bar(B_PF + t), p_cnt & 1, kSiteMmaPFull);
+          if (ok) ok = wait_all(bar(B_PF + t), p_cnt & 1, kSiteMmaPFull);
           if (ok) ok = take_turn();
           if (!ok) break;
+          ++p_cnt;
           ptx::tc_fence_after();
-          if (live_j) {
-            ++p_cnt;
-            issue_pv<D, PAIR>(tO, tS, v_desc(vi), any_pv);
-            any_pv = true;
-          }
-          if (live_next) issue_s<D, PAIR>(tS, q_desc, k_desc(ki));
+          issue_pv<D, PAIR>(tO, tS, v_desc(vi), j > 0);
+          if (has_next) issue_s<D, PAIR>(tS, q_desc, k_desc(ki));
           pass_turn();
           commit(kv_empty(vi));
           if (has_next) {
-            if (live_next) commit(bar(B_SF + t));
+            commit(bar(B_SF + t));
             if (j + 2 == n) commit(bar(B_QE + t));
             commit(kv_empty(ki));
           } else {
             commit(bar(B_OF + t));
           }
-          live_j = live_next;
         }
         kv_cnt = k0 + 2 * (uint32_t)n;
         ++act;
@@ -786,13 +770,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const float* relrow =
           p.rel_bias ? p.rel_bias + (size_t)it.h * (2 * (size_t)p.rel_max + 1) : nullptr;
       const float rel_scale = SOFTCAP ? 2.0f * kLog2e / p.softcap : kLog2e;
-      // Score transform coefficients (t: the exponent, log2 units).
+      // Score transform coefficients.
       //   plain:   t = s * scale * log2(e)             (folded into the exp)
       //   ALiBi:   t = s * scale * log2(e) + slope2 * (j - qpos)
       //   softcap: y = (s * scale + bias) * 2 log2(e) / cap,
-      //            t = cap log2(e) tanh(y / (2 log2(e)))
-      //              = cap log2(e) * (1 - 2 / (2^y + 1))
-      //            (the pre-cap value v is s itself without biases)
+      //            t = cap log2(e) * (1 - 2 / (2^y + 1))
       const float sc = SOFTCAP ? p.scale * (2.0f * kLog2e / p.softcap) : p.scale_log2;
       const float capl2 = p.softcap * kLog2e;
 
@@ -804,7 +786,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const int kt = (int)entry_tile(entry);
         const uint32_t cls = entry_cls(entry, tc);
         const int j0 = kt * kTileN;
-        if (!PAIR && cls == kEmpty) continue;  // no S, no P: skipped by the issuer too
         bool got = wait_bar<PAIR>(bar(B_SF + t), s_cnt & 1, ctl, kSiteSmxSFull);
         ok = __all_sync(0xffffffffu, got);
         if (!ok) break;
@@ -819,7 +800,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           ptx::named_bar_sync(1 + t, 128);
         }
 
-        if (cls == kEmpty) {  // CTA pair: the peer's rows need this tile
+        if (cls == kEmpty) {
           uint32_t z[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) z[c] = 0u;
@@ -847,114 +828,71 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               tv[96 + c] = __uint_as_float(r3[c]);
             }
           }
-          // score mods
-          // relative-position bias: where the whole tile lies beyond +-R of
-          // every row of the warp, the clamped bias is one table entry,
-          // folded into the constant term below; otherwise a loop of its own
-          // (a uniform branch, so the loops stay branch-free), scaled so it
-          // adds table * rel_scale to s * sc
-          float rel_const = 0.f;
-          if constexpr (ALIBI) {
-            if (relrow != nullptr) {
-              const int lo_r = j0 - qpos, hi_r = j0 + kTileN - 1 - qpos;
-              if (__all_sync(0xffffffffu, hi_r <= -p.rel_max)) {
-                rel_const = __ldg(relrow) * rel_scale;
-              } else if (__all_sync(0xffffffffu, lo_r >= p.rel_max)) {
-                rel_const = __ldg(relrow + 2 * p.rel_max) * rel_scale;
-              } else {
-                const float rs = rel_scale / sc;
+          if constexpr (SOFTCAP) {
+            // score mods
+            // relative-position bias: where the whole tile lies beyond +-R of
+            // every row of the warp, the clamped bias is one table entry,
+            // folded into the constant term below; otherwise a loop of its own
+            // (a uniform branch, so the loops stay branch-free), scaled so it
+            // adds table * rel_scale to s * sc
+            float rel_const = 0.f;
+            if constexpr (ALIBI) {
+              if (relrow != nullptr) {
+                const int lo_r = j0 - qpos, hi_r = j0 + kTileN - 1 - qpos;
+                if (__all_sync(0xffffffffu, hi_r <= -p.rel_max)) {
+                  rel_const = __ldg(relrow) * rel_scale;
+                } else if (__all_sync(0xffffffffu, lo_r >= p.rel_max)) {
+                  rel_const = __ldg(relrow + 2 * p.rel_max) * rel_scale;
+                } else {
+                  const float rs = rel_scale / sc;
 #pragma unroll
-                for (int c = 0; c < kTileN; ++c) {
-                  const int r = min(max(j0 + c - qpos, -p.rel_max), p.rel_max);
-                  tv[c] = fmaf(__ldg(relrow + r + p.rel_max), rs, tv[c]);
+                  for (int c = 0; c < kTileN; ++c) {
+                    const int r = min(max(j0 + c - qpos, -p.rel_max), p.rel_max);
+                    tv[c] = fmaf(__ldg(relrow + r + p.rel_max), rs, tv[c]);
+                  }
                 }
               }
-            }
-            // additive position biases, paired fp32 instructions: the
-            // exponent's log2 units, or with the soft cap the units of
-            // y = 2 log2(e) x / cap, the cap itself following below
-            const float b0 = fmaf(slope2, (float)(j0 - qpos), rel_const);
-            const uint64_t sc2 = ptx::f2(sc, sc), sl2 = ptx::f2(slope2, slope2),
-                           b02 = ptx::f2(b0, b0);
+              // additive position biases, paired fp32 instructions: the
+              // exponent's log2 units, or with the soft cap the units of
+              // y = 2 log2(e) x / cap, the cap itself following below
+              const float b0 = fmaf(slope2, (float)(j0 - qpos), rel_const);
+              const uint64_t sc2 = ptx::f2(sc, sc), sl2 = ptx::f2(slope2, slope2),
+                             b02 = ptx::f2(b0, b0);
 #pragma unroll
-            for (int c = 0; c < kTileN; c += 2) {
-              const uint64_t bias2 = ptx::ffma2(sl2, ptx::f2((float)c, (float)(c + 1)), b02);
-              ptx::f2_split(ptx::ffma2(ptx::f2(tv[c], tv[c + 1]), sc2, bias2), tv[c], tv[c + 1]);
-            }
-          }
-          // mask (partial tiles only), as an interval per row or by doc ids
-          auto apply_mask = [&]() {
-            const int clo = lo - j0, chi = hi - j0;
-            if (has_doc) {
-#pragma unroll
-              for (int c = 0; c < kTileN; ++c) {
-                const bool vis = (c >= clo) & (c <= chi) & (sdoc[c] == doc_i);
-                tv[c] = vis ? tv[c] : -INFINITY;
-              }
-            } else {
-#pragma unroll
-              for (int c = 0; c < kTileN; ++c) {
-                const bool vis = (c >= clo) & (c <= chi);
-                tv[c] = vis ? tv[c] : -INFINITY;
+              for (int c = 0; c < kTileN; c += 2) {
+                const uint64_t bias2 = ptx::ffma2(sl2, ptx::f2((float)c, (float)(c + 1)), b02);
+                ptx::f2_split(ptx::ffma2(ptx::f2(tv[c], tv[c + 1]), sc2, bias2), tv[c], tv[c + 1]);
               }
             }
-          };
-          // row max: eight independent chains (measured faster on GB300 than
-          // the three-input max)
-          auto row_max = [&]() {
-            float mxa[8];
-#pragma unroll
-            for (int a = 0; a < 8; ++a) mxa[a] = tv[a];
-#pragma unroll
-            for (int c = 8; c < kTileN; c += 16) {
-#pragma unroll
-              for (int a = 0; a < 8; ++a) mxa[a] = fmaxf(fmaxf(mxa[a], tv[c + a]), tv[c + 8 + a]);
-            }
-            return fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
-                         fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
-          };
-          auto row_min = [&]() {
-            float mna[8];
-#pragma unroll
-            for (int a = 0; a < 8; ++a) mna[a] = tv[a];
-#pragma unroll
-            for (int c = 8; c < kTileN; c += 16) {
-#pragma unroll
-              for (int a = 0; a < 8; ++a) mna[a] = fminf(fminf(mna[a], tv[c + a]), tv[c + 8 + a]);
-            }
-            return fminf(fminf(fminf(mna[0], mna[1]), fminf(mna[2], mna[3])),
-                         fminf(fminf(mna[4], mna[5]), fminf(mna[6], mna[7])));
-          };
-          // conditional rescale: the row's reference max moves only when the
-          // tile's max exceeds it by more than tau; returns the max to
-          // subtract in the exponent
-          auto update_max = [&](float mx) -> float {
-            const float m_new = fmaxf(m_ref, mx);
-            const bool need = m_new > m_ref + tau;
-            const bool had = m_ref != -INFINITY;
-            float factor = 1.0f;
-            if (need) {
-              factor = ptx::ex2_approx(m_ref - m_new);
-              l *= factor;
-              m_ref = m_new;
-            }
-            const bool resc = need && had;
-            if (__any_sync(0xffffffffu, resc)) {
-              const float f = resc ? factor : 1.0f;
-#pragma unroll
-              for (int c4 = 0; c4 < D / 32; ++c4) {
-                uint32_t o[32];
-                ptx::tmem_ld32(tO + (uint32_t)(c4 * 32), o);
-                ptx::tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
-                ptx::tmem_st32(tO + (uint32_t)(c4 * 32), o);
+            // conditional rescale: the row's reference max moves only when the
+            // tile's max exceeds it by more than tau; returns the max to
+            // subtract in the exponent
+            auto update_max = [&](float mx) -> float {
+              const float m_new = fmaxf(m_ref, mx);
+              const bool need = m_new > m_ref + tau;
+              const bool had = m_ref != -INFINITY;
+              float factor = 1.0f;
+              if (need) {
+                factor = ptx::ex2_approx(m_ref - m_new);
+                l *= factor;
+                m_ref = m_new;
               }
-            }
-            return (m_ref == -INFINITY) ? 0.f : m_ref;
-          };
-          float la[4] = {0.f, 0.f, 0.f, 0.f};
-          if constexpr (SOFTCAP) {
+              const bool resc = need && had;
+              if (__any_sync(0xffffffffu, resc)) {
+                const float f = resc ? factor : 1.0f;
+#pragma unroll
+                for (int c4 = 0; c4 < D / 32; ++c4) {
+                  uint32_t o[32];
+                  ptx::tmem_ld32(tO + (uint32_t)(c4 * 32), o);
+                  ptx::tmem_wait_ld();
+#pragma unroll
+                  for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
+                  ptx::tmem_st32(tO + (uint32_t)(c4 * 32), o);
+                }
+              }
+              return (m_ref == -INFINITY) ? 0.f : m_ref;
+            };
+            float la[4] = {0.f, 0.f, 0.f, 0.f};
             // Soft cap t = cap log2(e) tanh(u) of the pre-cap value v (the raw
             // score, or y with position biases; u = kk v).  tanh is monotone,
             // so the row max is taken on v and capped once.  Where every
@@ -1093,18 +1031,110 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               softcap_tile(std::true_type{});
             else
               softcap_tile(std::false_type{});
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) arrive(B_PF + t);
+            l += (la[0] + la[1]) + (la[2] + la[3]);
           } else {
-          if (cls == kPartial) apply_mask();
-          float mx = row_max();
+          // score mods
+          // relative-position bias: where the whole tile lies beyond +-R of
+          // every row of the warp, the clamped bias is one table entry,
+          // folded into the constant term below; otherwise a loop of its own
+          // (a uniform branch, so the loops stay branch-free), scaled so it
+          // adds table * rel_scale to s * sc
+          float rel_const = 0.f;
+          if constexpr (ALIBI) {
+            if (relrow != nullptr) {
+              const int lo_r = j0 - qpos, hi_r = j0 + kTileN - 1 - qpos;
+              if (__all_sync(0xffffffffu, hi_r <= -p.rel_max)) {
+                rel_const = __ldg(relrow) * rel_scale;
+              } else if (__all_sync(0xffffffffu, lo_r >= p.rel_max)) {
+                rel_const = __ldg(relrow + 2 * p.rel_max) * rel_scale;
+              } else {
+                const float rs = rel_scale / sc;
+#pragma unroll
+                for (int c = 0; c < kTileN; ++c) {
+                  const int r = min(max(j0 + c - qpos, -p.rel_max), p.rel_max);
+                  tv[c] = fmaf(__ldg(relrow + r + p.rel_max), rs, tv[c]);
+                }
+              }
+            }
+          }
+          if constexpr (ALIBI) {
+            // paired fp32 instructions, two columns at a time
+            const float b0 = fmaf(slope2, (float)(j0 - qpos), rel_const);
+            const uint64_t sc2 = ptx::f2(sc, sc), sl2 = ptx::f2(slope2, slope2),
+                           b02 = ptx::f2(b0, b0);
+#pragma unroll
+            for (int c = 0; c < kTileN; c += 2) {
+              const uint64_t bias2 = ptx::ffma2(sl2, ptx::f2((float)c, (float)(c + 1)), b02);
+              uint64_t x2 = ptx::ffma2(ptx::f2(tv[c], tv[c + 1]), sc2, bias2);
+              ptx::f2_split(x2, tv[c], tv[c + 1]);
+            }
+          }
+          // mask (partial tiles only)
+          if (cls == kPartial) {
+            const int clo = lo - j0, chi = hi - j0;
+            if (has_doc) {
+#pragma unroll
+              for (int c = 0; c < kTileN; ++c) {
+                const bool vis = (c >= clo) & (c <= chi) & (sdoc[c] == doc_i);
+                tv[c] = vis ? tv[c] : -INFINITY;
+              }
+            } else {
+#pragma unroll
+              for (int c = 0; c < kTileN; ++c) {
+                const bool vis = (c >= clo) & (c <= chi);
+                tv[c] = vis ? tv[c] : -INFINITY;
+              }
+            }
+          }
+          // row max: eight independent chains (measured faster on GB300 than
+          // the three-input max)
+          float mxa[8];
+#pragma unroll
+          for (int a = 0; a < 8; ++a) mxa[a] = tv[a];
+#pragma unroll
+          for (int c = 8; c < kTileN; c += 16) {
+#pragma unroll
+            for (int a = 0; a < 8; ++a) mxa[a] = fmaxf(fmaxf(mxa[a], tv[c + a]), tv[c + 8 + a]);
+          }
+          float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
+                           fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
           constexpr bool kPlain = !ALIBI;
           const float xs = kPlain ? p.scale_log2 : 1.0f;  // raw scores still need the scale
           mx = kPlain ? mx * xs : mx;
-          const float m_use = update_max(mx);
+          // conditional rescale
+          const float m_new = fmaxf(m_ref, mx);
+          const bool need = m_new > m_ref + tau;
+          const bool had = m_ref != -INFINITY;
+          float factor = 1.0f;
+          if (need) {
+            factor = ptx::ex2_approx(m_ref - m_new);
+            l *= factor;
+            m_ref = m_new;
+          }
+          const bool resc = need && had;
+          if (__any_sync(0xffffffffu, resc)) {
+            const float f = resc ? factor : 1.0f;
+#pragma unroll
+            for (int c4 = 0; c4 < D / 32; ++c4) {
+              uint32_t o[32];
+              ptx::tmem_ld32(tO + (uint32_t)(c4 * 32), o);
+              ptx::tmem_wait_ld();
+#pragma unroll
+              for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
+              ptx::tmem_st32(tO + (uint32_t)(c4 * 32), o);
+            }
+          }
+          const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
           // exponentials, row sum, bf16 P written over S.  The first
           // poly_chunks 16-column chunks of the row evaluate exp2 with the
           // FMA polynomial, the rest with the hardware unit ("FlashAttention-4
           // explained", "Forward pass fixes", "Software-emulated
           // exponentials"); the choice is uniform across the warp.
+          float la[4] = {0.f, 0.f, 0.f, 0.f};
           const int npc = p.poly_chunks;
           if (npc == 0) {
             // hardware exp2 only: one straight-line loop (the chunked form
@@ -1160,12 +1190,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             ptx::tmem_st32(tS + (uint32_t)(h2 * 32), pk);
           }
           }
-          }
           ptx::tmem_wait_st();
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) arrive(B_PF + t);
           l += (la[0] + la[1]) + (la[2] + la[3]);
+          }
         }
       }
       if (!ok) break;
@@ -1193,14 +1223,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (lane == 0) arrive(B_OE + t);
         const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
         if (valid) {
-          // a tile whose every key tile was EMPTY had no PV: its O columns
-          // still hold the previous item's accumulator, so write zeros
-          if (!seen) {
-#pragma unroll
-            for (int c4 = 0; c4 < D / 32; ++c4)
-#pragma unroll
-              for (int c = 0; c < 32; ++c) o[c4][c] = 0u;
-          }
 #pragma unroll
           for (int c4 = 0; c4 < D / 32; ++c4) {
             uint32_t pk[16];
