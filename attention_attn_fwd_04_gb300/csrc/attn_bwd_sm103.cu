@@ -52,8 +52,12 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <float.h>
+#include <math.h>
+
 #include "attn_internal.h"
 #include "sm103_ptx.cuh"
+#include "tanh_poly.h"
 
 namespace attn {
 
@@ -136,6 +140,10 @@ struct BParams {
   DeviceStatus* status;
   uint64_t budget_ns;
   int debug_stall;  // test hook: 1 = the dQ kernel, 2 = the dK/dV kernel
+  // soft cap on the FMA pipes, as in the forward: t = y Q(y^2) for the
+  // score y in the units 2 log2(e) x / cap while |y| <= tlim
+  float tq[4];
+  float tlim;
 };
 
 struct BCtl {
@@ -253,6 +261,50 @@ __device__ __forceinline__ float score_t(float s, float bias_pos, const ScoreMod
   }
   return x;
 }
+// The score transform of N columns in place, their bias positions
+// pos0 + step * c: as score_t, except that a soft cap whose scores all lie
+// within the polynomial's range for every lane of the warp (always, for
+// scores of ordinary size) is evaluated as t = y Q(y^2) on the FMA pipes
+// (tanh_poly.h; paired fp32 instructions) instead of from the exp2 and
+// reciprocal units, whose reciprocal runs at half the exp2 rate.
+template <bool ALIBI, bool SOFTCAP, int N>
+__device__ __forceinline__ void score_cols(float (&tv)[N], float pos0, float step,
+                                           const ScoreMod& m, const BParams& p) {
+  if constexpr (!SOFTCAP) {
+#pragma unroll
+    for (int c = 0; c < N; ++c) tv[c] = score_t<ALIBI, SOFTCAP>(tv[c], pos0 + step * (float)c, m);
+  } else {
+    float mx = -INFINITY, mn = INFINITY;
+#pragma unroll
+    for (int c = 0; c < N; ++c) {
+      float y = tv[c] * m.sc;
+      if constexpr (ALIBI) y = fmaf(m.slope2, pos0 + step * (float)c, y);
+      tv[c] = y;
+      mx = fmaxf(mx, y);
+      mn = fminf(mn, y);
+    }
+    if (__all_sync(0xffffffffu, mx <= p.tlim && mn >= -p.tlim)) {
+      const uint64_t q3 = ptx::f2(p.tq[3], p.tq[3]), q2 = ptx::f2(p.tq[2], p.tq[2]),
+                     q1 = ptx::f2(p.tq[1], p.tq[1]), q0 = ptx::f2(p.tq[0], p.tq[0]);
+#pragma unroll
+      for (int c = 0; c < N; c += 2) {
+        const uint64_t y2 = ptx::f2(tv[c], tv[c + 1]);
+        const uint64_t w2 = ptx::fmul2(y2, y2);
+        uint64_t r2 = ptx::ffma2(w2, q3, q2);
+        r2 = ptx::ffma2(r2, w2, q1);
+        r2 = ptx::ffma2(r2, w2, q0);
+        ptx::f2_split(ptx::fmul2(y2, r2), tv[c], tv[c + 1]);
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < N; ++c) {
+        const float e = ptx::ex2_approx(tv[c]);
+        tv[c] = m.capl2 * (1.0f - 2.0f * ptx::rcp_approx(e + 1.0f));
+      }
+    }
+  }
+}
+
 template <bool ALIBI, bool SOFTCAP>
 __device__ __forceinline__ ScoreMod make_mod(const BParams& p, int h) {
   ScoreMod m;
@@ -725,11 +777,7 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dq_kernel(const __grid_const
         // the plain score (a scale) is folded into the exponential below
         constexpr bool kPlain = !ALIBI && !SOFTCAP;
         add_rel_bias<ALIBI, SOFTCAP, kBCols>(tv, p, it.h, j0 - qpos, 1, md);
-        if constexpr (!kPlain) {
-#pragma unroll
-          for (int c = 0; c < kBCols; ++c)
-            tv[c] = score_t<ALIBI, SOFTCAP>(tv[c], (float)(j0 + c - qpos), md);
-        }
+        if constexpr (!kPlain) score_cols<ALIBI, SOFTCAP>(tv, (float)(j0 - qpos), 1.0f, md, p);
         if (cls == kPartial) {
           const int clo = lo - j0, chi = hi - j0;
           if (has_doc) {
@@ -1125,11 +1173,7 @@ __global__ void __launch_bounds__(kBThreads, 1) bwd_dkdv_kernel(const __grid_con
           // the plain score (a scale) is folded into the exponential below
           constexpr bool kPlain = !ALIBI && !SOFTCAP;
           add_rel_bias<ALIBI, SOFTCAP, kBCols>(tv, p, h, j - (i0 + p.q_offset), -1, md);
-          if constexpr (!kPlain) {
-#pragma unroll
-            for (int c = 0; c < kBCols; ++c)
-              tv[c] = score_t<ALIBI, SOFTCAP>(tv[c], jb - (float)c, md);
-          }
+          if constexpr (!kPlain) score_cols<ALIBI, SOFTCAP>(tv, jb, -1.0f, md, p);
           // the mask in a loop of its own (rows beyond S_k see nothing)
           if (!valid || cls == kPartial) {
             const int clo = ilo - i0, chi = ihi - i0;
@@ -1421,6 +1465,22 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
   const double ms = a.wait_budget_ms > 0 ? a.wait_budget_ms : 2000.0;
   bp.budget_ns = (uint64_t)(ms * 1e6);
   bp.debug_stall = a.debug_stall;
+  bp.tlim = -1.0f;  // no polynomial unless its coefficients are normal numbers
+  if (bp.softcap > 0.f) {
+    // the score reaches the cap as y = 2 log2(e) x / cap = 2 log2(e) u
+    const double l2e = 1.4426950408889634, kk = 1.0 / (2.0 * l2e);
+    const double C = (double)bp.softcap * l2e;
+    const double r[4] = {ATTN_TANH_POLY_R0, ATTN_TANH_POLY_R1, ATTN_TANH_POLY_R2,
+                         ATTN_TANH_POLY_R3};
+    double kpow = kk;
+    bool normal = true;
+    for (int i = 0; i < 4; ++i) {
+      bp.tq[i] = (float)(C * r[i] * kpow);
+      normal = normal && fabsf(bp.tq[i]) >= FLT_MIN && isfinite(bp.tq[i]);
+      kpow *= kk * kk;
+    }
+    if (normal) bp.tlim = (float)(ATTN_TANH_POLY_U0 / kk);
+  }
 
   // row statistics, then the two gradient kernels
   const int BH = a.B * a.H;
