@@ -142,7 +142,7 @@ struct BParams {
   int debug_stall;  // test hook: 1 = the dQ kernel, 2 = the dK/dV kernel
   // soft cap on the FMA pipes, as in the forward: t = y Q(y^2) for the
   // score y in the units 2 log2(e) x / cap while |y| <= tlim
-  float tq[4];
+  float tq[3];
   float tlim;
 };
 
@@ -284,14 +284,13 @@ __device__ __forceinline__ void score_cols(float (&tv)[N], float pos0, float ste
       mn = fminf(mn, y);
     }
     if (__all_sync(0xffffffffu, mx <= p.tlim && mn >= -p.tlim)) {
-      const uint64_t q3 = ptx::f2(p.tq[3], p.tq[3]), q2 = ptx::f2(p.tq[2], p.tq[2]),
-                     q1 = ptx::f2(p.tq[1], p.tq[1]), q0 = ptx::f2(p.tq[0], p.tq[0]);
+      const uint64_t q2 = ptx::f2(p.tq[2], p.tq[2]), q1 = ptx::f2(p.tq[1], p.tq[1]),
+                     q0 = ptx::f2(p.tq[0], p.tq[0]);
 #pragma unroll
       for (int c = 0; c < N; c += 2) {
         const uint64_t y2 = ptx::f2(tv[c], tv[c + 1]);
         const uint64_t w2 = ptx::fmul2(y2, y2);
-        uint64_t r2 = ptx::ffma2(w2, q3, q2);
-        r2 = ptx::ffma2(r2, w2, q1);
+        uint64_t r2 = ptx::ffma2(w2, q2, q1);
         r2 = ptx::ffma2(r2, w2, q0);
         ptx::f2_split(ptx::fmul2(y2, r2), tv[c], tv[c + 1]);
       }
@@ -1470,11 +1469,10 @@ cudaError_t launch_attn_bwd(const BwdArgs& a, cudaStream_t stream) {
     // the score reaches the cap as y = 2 log2(e) x / cap = 2 log2(e) u
     const double l2e = 1.4426950408889634, kk = 1.0 / (2.0 * l2e);
     const double C = (double)bp.softcap * l2e;
-    const double r[4] = {ATTN_TANH_POLY_R0, ATTN_TANH_POLY_R1, ATTN_TANH_POLY_R2,
-                         ATTN_TANH_POLY_R3};
+    const double r[3] = {ATTN_TANH_POLY_R0, ATTN_TANH_POLY_R1, ATTN_TANH_POLY_R2};
     double kpow = kk;
     bool normal = true;
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 3; ++i) {
       bp.tq[i] = (float)(C * r[i] * kpow);
       normal = normal && fabsf(bp.tq[i]) >= FLT_MIN && isfinite(bp.tq[i]);
       kpow *= kk * kk;

@@ -160,7 +160,7 @@ struct KParams {
   // soft cap on the FMA pipes: t = v Q(v^2) with Q's coefficients tq (the
   // fit of tanh_poly.h scaled by cap log2(e) and powers of u / v) while
   // |v| <= tlim; else y = v ty and the exp2 / reciprocal formula
-  float tq[4];
+  float tq[3];
   float tlim;
   float ty;
 };
@@ -903,28 +903,52 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             // exp2 and reciprocal units ("FlashAttention-4 explained",
             // "Forward pass fixes": moving transcendental work off the MUFU
             // unit, whose reciprocal runs at half the exp2 rate on GB300).
-            // On a PARTIAL tile the hidden v become NaN, which the min / max
-            // instructions skip, so the range and the max cover the visible
-            // scores only; their exponent argument is NaN too and becomes -inf
-            // through fmaxf(NaN, -inf) = -inf, so their exponential is exactly
-            // 0.  The two tile classes run separate straight-line copies of
-            // this body.
+            // On a PARTIAL tile the hidden v of a mixed chunk become NaN,
+            // which the min / max instructions skip, so the range and the max
+            // cover the visible scores only; their exponent argument is NaN
+            // too and becomes -inf through fmaxf(NaN, -inf) = -inf, so their
+            // exponential is exactly 0.  The two tile classes run separate
+            // straight-line copies of this body.
             auto softcap_tile = [&](auto partial_tag) {
               constexpr bool kPart = decltype(partial_tag)::value;
+              // On a PARTIAL tile each 32-column chunk is classified for the
+              // warp's 32 rows: hidden for every row (bit k of hid; skipped by
+              // the range, the max and the exponentials, its P stored as 0),
+              // mixed (bit k of mix; hidden scores set to NaN one by one), or
+              // visible for every row.  With a window or causal band, a
+              // warp's rows differ by at most 31 positions, so on a diagonal
+              // or window-edge tile one chunk is mixed and the others are
+              // whole.  Document ids compared key by key make every chunk
+              // that is not hidden mixed.
+              uint32_t hid = 0u, mix = 0u;
               if constexpr (kPart) {
                 const int clo = lo - j0, chi = hi - j0;
                 const float qnan = __int_as_float(0x7fc00000);
-                if (has_doc) {
 #pragma unroll
-                  for (int c = 0; c < kTileN; ++c) {
-                    const bool vis = (c >= clo) & (c <= chi) & (sdoc[c] == doc_i);
-                    tv[c] = vis ? tv[c] : qnan;
-                  }
-                } else {
+                for (int k = 0; k < 4; ++k) {
+                  const bool h = (chi < 32 * k) || (clo > 32 * k + 31);
+                  const bool v = !has_doc && clo <= 32 * k && chi >= 32 * k + 31;
+                  const bool all_h = __all_sync(0xffffffffu, h);
+                  const bool all_v = __all_sync(0xffffffffu, v);
+                  hid |= (uint32_t)all_h << k;
+                  mix |= (uint32_t)!(all_h || all_v) << k;
+                }
 #pragma unroll
-                  for (int c = 0; c < kTileN; ++c) {
-                    const bool vis = (c >= clo) & (c <= chi);
-                    tv[c] = vis ? tv[c] : qnan;
+                for (int k = 0; k < 4; ++k) {
+                  if ((mix >> k) & 1u) {
+                    if (has_doc) {
+#pragma unroll
+                      for (int c = 32 * k; c < 32 * k + 32; ++c) {
+                        const bool vis = (c >= clo) & (c <= chi) & (sdoc[c] == doc_i);
+                        tv[c] = vis ? tv[c] : qnan;
+                      }
+                    } else {
+#pragma unroll
+                      for (int c = 32 * k; c < 32 * k + 32; ++c) {
+                        const bool vis = (c >= clo) & (c <= chi);
+                        tv[c] = vis ? tv[c] : qnan;
+                      }
+                    }
                   }
                 }
               }
@@ -932,22 +956,41 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               float vmax, vmin;
               {
                 float mxa[4], mna[4];
+                if constexpr (kPart) {
+                  // chains start at NaN, which the min / max instructions skip
 #pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                  mxa[a] = ptx::fmax3(tv[2 * a], tv[2 * a + 1], tv[8 + 2 * a]);
-                  mna[a] = ptx::fmin3(tv[2 * a], tv[2 * a + 1], tv[8 + 2 * a]);
-                }
+                  for (int a = 0; a < 4; ++a) mxa[a] = mna[a] = __int_as_float(0x7fc00000);
 #pragma unroll
-                for (int a = 0; a < 4; ++a) {  // columns 9, 11, 13, 15
-                  mxa[a] = fmaxf(mxa[a], tv[9 + 2 * a]);
-                  mna[a] = fminf(mna[a], tv[9 + 2 * a]);
-                }
+                  for (int k = 0; k < 4; ++k) {
+                    if (!((hid >> k) & 1u)) {
 #pragma unroll
-                for (int c = 16; c < kTileN; c += 8) {
+                      for (int c = 32 * k; c < 32 * k + 32; c += 8) {
+#pragma unroll
+                        for (int a = 0; a < 4; ++a) {
+                          mxa[a] = ptx::fmax3(mxa[a], tv[c + 2 * a], tv[c + 2 * a + 1]);
+                          mna[a] = ptx::fmin3(mna[a], tv[c + 2 * a], tv[c + 2 * a + 1]);
+                        }
+                      }
+                    }
+                  }
+                } else {
 #pragma unroll
                   for (int a = 0; a < 4; ++a) {
-                    mxa[a] = ptx::fmax3(mxa[a], tv[c + 2 * a], tv[c + 2 * a + 1]);
-                    mna[a] = ptx::fmin3(mna[a], tv[c + 2 * a], tv[c + 2 * a + 1]);
+                    mxa[a] = ptx::fmax3(tv[2 * a], tv[2 * a + 1], tv[8 + 2 * a]);
+                    mna[a] = ptx::fmin3(tv[2 * a], tv[2 * a + 1], tv[8 + 2 * a]);
+                  }
+#pragma unroll
+                  for (int a = 0; a < 4; ++a) {  // columns 9, 11, 13, 15
+                    mxa[a] = fmaxf(mxa[a], tv[9 + 2 * a]);
+                    mna[a] = fminf(mna[a], tv[9 + 2 * a]);
+                  }
+#pragma unroll
+                  for (int c = 16; c < kTileN; c += 8) {
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) {
+                      mxa[a] = ptx::fmax3(mxa[a], tv[c + 2 * a], tv[c + 2 * a + 1]);
+                      mna[a] = ptx::fmin3(mna[a], tv[c + 2 * a], tv[c + 2 * a + 1]);
+                    }
                   }
                 }
                 vmax = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
@@ -961,8 +1004,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 mx = -INFINITY;
               } else if (poly) {
                 const float w = vmax * vmax;
-                float q = fmaf(p.tq[3], w, p.tq[2]);
-                q = fmaf(q, w, p.tq[1]);
+                float q = fmaf(p.tq[2], w, p.tq[1]);
                 q = fmaf(q, w, p.tq[0]);
                 mx = vmax * q;
               } else {
@@ -971,58 +1013,63 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               }
               const float m_use = update_max(mx);
               uint64_t acc2[2] = {0ull, 0ull};
-              // the exponent argument of a hidden score (NaN) becomes -inf
-              auto hide = [](float a) { return kPart ? fmaxf(a, -INFINITY) : a; };
-              if (poly) {
-                const uint64_t q3 = ptx::f2(p.tq[3], p.tq[3]), q2 = ptx::f2(p.tq[2], p.tq[2]),
-                               q1 = ptx::f2(p.tq[1], p.tq[1]), q0 = ptx::f2(p.tq[0], p.tq[0]),
-                               nm2 = ptx::f2(-m_use, -m_use);
+              // the exponentials of P, 32 bf16 pairs of columns per Tensor
+              // Memory store; arg(a, b, ea, eb) gives the exponent arguments
+              // of two columns.  The exponent argument of a hidden score
+              // (NaN) becomes -inf, so its exponential is exactly 0.
+              auto exp_pass = [&](auto arg) {
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
                   uint32_t pk[32];
 #pragma unroll
-                  for (int c = 0; c < 32; ++c) {
-                    const uint64_t v2 = ptx::f2(tv[h2 * 64 + 2 * c], tv[h2 * 64 + 2 * c + 1]);
-                    const uint64_t w2 = ptx::fmul2(v2, v2);
-                    uint64_t r2 = ptx::ffma2(w2, q3, q2);
-                    r2 = ptx::ffma2(r2, w2, q1);
-                    r2 = ptx::ffma2(r2, w2, q0);
-                    float pa, pb;
-                    ptx::f2_split(ptx::ffma2(v2, r2, nm2), pa, pb);
-                    pa = ptx::ex2_approx(hide(pa));
-                    pb = ptx::ex2_approx(hide(pb));
-                    acc2[c & 1] = ptx::fadd2(acc2[c & 1], ptx::f2(pa, pb));
-                    pk[c] = ptx::pack_bf16x2(pa, pb);
+                  for (int hf = 0; hf < 2; ++hf) {
+                    if (kPart && ((hid >> (2 * h2 + hf)) & 1u)) {
+#pragma unroll
+                      for (int c = 16 * hf; c < 16 * hf + 16; ++c) pk[c] = 0u;
+                    } else {
+#pragma unroll
+                      for (int c = 16 * hf; c < 16 * hf + 16; ++c) {
+                        float pa, pb;
+                        arg(tv[h2 * 64 + 2 * c], tv[h2 * 64 + 2 * c + 1], pa, pb);
+                        if constexpr (kPart) {
+                          pa = fmaxf(pa, -INFINITY);
+                          pb = fmaxf(pb, -INFINITY);
+                        }
+                        pa = ptx::ex2_approx(pa);
+                        pb = ptx::ex2_approx(pb);
+                        acc2[c & 1] = ptx::fadd2(acc2[c & 1], ptx::f2(pa, pb));
+                        pk[c] = ptx::pack_bf16x2(pa, pb);
+                      }
+                    }
                   }
                   ptx::tmem_st32(tS + (uint32_t)(h2 * 32), pk);
                 }
+              };
+              if (poly) {
+                const uint64_t q2 = ptx::f2(p.tq[2], p.tq[2]), q1 = ptx::f2(p.tq[1], p.tq[1]),
+                               q0 = ptx::f2(p.tq[0], p.tq[0]), nm2 = ptx::f2(-m_use, -m_use);
+                exp_pass([&](float a, float b, float& ea, float& eb) {
+                  const uint64_t v2 = ptx::f2(a, b);
+                  const uint64_t w2 = ptx::fmul2(v2, v2);
+                  uint64_t r2 = ptx::ffma2(w2, q2, q1);
+                  r2 = ptx::ffma2(r2, w2, q0);
+                  ptx::f2_split(ptx::ffma2(v2, r2, nm2), ea, eb);
+                });
               } else {
                 const uint64_t ty2 = ptx::f2(p.ty, p.ty), one2 = ptx::f2(1.0f, 1.0f),
                                m2c2 = ptx::f2(-2.0f * capl2, -2.0f * capl2),
                                cm2 = ptx::f2(capl2 - m_use, capl2 - m_use);
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                  uint32_t pk[32];
-#pragma unroll
-                  for (int c = 0; c < 32; ++c) {
-                    const uint64_t v2 = ptx::f2(tv[h2 * 64 + 2 * c], tv[h2 * 64 + 2 * c + 1]);
-                    float ea, eb;
-                    ptx::f2_split(ptx::fmul2(v2, ty2), ea, eb);
-                    ea = ptx::ex2_approx(ea);
-                    eb = ptx::ex2_approx(eb);
-                    float da, db;
-                    ptx::f2_split(ptx::fadd2(ptx::f2(ea, eb), one2), da, db);
-                    float pa, pb;
-                    ptx::f2_split(ptx::ffma2(ptx::f2(ptx::rcp_approx(da), ptx::rcp_approx(db)), m2c2,
-                                             cm2),
-                                  pa, pb);
-                    pa = ptx::ex2_approx(hide(pa));
-                    pb = ptx::ex2_approx(hide(pb));
-                    acc2[c & 1] = ptx::fadd2(acc2[c & 1], ptx::f2(pa, pb));
-                    pk[c] = ptx::pack_bf16x2(pa, pb);
-                  }
-                  ptx::tmem_st32(tS + (uint32_t)(h2 * 32), pk);
-                }
+                exp_pass([&](float a, float b, float& ea, float& eb) {
+                  float xa, xb;
+                  ptx::f2_split(ptx::fmul2(ptx::f2(a, b), ty2), xa, xb);
+                  xa = ptx::ex2_approx(xa);
+                  xb = ptx::ex2_approx(xb);
+                  float da, db;
+                  ptx::f2_split(ptx::fadd2(ptx::f2(xa, xb), one2), da, db);
+                  ptx::f2_split(ptx::ffma2(ptx::f2(ptx::rcp_approx(da), ptx::rcp_approx(db)), m2c2,
+                                           cm2),
+                                ea, eb);
+                });
               }
               ptx::f2_split(acc2[0], la[0], la[1]);
               ptx::f2_split(acc2[1], la[2], la[3]);
@@ -1073,21 +1120,39 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               ptx::f2_split(x2, tv[c], tv[c + 1]);
             }
           }
-          // mask (partial tiles only)
+          // mask (partial tiles only).  The position-bias variant masks by
+          // 32-column chunks: a chunk that every row of the warp sees whole
+          // is left as it is, the others are masked score by score (documents
+          // + ALiBi +3%; a third branch that set a hidden chunk to -inf as a
+          // whole made the kernel spill).  The plain variant, whose partial
+          // tiles are few (the causal diagonal), keeps one loop: the chunked
+          // form cost it 7% on dense and causal, where no tile is partial.
           if (cls == kPartial) {
             const int clo = lo - j0, chi = hi - j0;
-            if (has_doc) {
+            auto mask_cols = [&](int c0, int c1) {
+              if (has_doc) {
 #pragma unroll
-              for (int c = 0; c < kTileN; ++c) {
-                const bool vis = (c >= clo) & (c <= chi) & (sdoc[c] == doc_i);
-                tv[c] = vis ? tv[c] : -INFINITY;
+                for (int c = c0; c < c1; ++c) {
+                  const bool vis = (c >= clo) & (c <= chi) & (sdoc[c] == doc_i);
+                  tv[c] = vis ? tv[c] : -INFINITY;
+                }
+              } else {
+#pragma unroll
+                for (int c = c0; c < c1; ++c) {
+                  const bool vis = (c >= clo) & (c <= chi);
+                  tv[c] = vis ? tv[c] : -INFINITY;
+                }
+              }
+            };
+            if constexpr (ALIBI) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const bool all_v = __all_sync(0xffffffffu, !has_doc && clo <= 32 * k &&
+                                                               chi >= 32 * k + 31);
+                if (!all_v) mask_cols(32 * k, 32 * k + 32);
               }
             } else {
-#pragma unroll
-              for (int c = 0; c < kTileN; ++c) {
-                const bool vis = (c >= clo) & (c <= chi);
-                tv[c] = vis ? tv[c] : -INFINITY;
-              }
+              mask_cols(0, kTileN);
             }
           }
           // row max: eight independent chains (measured faster on GB300 than
@@ -1439,11 +1504,10 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
     const double l2e = 1.4426950408889634;
     const double kk = biased ? 1.0 / (2.0 * l2e) : (double)a.scale / (double)kp.softcap;
     const double C = (double)kp.softcap * l2e;
-    const double r[4] = {ATTN_TANH_POLY_R0, ATTN_TANH_POLY_R1, ATTN_TANH_POLY_R2,
-                         ATTN_TANH_POLY_R3};
+    const double r[3] = {ATTN_TANH_POLY_R0, ATTN_TANH_POLY_R1, ATTN_TANH_POLY_R2};
     double kpow = kk;
     bool normal = true;
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < 3; ++i) {
       kp.tq[i] = (float)(C * r[i] * kpow);
       normal = normal && fabsf(kp.tq[i]) >= FLT_MIN && isfinite(kp.tq[i]);
       kpow *= kk * kk;

@@ -95,6 +95,11 @@ SMALL = [
     (1, 4, 4, 600, 600, 128, {"causal": True, "alibi": True}),
     (1, 2, 2, 520, 520, 64, {"alibi": True, "softcap": 2.0}),
     (1, 2, 2, 384, 384, 128, {"causal": True, "q_offset": -100}),  # rows with no key
+    # soft cap on band masks: a warp's 32-column chunks of a partial tile are
+    # hidden, mixed or visible, at offsets that are not multiples of 32
+    (1, 2, 2, 900, 900, 128, {"window": 300, "softcap": 30.0}),
+    (1, 2, 1, 700, 760, 64, {"window": 129, "softcap": 10.0, "q_offset": 37}),
+    (1, 2, 2, 520, 520, 128, {"window": 1, "softcap": 30.0}),  # one key per row
 ]
 
 
@@ -135,6 +140,7 @@ def test_unsorted_document_ids(attn):
     assert attn.decode_block_mask(bm)["docs_sorted"] == 0  # element-wise equality path
     run_and_compare(attn, q, k, v, 0.125, doc_ids=doc_ids)
     run_and_compare(attn, q, k, v, 0.125, doc_ids=doc_ids, causal=True)
+    run_and_compare(attn, q, k, v, 0.125, doc_ids=doc_ids, causal=True, softcap=30.0)
 
 
 def test_document_order_flag_across_blocks(attn):

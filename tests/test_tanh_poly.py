@@ -20,8 +20,8 @@ f32 = np.float32
 def header():
     text = open(os.path.join(CSRC, "tanh_poly.h")).read()
     r = [float.fromhex(re.search(r"ATTN_TANH_POLY_R%d (\S+)" % i, text).group(1))
-         for i in range(4)]
-    assert "ATTN_TANH_POLY_R4" not in text
+         for i in range(3)]
+    assert "ATTN_TANH_POLY_R3" not in text
     u0 = float(re.search(r"ATTN_TANH_POLY_U0 (\S+)", text).group(1))
     err = float(re.search(r"ATTN_TANH_POLY_MAX_ABS_ERR (\S+)", text).group(1))
     return r, u0, err
@@ -33,7 +33,7 @@ def host_coefficients(scale, cap, biased):
     r, u0, _ = header()
     kk = 1.0 / (2.0 * L2E) if biased else scale / cap
     C = cap * L2E
-    tq = [f32(C * r[i] * kk ** (2 * i + 1)) for i in range(4)]
+    tq = [f32(C * r[i] * kk ** (2 * i + 1)) for i in range(3)]
     return tq, f32(u0 / kk), kk
 
 
@@ -42,9 +42,8 @@ def kernel_eval(v, tq):
     v = np.asarray(v, dtype=f32)
     with np.errstate(invalid="ignore", over="ignore"):
         w = (v.astype(np.float64) * v).astype(f32)
-        q = (w.astype(np.float64) * tq[3] + np.float64(tq[2])).astype(f32)
-        for c in (tq[1], tq[0]):
-            q = (q.astype(np.float64) * w + np.float64(c)).astype(f32)
+        q = (w.astype(np.float64) * tq[2] + np.float64(tq[1])).astype(f32)
+        q = (q.astype(np.float64) * w + np.float64(tq[0])).astype(f32)
         return (v.astype(np.float64) * q).astype(f32)
 
 
@@ -63,7 +62,7 @@ def test_relative_error_of_the_fit_on_the_range():
     u = np.linspace(-u0, u0, 400001)
     p = u * np.polyval(np.asarray(r)[::-1], u * u)
     rel = np.abs(p - np.tanh(u)) / np.maximum(np.abs(np.tanh(u)), 1e-300)
-    assert rel[np.abs(u) > 1e-6].max() <= 6e-7
+    assert rel[np.abs(u) > 1e-6].max() <= 7e-6
 
 
 @pytest.mark.parametrize("scale,cap,biased", [(1 / np.sqrt(128), 30.0, False),
@@ -76,9 +75,10 @@ def test_scaled_evaluation_matches_the_soft_cap(scale, cap, biased):
     v = np.linspace(-float(tlim), float(tlim), 200001).astype(f32)
     got = kernel_eval(v, tq).astype(np.float64)
     want = cap * L2E * np.tanh(kk * v.astype(np.float64))
-    # a score error far below the fp32 rounding of ordinary scores: the
-    # polynomial's 1.2e-7 in tanh times cap log2(e), plus float32 rounding
-    assert np.abs(got - want).max() <= 4e-7 * cap * L2E + 2e-7 * np.abs(want).max()
+    # the polynomial's 2.4e-6 in tanh times cap log2(e), plus float32
+    # rounding: at cap 30 about 1e-4 of an exponent, far below the bf16
+    # rounding of P (2^-9 relative)
+    assert np.abs(got - want).max() <= 2.6e-6 * cap * L2E + 2e-7 * np.abs(want).max()
 
 
 def test_masked_scores_give_minus_infinity():
