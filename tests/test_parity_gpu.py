@@ -100,6 +100,10 @@ SMALL = [
     (1, 2, 2, 900, 900, 128, {"window": 300, "softcap": 30.0}),
     (1, 2, 1, 700, 760, 64, {"window": 129, "softcap": 10.0, "q_offset": 37}),
     (1, 2, 2, 520, 520, 128, {"window": 1, "softcap": 30.0}),  # one key per row
+    # larger caps (Gemma-style 50) and a cap just below 35
+    (1, 2, 2, 640, 640, 128, {"causal": True, "softcap": 50.0}),
+    (1, 2, 2, 520, 520, 64, {"window": 200, "alibi": True, "softcap": 50.0}),
+    (1, 2, 2, 600, 600, 128, {"window": 333, "softcap": 34.0}),
 ]
 
 
