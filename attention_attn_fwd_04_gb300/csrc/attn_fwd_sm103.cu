@@ -263,6 +263,13 @@ __device__ __forceinline__ int item_of(int r) {
   const int c = PAIR ? (int)ptx::cluster_id_x() : (int)blockIdx.x;
   return r * G + ((r & 1) ? (G - 1 - c) : c);
 }
+// Rounds of the snake schedule that hold an item for this CTA (or pair).
+template <bool PAIR>
+__device__ __forceinline__ int rounds_of(int n_items) {
+  const int G = PAIR ? (int)ptx::cluster_count_x() : (int)gridDim.x;
+  const int full = n_items / G;
+  return full + (item_of<PAIR>(full) < n_items ? 1 : 0);
+}
 
 // Descriptor bits that do not depend on the start address: K-major tiles
 // (Q, K) and the MN-major V tile.  A full descriptor is this constant plus
@@ -353,6 +360,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   }
   const int uniform = hdr->uniform;
   const int docs_sorted = hdr->docs_sorted;
+  // The r-th item of this CTA.  The soft-cap variant takes its items in
+  // reverse when their work differs: with a sliding window nearly every item
+  // has the same length, so in schedule order all CTAs reach their item
+  // boundaries (and the O stores there) together; starting the CTAs whose
+  // last item is short with that item staggers them (window 1024 + soft cap
+  // +1.3%).  The other variants keep the schedule order: the same change cost
+  // them 1-2% through the code of their item loop alone.
+  int n_rev = 0;
+  if constexpr (SOFTCAP) n_rev = uniform ? 0 : rounds_of<PAIR>(p.n_items);
+  auto my_item = [&](int r) {
+    if constexpr (SOFTCAP) {
+      if (n_rev > 0) return r < n_rev ? item_of<PAIR>(n_rev - 1 - r) : p.n_items;
+    }
+    return item_of<PAIR>(r);
+  };
 
   // ---- CTA pair --------------------------------------------------------
   // rank 0 issues every MMA of the pair; the work units of the persistent
@@ -436,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       uint32_t kv_cnt = 0;
       bool ok = true;
       for (int r = 0; ok; ++r) {
-        const int w = item_of<PAIR>(r);
+        const int w = my_item(r);
         if (w >= p.n_items) break;
         const Item it = decode_item<kHalves>(p, w, uniform);
         const int n = p.cnt[it.e];
@@ -507,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       bool ok = true;
       int q_phase[2] = {-1, -1};  // parity of the last Q_t load issued
       for (int r = 0; ok; ++r) {
-        const int w = item_of<PAIR>(r);
+        const int w = my_item(r);
         if (w >= p.n_items) break;
         const Item it = decode_item<kHalves>(p, w, uniform);
         if (p.cnt[it.e] == 0) continue;
@@ -628,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       int act = 0;
       bool ok = true;
       for (int r = 0; ok; ++r) {
-        const int w = item_of<PAIR>(r);
+        const int w = my_item(r);
         if (w >= p.n_items) break;
         const Item it = decode_item<kHalves>(p, w, uniform);
         const int n = p.cnt[it.e];
@@ -717,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     int act = 0;
     bool ok = true;
     for (int r = 0; ok; ++r) {
-      const int w = item_of<PAIR>(r);
+      const int w = my_item(r);
       if (w >= p.n_items) break;
       const Item it = decode_item<kHalves>(p, w, uniform);
       const int n = p.cnt[it.e];
