@@ -94,6 +94,8 @@ enum Site : int {
   kSiteMmaDebugStall = 26,
   kSiteSmxSFull = 30,
   kSiteSmxOFull = 31,
+  kSiteLoadOstFull = 12,
+  kSiteSmxOstEmpty = 34,
 };
 
 // PAIR: the CTA is one of a pair (a cluster of two) whose MMAs span both
@@ -101,26 +103,34 @@ enum Site : int {
 // half of every key / value tile: keys [64 r, 64 r + 64) of a K tile and
 // columns [64 r, 64 r + 64) of a V tile for the CTA of rank r, 16 KB either
 // way, so a ring stage holds 16 KB instead of a whole 32 KB tile.
-template <int D, bool PAIR = false>
+// OST: the epilogue stages each O tile in shared memory for a TMA store.
+template <int D, bool PAIR = false, bool OST = false>
 struct Cfg {
   static_assert(!PAIR || D == 128, "the CTA-pair forward is built for D = 128");
+  static_assert(!(PAIR && OST), "the staged O store is a one-CTA form");
   static constexpr int kHalfBytes = kTileM * 64 * 2;  // 128 rows x 64 bf16, 128-byte swizzle
   static constexpr int kHalves = D / 64;
   static constexpr int kTileBytes = kHalves * kHalfBytes;
   static constexpr int kKPartHalfBytes = 64 * 64 * 2;  // PAIR: 64 keys x 64 columns of K
+  static_assert(kKPartHalfBytes % 1024 == 0, "half-tile alignment");
   static constexpr int kStageBytes = PAIR ? kTileBytes / 2 : kTileBytes;
   static constexpr int kStages = PAIR ? 8 : ((D == 128) ? 4 : 8);
   static constexpr int kOCol = 256;  // O_t at column 256 + t * D; S_t at t * 128
   static constexpr int kSmemQ = 0;
   static constexpr int kSmemKV = kSmemQ + 2 * kTileBytes;
-  static constexpr int kSmemBar = kSmemKV + kStages * kStageBytes;
+  // O staging for the epilogue's TMA store (one tile, OST only)
+  static constexpr int kSmemOst = kSmemKV + kStages * kStageBytes;
+  static constexpr int kSmemBar = kSmemOst + (OST ? kTileBytes : 0);
   // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_full[2]
-  //           o_full[2] o_empty[2] drain never (the test hook's)
-  static constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 2 + 2 + 2 + 1 + 1;
+  //           o_full[2] o_empty[2] drain never (the test hook's); OST:
+  //           staged_full staged_empty
+  static constexpr int kNumBars =
+      2 + 2 + kStages + kStages + 2 + 2 + 2 + 2 + 1 + 1 + (OST ? 2 : 0);
   static constexpr int kSmemMisc = kSmemBar + 8 * kNumBars;
   static constexpr int kSmemDoc = (kSmemMisc + 16 + 15) / 16 * 16;  // int sdoc[2][128]
   static constexpr int kSmemBytes = kSmemDoc + 2 * kTileN * 4;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;  // slack for 1024-byte alignment
+  static_assert(kSmemAlloc <= 227 * 1024, "shared memory per CTA");
 };
 
 
@@ -163,6 +173,7 @@ struct KParams {
   float tq[3];
   float tlim;
   float ty;
+  CUtensorMap tmap_o;  // O, for the staged epilogue's TMA store
 };
 
 struct Ctl {
@@ -323,7 +334,12 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint6
 template <int D, bool ALIBI, bool SOFTCAP, bool PAIR, bool QUAD>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ KParams p) {
   static_assert(!PAIR || QUAD, "a CTA pair works on four-tile entries");
-  using C = Cfg<D, PAIR>;
+  // The one-CTA soft-cap form stages O in shared memory and the Q loader
+  // warp stores it with TMA: with a sliding window every CTA reaches its
+  // item boundaries at about the same time, and the softmax warps no
+  // longer wait there while the O stores of all CTAs drain.
+  constexpr bool kOst = SOFTCAP && !PAIR;
+  using C = Cfg<D, PAIR, kOst>;
   constexpr int kTpe = QUAD ? kTilesPerQuad : kTilesPerItem;  // query tiles per entry
   constexpr bool kHalves = QUAD && !PAIR;
   extern __shared__ uint8_t smem_raw[];
@@ -389,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   auto bar = [&](int i) { return sbase + (uint32_t)(C::kSmemBar + 8 * i); };
   const int B_QF = 0, B_QE = 2, B_KVF = 4, B_KVE = 4 + C::kStages, B_SF = 4 + 2 * C::kStages,
             B_PF = B_SF + 2, B_OF = B_PF + 2, B_OE = B_OF + 2, B_DRAIN = B_OE + 2,
-            B_NEVER = B_DRAIN + 1;
+            B_NEVER = B_DRAIN + 1, B_OSTF = B_NEVER + 1, B_OSTE = B_NEVER + 2;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kSmemMisc);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::kSmemMisc + 4);
   volatile int* s_turn = reinterpret_cast<volatile int*>(smem + C::kSmemMisc + 8);
@@ -414,6 +430,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     ptx::mbar_init(bar(B_DRAIN), 2);
     ptx::mbar_init(bar(B_NEVER), 1);
+    if constexpr (kOst) {
+      ptx::mbar_init(bar(B_OSTF), 4);  // staged O tile full: one arrival per softmax warp
+      ptx::mbar_init(bar(B_OSTE), 1);  // staged O tile read by its TMA store
+    }
     *s_abort = 0;
     *s_turn = 0;
     ptx::fence_mbar_init();
@@ -524,10 +544,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       // PAIR: each CTA loads its own query tiles; the copies complete on
       // rank 0's barrier, armed by rank 0 for both CTAs' bytes.
       ptx::prefetch_tmap(&p.tmap_q);
+      if constexpr (kOst) ptx::prefetch_tmap(&p.tmap_o);
       const uint64_t pol_q = ptx::policy_evict_first();
       int act = 0;
       bool ok = true;
       int q_phase[2] = {-1, -1};  // parity of the last Q_t load issued
+      // OST: this thread also stores the O tiles the softmax warpgroups stage
+      // in shared memory, one item behind its Q loads (tile 0, then tile 1
+      // of each item: the order in which the staging buffer is handed over).
+      int prev_row0[2] = {0, 0}, prev_bh = 0;
+      auto store_o = [&](int a) -> bool {
+        for (int t = 0; t < 2; ++t) {
+          const int e = 2 * a + t;
+          if (!wait_bar<PAIR>(bar(B_OSTF), (uint32_t)(e & 1), ctl, kSiteLoadOstFull)) return false;
+          if (prev_row0[t] < p.S_q) {  // a tile wholly past S_q has nothing to store
+#pragma unroll
+            for (int hx = 0; hx < C::kHalves; ++hx)
+              ptx::tma_store_3d(&p.tmap_o, sbase + C::kSmemOst + hx * C::kHalfBytes, hx * 64,
+                                prev_row0[t], prev_bh);
+          }
+          ptx::bulk_commit_group();
+          ptx::bulk_wait_group_read0();
+          ptx::mbar_arrive(bar(B_OSTE));
+        }
+        return true;
+      };
       for (int r = 0; ok; ++r) {
         const int w = my_item(r);
         if (w >= p.n_items) break;
@@ -554,7 +595,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           }
           q_phase[t] = act & 1;
         }
+        if constexpr (kOst) {
+          if (ok && act > 0) ok = store_o(act - 1);
+          for (int t = 0; t < 2; ++t) prev_row0[t] = (it.pair * kTpe + ci(it, t)) * kTileM;
+          prev_bh = it.b * p.H + it.h;
+        }
         ++act;
+      }
+      if constexpr (kOst) {
+        if (ok && act > 0) ok = store_o(act - 1);
+        ptx::bulk_wait_group0();  // every O store has landed before the CTA exits
       }
       if (!ok) {
         if (PAIR && rank != 0) {
@@ -1308,6 +1358,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) arrive(B_OE + t);
+        if constexpr (kOst) {
+          // Stage the row for the Q loader's TMA store: 128-byte rows in each
+          // 64-column half, 16-byte chunks swizzled by the row (the tensor
+          // map's 128-byte swizzle), so the warp's stores spread over all
+          // banks.  Rows past S_q are staged too; the store clips them.  The
+          // buffer alternates between the tiles: epilogue e waits until
+          // epilogue e - 1's store has read it.
+          const int e = 2 * act + t;
+          if (e > 0) {
+            const bool got = wait_bar<PAIR>(bar(B_OSTE), (uint32_t)((e - 1) & 1), ctl,
+                                            kSiteSmxOstEmpty);
+            ok = __all_sync(0xffffffffu, got);
+            if (!ok) break;
+          }
+          const uint32_t srow = sbase + C::kSmemOst + (uint32_t)(row * 128);
+#pragma unroll
+          for (int c4 = 0; c4 < D / 32; ++c4) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+              pk[c] = ptx::pack_bf16x2(__uint_as_float(o[c4][2 * c]) * inv_l,
+                                       __uint_as_float(o[c4][2 * c + 1]) * inv_l);
+            const uint32_t half = srow + (uint32_t)((c4 / 2) * C::kHalfBytes);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              const int j = (c4 % 2) * 4 + cc;  // 16-byte chunk of the 128-byte row
+              ptx::sts_v4(half + (uint32_t)((j ^ (row & 7)) * 16), pk[4 * cc], pk[4 * cc + 1],
+                          pk[4 * cc + 2], pk[4 * cc + 3]);
+            }
+          }
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bar(B_OSTF));
+        } else {
         const bool out32 = (reinterpret_cast<uintptr_t>(p.out) & 31u) == 0;
         if (valid) {
 #pragma unroll
@@ -1327,6 +1411,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
             }
           }
+        }
         }
       }
       if (valid && p.lse) p.lse[row_id] = seen ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
@@ -1407,13 +1492,13 @@ cudaError_t launch_variant(const KParams& kp, int grid, cudaStream_t stream, int
   cudaError_t err = cudaSuccess;
   if (!cache || !attr_set[dev].load(std::memory_order_relaxed)) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               Cfg<D, PAIR>::kSmemAlloc);
+                               Cfg<D, PAIR, SOFTCAP && !PAIR>::kSmemAlloc);
     if (err != cudaSuccess) return err;
     if (cache) attr_set[dev].store(true, std::memory_order_relaxed);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<D, PAIR>::kSmemAlloc;
+  cfg.dynamicSmemBytes = Cfg<D, PAIR, SOFTCAP && !PAIR>::kSmemAlloc;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1476,7 +1561,9 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
   if (!make_map(&kp.tmap_q, a.q, a.D, a.S_q, a.B * a.H) ||
       !make_map(&kp.tmap_k, a.k, a.D, a.S_k, a.B * a.H_kv) ||
       !make_map(&kp.tmap_v, a.v, a.D, a.S_k, a.B * a.H_kv) ||
-      (pair && !make_map(&kp.tmap_kh, a.k, a.D, a.S_k, a.B * a.H_kv, kTileN / 2)))
+      (pair && !make_map(&kp.tmap_kh, a.k, a.D, a.S_k, a.B * a.H_kv, kTileN / 2)) ||
+      (!pair && (a.score_flags & ATTN_SCORE_SOFTCAP) &&
+       !make_map(&kp.tmap_o, a.out, a.D, a.S_q, a.B * a.H)))
     return cudaErrorInvalidValue;
   BlockMaskGeom g = block_mask_geom(a.B, a.S_q, a.S_k, a.mask.flags, a.tpe);
   kp.out = reinterpret_cast<__nv_bfloat16*>(a.out);
