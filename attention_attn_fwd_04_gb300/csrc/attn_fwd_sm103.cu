@@ -334,11 +334,12 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem_o, uint32_t tmem_p, uint6
 template <int D, bool ALIBI, bool SOFTCAP, bool PAIR, bool QUAD>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ KParams p) {
   static_assert(!PAIR || QUAD, "a CTA pair works on four-tile entries");
-  // The one-CTA soft-cap form stages O in shared memory and the Q loader
-  // warp stores it with TMA: with a sliding window every CTA reaches its
-  // item boundaries at about the same time, and the softmax warps no
-  // longer wait there while the O stores of all CTAs drain.
-  constexpr bool kOst = SOFTCAP && !PAIR;
+  // The one-CTA soft-cap and position-bias forms stage O in shared memory
+  // and the Q loader warp stores it with TMA, so their softmax warps do not
+  // wait at item boundaries while the O stores drain (with a sliding window
+  // every CTA reaches them at about the same time; documents have short
+  // items).  The plain form keeps direct stores: its items are long.
+  constexpr bool kOst = (SOFTCAP || ALIBI) && !PAIR;
   using C = Cfg<D, PAIR, kOst>;
   constexpr int kTpe = QUAD ? kTilesPerQuad : kTilesPerItem;  // query tiles per entry
   constexpr bool kHalves = QUAD && !PAIR;
@@ -1492,13 +1493,13 @@ cudaError_t launch_variant(const KParams& kp, int grid, cudaStream_t stream, int
   cudaError_t err = cudaSuccess;
   if (!cache || !attr_set[dev].load(std::memory_order_relaxed)) {
     err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               Cfg<D, PAIR, SOFTCAP && !PAIR>::kSmemAlloc);
+                               Cfg<D, PAIR, (SOFTCAP || ALIBI) && !PAIR>::kSmemAlloc);
     if (err != cudaSuccess) return err;
     if (cache) attr_set[dev].store(true, std::memory_order_relaxed);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<D, PAIR, SOFTCAP && !PAIR>::kSmemAlloc;
+  cfg.dynamicSmemBytes = Cfg<D, PAIR, (SOFTCAP || ALIBI) && !PAIR>::kSmemAlloc;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1562,7 +1563,7 @@ cudaError_t launch_attn_fwd(const FwdArgs& a, cudaStream_t stream) {
       !make_map(&kp.tmap_k, a.k, a.D, a.S_k, a.B * a.H_kv) ||
       !make_map(&kp.tmap_v, a.v, a.D, a.S_k, a.B * a.H_kv) ||
       (pair && !make_map(&kp.tmap_kh, a.k, a.D, a.S_k, a.B * a.H_kv, kTileN / 2)) ||
-      (!pair && (a.score_flags & ATTN_SCORE_SOFTCAP) &&
+      (!pair && (a.score_flags & (ATTN_SCORE_SOFTCAP | ATTN_SCORE_ALIBI | ATTN_SCORE_RELBIAS)) &&
        !make_map(&kp.tmap_o, a.out, a.D, a.S_q, a.B * a.H)))
     return cudaErrorInvalidValue;
   BlockMaskGeom g = block_mask_geom(a.B, a.S_q, a.S_k, a.mask.flags, a.tpe);
