@@ -85,6 +85,7 @@ enum Site : int {
   kSiteHeader = 1,
   kSiteLoadQEmpty = 10,
   kSiteLoadKvEmpty = 11,
+  kSiteLoadOstFull = 12,
   kSiteMmaQFull = 20,
   kSiteMmaKvFull = 21,
   kSiteMmaPFull = 22,
@@ -94,7 +95,6 @@ enum Site : int {
   kSiteMmaDebugStall = 26,
   kSiteSmxSFull = 30,
   kSiteSmxOFull = 31,
-  kSiteLoadOstFull = 12,
   kSiteSmxOstEmpty = 34,
 };
 
