@@ -104,6 +104,11 @@ SMALL = [
     (1, 2, 2, 640, 640, 128, {"causal": True, "softcap": 50.0}),
     (1, 2, 2, 520, 520, 64, {"window": 200, "alibi": True, "softcap": 50.0}),
     (1, 2, 2, 600, 600, 128, {"window": 333, "softcap": 34.0}),
+    # whole query tiles without a visible key (items with no key tile) in the
+    # variants whose O goes out through a staged TMA store, and a ragged S_q
+    (1, 2, 2, 520, 520, 128, {"causal": True, "q_offset": -300, "alibi": True}),
+    (1, 2, 2, 520, 520, 64, {"causal": True, "q_offset": -300, "softcap": 30.0}),
+    (2, 3, 1, 333, 400, 128, {"window": 150, "softcap": 20.0, "alibi": True}),
 ]
 
 
