@@ -417,41 +417,48 @@ def test_mismatched_block_mask_is_reported(attn):
     assert attn.get_device_status(device=DEV) == 0       # cleared
 
 
-def test_wait_timeout_is_reported_and_context_survives(attn):
+@pytest.mark.parametrize("mods", [{"causal": True}, {"causal": True, "softcap": 30.0},
+                                  {"causal": True, "alibi": True}])
+def test_wait_timeout_is_reported_and_context_survives(attn, mods):
     # The test hook makes the MMA issuers wait on a barrier nothing arrives
     # on: the bounded wait must run out, the kernel must record
     # ATTN_ERR_TIMEOUT and return (no trap, no hang), and the next call on
-    # the same context must be correct.
+    # the same context must be correct.  The soft-cap and ALiBi variants
+    # also drain their staged O stores on the way out.
     B, H, S, D = 1, 2, 512, 128
     q, k, v = rand_inputs(B, H, H, S, S, D, seed=16)
     old_budget = attn.get_option("wait_budget_ms")
     try:
         attn.set_option("wait_budget_ms", 20)
         attn.set_option("debug_stall", 1)
-        attn.attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), causal=True)
+        attn.attn_fwd(q.to(DEV), k.to(DEV), v.to(DEV), **mods)
         assert attn.get_device_status(device=DEV) == 4  # ATTN_ERR_TIMEOUT
     finally:
         attn.set_option("debug_stall", 0)
         attn.set_option("wait_budget_ms", old_budget)
     assert attn.get_device_status(device=DEV) == 0
-    run_and_compare(attn, q, k, v, 1 / math.sqrt(D), causal=True)
+    run_and_compare(attn, q, k, v, 1 / math.sqrt(D), **mods)
 
 
 @pytest.mark.parametrize("D", [128, 64])
-def test_output_aligned_to_16_bytes_only(attn, D):
+@pytest.mark.parametrize("mods", [{"causal": True}, {"causal": True, "softcap": 30.0},
+                                  {"causal": True, "alibi": True}])
+def test_output_aligned_to_16_bytes_only(attn, D, mods):
     # out 16- but not 32-byte aligned takes the epilogue's 16-byte stores
-    # (32-byte aligned outputs take 32-byte stores): identical results
+    # (32-byte aligned outputs take 32-byte stores; the soft-cap and ALiBi
+    # variants store through a tensor map on the same base): identical
+    # results
     B, H, S = 1, 2, 700
     q, k, v = rand_inputs(B, H, H, S, S, D, seed=31)
     qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
-    o_ref, l_ref = attn.attn_fwd(qd, kd, vd, causal=True)
+    o_ref, l_ref = attn.attn_fwd(qd, kd, vd, **mods)
     assert o_ref.data_ptr() % 32 == 0
     n = o_ref.numel()
     flat = torch.empty(n + 16, dtype=torch.bfloat16, device=DEV)
     out = flat[8:8 + n].view(B, H, S, D)
     assert out.data_ptr() % 32 == 16
     lse = torch.empty_like(l_ref)
-    attn.attn_fwd_into(qd, kd, vd, out, lse, causal=True)
+    attn.attn_fwd_into(qd, kd, vd, out, lse, **mods)
     assert attn.get_device_status(device=DEV) == 0
     assert torch.equal(out, o_ref) and torch.equal(lse, l_ref)
 
